@@ -1,0 +1,350 @@
+"""Pins of the CPU oracle to facts fixed outside the oracle itself.
+
+Each ``pin_*`` takes a loaded oracle library and raises AssertionError when
+the oracle disagrees with: exact integer or rational arithmetic (brute force
+with Python integers and fractions), an independent library routine (NumPy
+float32 arithmetic, torch's CPU bf16 cast, torch.optim.SGD), values worked
+out by hand, or invariants of the collectives.  ``test_oracle_pins`` runs
+them on the oracle; ``test_oracle_mutants`` runs them on copies of the
+oracle with planted mistakes and requires each copy to fail at least one.
+"""
+from __future__ import annotations
+
+import math
+from fractions import Fraction
+
+import numpy as np
+
+import oracle
+from oracle import BF16, F32, MEAN, SUM  # noqa: F401
+
+SIZES = (0, 1, 2, 3, 5, 8, 17, 33)
+
+
+def round_to_f32(q: Fraction) -> float:
+    """The fp32 nearest to the rational q, ties to even (normal range)."""
+    if q == 0:
+        return 0.0
+    neg, a, e = q < 0, abs(q), 0
+    while a >= 2 ** 24:
+        a /= 2
+        e += 1
+    while a < 2 ** 23:
+        a *= 2
+        e -= 1
+    m = math.floor(a)
+    rem = a - m
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and m % 2 == 1):
+        m += 1
+    v = math.ldexp(float(m), e)
+    return -v if neg else v
+
+
+def f32(v) -> np.ndarray:
+    return np.asarray(v, dtype=np.float32)
+
+
+def bits(a: np.ndarray) -> np.ndarray:
+    return np.ascontiguousarray(a).view(np.uint32 if a.dtype == np.float32 else np.uint16)
+
+
+# ------------------------------------------------------------ all-reduce
+
+def pin_sum_integers_exact(L):
+    """Integer-valued inputs whose sums stay below 2**24: every order gives
+    the exact integer sum, so the oracle must return it, on every replica."""
+    rng = np.random.default_rng(1)
+    for P in range(1, 9):
+        for n in SIZES:
+            xs = [f32(rng.integers(-(1 << 20), 1 << 20, n)) for _ in range(P)]
+            out = oracle.all_reduce(xs, op=SUM, L=L)
+            want = np.sum([x.astype(np.int64) for x in xs], axis=0) if n else np.zeros(0)
+            for r in range(P):
+                assert np.array_equal(out[r].astype(np.int64), want), (P, n, r)
+
+
+def pin_mean_rational_exact(L):
+    """Mean of integer-valued inputs is the exact sum (Python ints) divided by
+    P and rounded once to fp32: brute force with fractions."""
+    rng = np.random.default_rng(2)
+    for P in range(1, 9):
+        for n in SIZES:
+            xs = [f32(rng.integers(-(1 << 20), 1 << 20, n)) for _ in range(P)]
+            out = oracle.all_reduce(xs, op=MEAN, L=L)
+            for i in range(n):
+                s = sum(int(x[i]) for x in xs)
+                want = np.float32(round_to_f32(Fraction(s, P)))
+                for r in range(P):
+                    assert bits(out[r][i:i + 1])[0] == bits(f32([want]))[0], (P, n, i, r)
+
+
+def pin_rank_order(L):
+    """Order-sensitive sums worked out by hand in fp32 (the ulp of 1e8 is 8,
+    of 2**24 is 2): only ascending rank order gives these values."""
+    cases = [
+        ([1e8, 1.0, -1e8, 1.0], 1.0),          # ((1e8+1)=1e8, -1e8 -> 0, +1) = 1
+        ([1.0, 1e8, -1e8], 0.0),               # (1+1e8)=1e8, -1e8 -> 0
+        ([2.0 ** 24, 1.0, 1.0], 2.0 ** 24),    # each +1 ties back to even 2**24
+        ([1.0, 1.0, 2.0 ** 24], 2.0 ** 24 + 2),
+        ([3.0, 2.0 ** 24, 2.0 ** 24], 2.0 ** 25 + 4),  # 3+2**24 -> 2**24+4 (tie to even)
+    ]
+    for vals, want in cases:
+        xs = [f32([v]) for v in vals]
+        out = oracle.all_reduce(xs, op=SUM, L=L)
+        assert float(out[0][0]) == want, (vals, float(out[0][0]), want)
+
+
+def pin_signed_zero(L):
+    """A sum of one term is that term: -0.0 survives when every replica is
+    -0.0; +0.0 + -0.0 is +0.0 under round-to-nearest."""
+    for P in (1, 2, 3, 8):
+        for op in (SUM, MEAN):
+            out = oracle.all_reduce([f32([-0.0]) for _ in range(P)], op=op, L=L)
+            assert bits(out[0])[0] == 0x80000000, (P, op)
+    out = oracle.all_reduce([f32([0.0]), f32([-0.0])], op=SUM, L=L)
+    assert bits(out[0])[0] == 0
+
+
+def numpy_all_reduce(xs, op):
+    """Independent route: NumPy float32 elementwise adds in rank order."""
+    acc = xs[0].astype(np.float32).copy()
+    for x in xs[1:]:
+        acc = np.add(acc, x, dtype=np.float32)
+    if op == MEAN:
+        acc = np.divide(acc, np.float32(len(xs)), dtype=np.float32)
+    return acc
+
+
+def pin_matches_numpy_f32(L):
+    """Random fp32 inputs (U(-1,1), N(0,1), mixed magnitudes): bit-exact with
+    NumPy's float32 add/divide taken in rank order."""
+    rng = np.random.default_rng(3)
+    for P in (1, 2, 3, 4, 5, 7, 8, 16):
+        n = 4099
+        xs = [f32(rng.uniform(-1, 1, n) * 10.0 ** rng.integers(-30, 30, n)) for _ in range(P)]
+        for op in (SUM, MEAN):
+            out = oracle.all_reduce(xs, op=op, L=L)
+            want = numpy_all_reduce(xs, op)
+            for r in range(P):
+                assert np.array_equal(bits(out[r]), bits(want)), (P, op, r)
+
+
+def _torch_bf16_bits(x: np.ndarray) -> np.ndarray:
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16) \
+        .view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_probe_values() -> np.ndarray:
+    """Every upper half (all signs, exponents and kept significands) combined
+    with the lower halves that decide rounding: 0, just below, at and above
+    one half, odd and even kept parts, all ones; NaNs removed."""
+    hi = np.arange(1 << 16, dtype=np.uint32) << 16
+    lows = np.array([0x0000, 0x0001, 0x3FFF, 0x7FFF, 0x8000, 0x8001, 0xC000, 0xFFFF], np.uint32)
+    u = (hi[:, None] | lows[None, :]).ravel()
+    f = u.view(np.float32)
+    return f[~np.isnan(f)]
+
+
+def pin_bf16_round_matches_torch(L):
+    """fp32 -> bf16 round-to-nearest-even against torch's CPU cast, on the
+    probe set (all 2**16 upper halves x the deciding lower halves)."""
+    f = bf16_probe_values()
+    want = _torch_bf16_bits(f)
+    got = oracle.f32_to_bf16(f, L=L)
+    assert np.array_equal(got, want), hex(int(f.view(np.uint32)[np.flatnonzero(got != want)[0]]))
+
+
+def pin_bf16_widen_matches_torch(L):
+    """bf16 -> fp32 is exact: compare with torch's CPU widening for every
+    non-NaN bf16 pattern."""
+    import torch
+    h = np.arange(1 << 16, dtype=np.uint16)
+    want = torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).float().numpy()
+    keep = ~np.isnan(want)
+    got = np.array([L.oracle_bf16_to_f32(int(v)) for v in h[keep][::5]], dtype=np.float32)
+    assert np.array_equal(bits(got), bits(want[keep][::5]))
+
+
+def pin_bf16_all_reduce(L):
+    """bf16 all-reduce = exact widening, NumPy fp32 rank-order sum (and
+    divide), one torch RNE cast at the end; bit-exact."""
+    rng = np.random.default_rng(4)
+    for P in (1, 2, 3, 4, 8):
+        n = 1031
+        xs32 = [f32(rng.normal(0, 1, n) * 10.0 ** rng.integers(-3, 3, n)) for _ in range(P)]
+        xs = [_torch_bf16_bits(x) for x in xs32]                 # bf16 inputs
+        wide = [(x.astype(np.uint32) << 16).view(np.float32) for x in xs]
+        for op in (SUM, MEAN):
+            out = oracle.all_reduce(xs, op=op, L=L)
+            want = _torch_bf16_bits(numpy_all_reduce(wide, op))
+            for r in range(P):
+                assert np.array_equal(out[r], want), (P, op, r)
+
+
+# ----------------------------------------------- reduce-scatter / gather
+
+def pin_reduce_scatter_by_hand(L):
+    """P=2, N=4: rank 0 keeps elements 0..1 of the sum, rank 1 keeps 2..3."""
+    xs = [f32([1, 2, 3, 4]), f32([10, 20, 30, 40])]
+    out = oracle.reduce_scatter(xs, op=SUM, L=L)
+    assert out[0].tolist() == [11, 22] and out[1].tolist() == [33, 44]
+    out = oracle.reduce_scatter(xs, op=MEAN, L=L)
+    assert out[0].tolist() == [5.5, 11] and out[1].tolist() == [16.5, 22]
+
+
+def pin_all_gather_by_hand(L):
+    """P=3: every rank receives shard 0 ++ shard 1 ++ shard 2."""
+    xs = [f32([1, 2]), f32([3, 4]), f32([5, 6])]
+    out = oracle.all_gather(xs, L=L)
+    for r in range(3):
+        assert out[r].tolist() == [1, 2, 3, 4, 5, 6], r
+
+
+def pin_rs_then_ag_is_all_reduce(L):
+    """Invariant: all-gather(reduce-scatter(x)) == all-reduce(x), bit for bit
+    (the two halves of the ring all-reduce)."""
+    rng = np.random.default_rng(5)
+    for P in (1, 2, 4, 8):
+        for dt in ("f32", "bf16"):
+            n = 24 * P
+            xs = [f32(rng.normal(0, 1, n)) for _ in range(P)]
+            if dt == "bf16":
+                xs = [(x.view(np.uint32) >> 16).astype(np.uint16) for x in xs]
+            for op in (SUM, MEAN):
+                ar = oracle.all_reduce(xs, op=op, L=L)
+                ag = oracle.all_gather(oracle.reduce_scatter(xs, op=op, L=L), L=L)
+                for r in range(P):
+                    assert np.array_equal(ag[r], ar[r]), (P, dt, op, r)
+
+
+def pin_broadcast(L):
+    """After a broadcast every replica holds the root's bytes; the root is
+    unchanged."""
+    rng = np.random.default_rng(6)
+    for P in (1, 2, 5):
+        for root in range(P):
+            xs = [f32(rng.normal(0, 1, 9)) for _ in range(P)]
+            ref = xs[root].copy()
+            oracle.broadcast(xs, root=root, L=L)
+            for r in range(P):
+                assert np.array_equal(bits(xs[r]), bits(ref)), (P, root, r)
+
+
+def pin_in_place_all_reduce(L):
+    """In place (recv = send) gives the same bits as out of place."""
+    rng = np.random.default_rng(7)
+    xs = [f32(rng.normal(0, 1, 37)) for _ in range(4)]
+    want = oracle.all_reduce(xs, op=MEAN, L=L)
+    ys = [x.copy() for x in xs]
+    oracle.all_reduce(ys, recv=ys, op=MEAN, L=L)
+    for r in range(4):
+        assert np.array_equal(bits(ys[r]), bits(want[r]))
+
+
+# ---------------------------------------------------------- buckets, SGD
+
+def pin_bucket_equals_per_tensor(L):
+    """A bucket of several tensors reduces each exactly as its own
+    all-reduce would (the operation is elementwise)."""
+    rng = np.random.default_rng(8)
+    P, sizes = 4, (1, 7, 64, 1000, 3)
+    tensors = [[f32(rng.normal(0, 1, n)) for _ in range(P)] for n in sizes]
+    want = [oracle.all_reduce(reps, op=MEAN, L=L) for reps in tensors]
+    oracle.bucket_all_reduce(tensors, op=MEAN, L=L)
+    for t, reps in enumerate(tensors):
+        for r in range(P):
+            assert np.array_equal(bits(reps[r]), bits(want[t][r])), (t, r)
+
+
+def pin_sgd_closed_form(L):
+    """One replica (P=1) with gradient 1 and v = 0: the first step gives
+    v = 1 and w = w - fl(0.1f); the second v = fl(fl(0.9f * 1) + 1) and
+    w = w - fl(0.1f * v), worked out with NumPy float32 scalars."""
+    lr, mu = np.float32(0.1), np.float32(0.9)
+    g = [[f32([1.0, 1.0])]]
+    w, v = [f32([0.5, -2.0])], [f32([0.0, 0.0])]
+    w0 = w[0].copy()
+    oracle.bucket_all_reduce(g, op=SUM, sgd=(lr, mu, w, v, 0), L=L)
+    assert v[0].tolist() == [1.0, 1.0]
+    assert np.array_equal(w[0], w0 - lr)
+    v1 = np.float32(np.float32(mu * np.float32(1.0)) + np.float32(1.0))
+    w1 = w[0].copy()
+    oracle.bucket_all_reduce([[f32([1.0, 1.0])]], op=SUM, sgd=(lr, mu, w, v, 0), L=L)
+    assert np.array_equal(v[0], f32([v1, v1]))
+    assert np.array_equal(w[0], w1 - np.float32(lr * v1))
+
+
+def pin_sgd_matches_torch(L):
+    """Momentum SGD against torch.optim.SGD(lr=0.1, momentum=0.9) on CPU, fed
+    the same reduced gradient, one step at a time from a common state (torch
+    is reset to the oracle's w and v before each step, so differences do not
+    compound).  v must agree bit for bit (torch computes fl(fl(0.9 v) + g)
+    too); w within 2 ulp of max(|w|, |lr v|), since torch may fuse
+    w - lr*v into one rounding."""
+    import torch
+    rng = np.random.default_rng(9)
+    P, n = 4, 513
+    w = [f32(rng.normal(0, 0.02, n))]
+    v = [np.zeros(n, np.float32)]
+    for step in range(3):
+        reps = [f32(rng.normal(0, 1e-3, n)) for _ in range(P)]
+        g = numpy_all_reduce(reps, MEAN)
+        p = torch.nn.Parameter(torch.from_numpy(w[0].copy()))
+        opt = torch.optim.SGD([p], lr=0.1, momentum=0.9, foreach=False)
+        if step > 0:
+            opt.state[p]["momentum_buffer"] = torch.from_numpy(v[0].copy())
+        p.grad = torch.from_numpy(g.copy())
+        opt.step()
+        w_old = w[0].copy()
+        oracle.bucket_all_reduce([reps], op=MEAN, sgd=(0.1, 0.9, w, v, 1), L=L)
+        assert np.array_equal(bits(reps[0]), bits(g)), step      # write-back = reduced g
+        assert np.array_equal(bits(v[0]), bits(opt.state[p]["momentum_buffer"].numpy())), step
+        scale = np.maximum(np.abs(w_old), np.abs(np.float32(0.1) * v[0]))
+        err = np.abs(w[0].astype(np.float64) - p.detach().numpy().astype(np.float64))
+        assert np.all(err <= 2 * np.spacing(scale).astype(np.float64)), step
+
+
+def pin_sgd_write_back_flag(L):
+    """write_back=0 leaves the gradient replicas untouched; 1 overwrites them
+    with the reduced gradient."""
+    reps = [f32([1.0, 2.0]), f32([3.0, 4.0])]
+    w, v = [f32([0, 0])], [f32([0, 0])]
+    oracle.bucket_all_reduce([reps], op=MEAN, sgd=(0.1, 0.9, w, v, 0), L=L)
+    assert reps[0].tolist() == [1, 2] and reps[1].tolist() == [3, 4]
+    oracle.bucket_all_reduce([reps], op=MEAN, sgd=(0.1, 0.9, w, v, 1), L=L)
+    assert reps[0].tolist() == [2, 3] and reps[1].tolist() == [2, 3]
+
+
+def pin_bucket_plan(L):
+    """Hand cases of the reverse-order greedy fill with a cap of 10 bytes,
+    plus the rule's invariants on the ViT-B/16 gradient set."""
+    assert oracle.bucket_plan([4, 4, 4], 10, L=L) == [1, 0, 0]        # fill from the end
+    assert oracle.bucket_plan([3, 12, 3], 10, L=L) == [2, 1, 0]       # oversized: alone
+    assert oracle.bucket_plan([5, 5, 5, 5], 10, L=L) == [1, 1, 0, 0]  # exactly the cap fits
+    assert oracle.bucket_plan([], 10, L=L) == []
+    import workloads
+    nb = [2 * n for n in workloads.vit_b16_numels()]
+    cap = 25 << 20
+    plan = oracle.bucket_plan(nb, cap, L=L)
+    k = max(plan) + 1
+    assert plan[-1] == 0 and all(plan[t] >= plan[t + 1] for t in range(len(plan) - 1))
+    fill = [0] * k
+    for t, b in enumerate(plan):
+        fill[b] += nb[t]
+    for b in range(k):
+        members = [t for t in range(len(plan)) if plan[t] == b]
+        assert fill[b] <= cap or len(members) == 1
+        if b + 1 < k:  # greedy: the next tensor would not have fitted
+            nxt = max(t for t in range(len(plan)) if plan[t] == b + 1)
+            assert fill[b] + nb[nxt] > cap
+
+
+ALL_PINS = [
+    pin_sum_integers_exact, pin_mean_rational_exact, pin_rank_order, pin_signed_zero,
+    pin_matches_numpy_f32, pin_bf16_round_matches_torch, pin_bf16_widen_matches_torch,
+    pin_bf16_all_reduce, pin_reduce_scatter_by_hand, pin_all_gather_by_hand,
+    pin_rs_then_ag_is_all_reduce, pin_broadcast, pin_in_place_all_reduce,
+    pin_bucket_equals_per_tensor, pin_sgd_closed_form, pin_sgd_matches_torch,
+    pin_sgd_write_back_flag, pin_bucket_plan,
+]

@@ -1,0 +1,61 @@
+"""Planted mistakes in copies of the oracle must each fail at least one pin.
+
+Each case patches one line of ``oracle/oracle.c`` in a temporary copy (a
+dropped term, a reversed order, a wrong divisor, a wrong rounding rule, a
+wrong index or sign), builds it with the same flags, and runs the pins of
+``pins.py`` until one fails.  The unpatched oracle passes them all
+(``test_oracle_pins``), so each failure here is caused by the planted
+mistake.
+"""
+import pytest
+
+import oracle
+import pins
+
+MUTANTS = {
+    "dropped_last_rank": ("for (int r = 1; r < P; ++r)\n        acc = acc + load",
+                          "for (int r = 1; r < P - 1; ++r)\n        acc = acc + load"),
+    "reversed_rank_order": (
+        "float acc = load(x[0], i, dtype);\n    for (int r = 1; r < P; ++r)\n"
+        "        acc = acc + load(x[r], i, dtype);",
+        "float acc = load(x[P - 1], i, dtype);\n    for (int r = P - 2; r >= 0; --r)\n"
+        "        acc = acc + load(x[r], i, dtype);"),
+    "seeded_with_plus_zero": (
+        "float acc = load(x[0], i, dtype);\n    for (int r = 1; r < P; ++r)",
+        "float acc = 0.0f;\n    for (int r = 0; r < P; ++r)"),
+    "mean_by_reciprocal": ("acc = acc / (float)P;", "acc = acc * (1.0f / (float)P);"),
+    "mean_missing": ("if (op == OR_MEAN)\n        acc = acc / (float)P;", "(void)op;"),
+    "bf16_ties_away": ("return (uint16_t)((u + 0x7FFFu + ((u >> 16) & 1u)) >> 16);",
+                       "return (uint16_t)((u + 0x8000u) >> 16);"),
+    "bf16_truncate": ("return (uint16_t)((u + 0x7FFFu + ((u >> 16) & 1u)) >> 16);",
+                      "return (uint16_t)(u >> 16);"),
+    "bf16_widen_wrong_half": ("uint32_t u = (uint32_t)h << 16;", "uint32_t u = (uint32_t)h;"),
+    "rs_strided_shard": ("(size_t)r * shard + j, dtype, op)", "(size_t)j * (size_t)P + r, dtype, op)"),
+    "ag_wrong_offset": ("char *dst = (char *)recv[r] + (size_t)s * bytes;",
+                        "char *dst = (char *)recv[r] + (size_t)r * bytes;"),
+    "bc_from_rank0": ("memcpy(buf[r], buf[root], n * elem_size(dtype));",
+                      "memcpy(buf[r], buf[0], n * elem_size(dtype));"),
+    "sgd_wrong_sign": ("w[i] = w[i] - step;", "w[i] = w[i] + step;"),
+    "sgd_step_uses_g": ("float step = lr * v[i];", "float step = lr * g;"),
+    "sgd_no_momentum": ("float mv = momentum * v[i];", "float mv = 0.0f * v[i];"),
+    "sgd_ignores_write_back": ("if (!sgd || write_back)", "if (!sgd)"),
+    "plan_forward_order": ("for (int t = ntensors - 1; t >= 0; --t)",
+                           "for (int t = 0; t < ntensors; ++t)"),
+    "plan_closes_at_cap": ("fill + nbytes[t] > cap_bytes", "fill + nbytes[t] >= cap_bytes"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_fails_a_pin(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = oracle.SRC.read_text()
+    assert src.count(old) == 1, f"mutation target of {name} not found exactly once"
+    mutant = tmp_path / "oracle_mutant.c"
+    mutant.write_text(src.replace(old, new))
+    L = oracle.load(oracle.build(src=mutant, out=tmp_path / "liboracle_mutant.so"))
+    for pin in pins.ALL_PINS:
+        try:
+            pin(L)
+        except AssertionError:
+            return
+    pytest.fail(f"planted mistake {name} passed every pin")
