@@ -1,0 +1,522 @@
+"""Benchmark of the gradient all-reduce hot path on GB300.
+
+One step is the data-parallel gradient synchronisation and optimizer step
+of ViT-B/16: P = 8 replicas of the model's 86,567,656 bf16 gradients
+(152 tensors in module order), packed into 25 MiB buckets in reverse
+order (8 buckets), each bucket all-reduced with Mean by one kernel launch
+fused with SGD (momentum 0.9, lr 0.1) on fp32 master weights, the reduced
+gradient written back to every replica.  Throughput is algorithmic bytes
+per second: per step every replica is read and written once (2*P*N*2
+bytes) and the fp32 weights and momentum are read and written once (16*N
+bytes), 4.155 GB in all.
+
+Output: one JSON line (rank 0).  ``value`` times the device-resident step
+with CUDA events; ``e2e`` times the same step through the public API from
+pinned host buffers (gradients in, updated weights out); ``roofline``
+relates the bucket kernel's own event-timed duration to the measured HBM
+copy bandwidth; ``sweep`` gives the flat all-reduce (and RS/AG/BC) GB/s
+against message size for P = 2, 4, 8; ``cpu_baseline`` times the CPU
+oracle on a bounded sample of the same step.
+
+``--impl reference`` times the CPU oracle (the only reference this
+project has) on the same workload and prints the same line with
+"impl": "reference".
+
+Under torchrun each rank runs its own replica group on its own GPU
+(replicas only: the method runs on one GPU and has no exchange between
+GPUs); the elapsed time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "all-reduce algorithm GB/s and % of GB300 HBM roofline vs bytes, P=2/4/8"
+WORKLOAD = ("vit_b16_ddp_step: P=8 replicas x 86,567,656 bf16 grads, 8 x 25 MiB buckets, "
+            "Mean all-reduce fused with SGD momentum (fp32 master), write-back")
+P_VIT = 8
+CAP = 25 << 20
+KERNEL_SOURCES = ["gar_device.cuh", "gar_kernels.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gar", "reference"], default="gar")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the size/replica sweep")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------ distributed
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Maximum of a per-rank float over all ranks (identity when alone)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def __exit__(self, *exc):
+        self.samples = []
+        if self.proc is None:
+            return False
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 8:
+                self.samples.append(parts)
+        return False
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for s in self.samples for k in range(4)
+                          if s[4 + k].lower() == "active"})
+        under_load = sorted(sm)[len(sm) // 2:] if sm else []
+        return {"sm_mhz": statistics.median(under_load) if under_load else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------- workloads
+
+def vit_layout():
+    import gradient_all_reduce_gb300 as gar
+    import workloads
+    numels = workloads.vit_b16_numels()
+    plan = gar.ar_bucket_plan([2 * n for n in numels], CAP)
+    offs = np.concatenate([[0], np.cumsum(numels)]).astype(np.int64)
+    buckets = [[] for _ in range(max(plan) + 1)]
+    for t in range(len(numels) - 1, -1, -1):
+        buckets[plan[t]].append(t)
+    return numels, offs, buckets
+
+
+def vit_bytes(n: int, P: int = P_VIT) -> int:
+    return 2 * P * n * 2 + 16 * n
+
+
+class VitStep:
+    """Device buffers and prepared bucket calls of one ViT-B/16 step."""
+
+    def __init__(self, comm, device):
+        import torch
+        import gradient_all_reduce_gb300 as gar
+        import workloads
+        from workloads import gpu as wgpu
+        self.numels, self.offs, self.buckets = vit_layout()
+        n = int(self.offs[-1])
+        self.n = n
+        self.grads = []
+        for r in range(P_VIT):
+            g = torch.empty(n, dtype=torch.bfloat16, device=device)
+            wgpu.fill(g, "normal", workloads.VIT_GRAD_SEED + r, std=workloads.VIT_GRAD_STD)
+            self.grads.append(g)
+        self.w = torch.empty(n, dtype=torch.float32, device=device)
+        wgpu.fill(self.w, "normal", workloads.VIT_MASTER_SEED, std=workloads.VIT_MASTER_STD)
+        self.v = torch.zeros(n, dtype=torch.float32, device=device)
+        o = self.offs
+        self.calls, self.bucket_bytes = [], []
+        for b in self.buckets:
+            ts = [[g[o[t]:o[t + 1]] for g in self.grads] for t in b]
+            sgd = (0.1, 0.9, [self.w[o[t]:o[t + 1]] for t in b],
+                   [self.v[o[t]:o[t + 1]] for t in b], 1)
+            self.calls.append(gar.PreparedBucket(comm, ts, [self.numels[t] for t in b],
+                                                 gar.AR_BF16, gar.AR_MEAN, sgd))
+            self.bucket_bytes.append(vit_bytes(sum(self.numels[t] for t in b)))
+        self.step_bytes = vit_bytes(n)
+
+    def step(self, stream):
+        for c in self.calls:
+            c(stream)
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        h.update((ROOT / "gradient_all_reduce_gb300" / "csrc" / name).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        return float(json.loads(p.read_text())["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def committed_traffic():
+    """DRAM bytes per launch of the bucket kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    p = ROOT / "profiles" / "traffic.json"
+    if not p.exists():
+        return None
+    d = json.loads(p.read_text())
+    if d.get("kernel_source_sha") != kernel_source_sha():
+        return None
+    return d
+
+
+# ------------------------------------------------------------- GPU timing
+
+def time_vit(args, device, stream, world):
+    """K timed steps of the ViT workload: step time from events around all
+    steps, per-launch durations of the bucket kernel from events around
+    each launch."""
+    import torch
+    import gradient_all_reduce_gb300 as gar
+    comm = gar.ar_init(P_VIT, device.index, gar.AR_MEAN)
+    try:
+        vs = VitStep(comm, device)
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                vs.step(stream)
+        torch.cuda.synchronize(device)
+        K = args.steps
+        nb = len(vs.calls)
+        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(nb)] for _ in range(K)]
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize(device)
+        with ClockSampler(device.index) as clocks, torch.cuda.stream(stream):
+            start.record(stream)
+            for k in range(K):
+                for b, c in enumerate(vs.calls):
+                    ev[k][b][0].record(stream)
+                    c(stream)
+                    ev[k][b][1].record(stream)
+            stop.record(stream)
+            torch.cuda.synchronize(device)
+        elapsed = start.elapsed_time(stop) / 1e3
+        launch_s = sum(e0.elapsed_time(e1) for row in ev for e0, e1 in row) / 1e3
+        status = gar.ar_get_async_error(comm)
+        if status != gar.AR_OK:
+            raise RuntimeError(f"device status {gar.ar_status_string(status)}")
+        return {"elapsed": elapsed, "launch_s": launch_s, "launches": K * nb,
+                "step_bytes": vs.step_bytes, "launch_bytes": sum(vs.bucket_bytes) * K,
+                "clocks": clocks.summary(), "n": vs.n}
+    finally:
+        gar.ar_destroy(comm)
+
+
+def time_e2e(args, device, stream):
+    """The same step from pinned host buffers: every step copies the P
+    gradient replicas in, runs the buckets, and copies the updated fp32
+    master weights out (all on one stream)."""
+    import torch
+    import gradient_all_reduce_gb300 as gar
+    comm = gar.ar_init(P_VIT, device.index, gar.AR_MEAN)
+    try:
+        vs = VitStep(comm, device)
+        host_g = [g.cpu().pin_memory() for g in vs.grads]
+        host_w = torch.empty(vs.n, dtype=torch.float32).pin_memory()
+        steps = max(3, min(args.steps, 50))
+
+        def one():
+            for r in range(P_VIT):
+                vs.grads[r].copy_(host_g[r], non_blocking=True)
+            vs.step(stream)
+            host_w.copy_(vs.w, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                one()
+            torch.cuda.synchronize(device)
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            for _ in range(steps):
+                one()
+            t1.record(stream)
+            torch.cuda.synchronize(device)
+        el = t0.elapsed_time(t1) / 1e3
+        return {"value": vs.step_bytes * steps / el / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": 2 * vs.n * P_VIT, "d2h_bytes_per_step": 4 * vs.n,
+                "steps": steps, "ms_per_step": el / steps * 1e3}
+    finally:
+        gar.ar_destroy(comm)
+
+
+def flush_l2(buf):
+    buf.add_(1)
+
+
+def time_sweep(device, stream):
+    """Flat all-reduce (Mean, in place) GB/s for P = 2, 4, 8 at 64 MiB,
+    256 MiB and 1 GiB per replica, fp32 and bf16; reduce-scatter,
+    all-gather and broadcast at 256 MiB per replica, P = 4 and 8; and the
+    latency of small all-reduces (4 KiB .. 1 MiB, P = 8, fp32).  L2 is
+    flushed (a 256 MiB write) between repetitions."""
+    import torch
+    import gradient_all_reduce_gb300 as gar
+    from workloads import gpu as wgpu
+    flush = torch.empty(64 << 20, dtype=torch.float32, device=device)
+    out = {"all_reduce": [], "reduce_scatter": [], "all_gather": [], "broadcast": [],
+           "small_all_reduce_us": []}
+
+    def timed(fn, reps, flush_between=True):
+        ts = []
+        with torch.cuda.stream(stream):
+            for i in range(reps + 3):
+                if flush_between:
+                    flush_l2(flush)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                if i >= 3:
+                    ts.append((e0, e1))
+            torch.cuda.synchronize(device)
+        return statistics.median(a.elapsed_time(b) / 1e3 for a, b in ts)
+
+    for P in (2, 4, 8):
+        comm = gar.ar_init(P, device.index, gar.AR_MEAN)
+        try:
+            for dt, s in ((gar.AR_F32, 4), (gar.AR_BF16, 2)):
+                tdt = torch.float32 if s == 4 else torch.bfloat16
+                for mib in (64, 256, 1024):
+                    n = (mib << 20) // s
+                    xs = [torch.empty(n, dtype=tdt, device=device) for _ in range(P)]
+                    for r, x in enumerate(xs):
+                        wgpu.fill(x, "uniform", r)
+                    t = timed(lambda: gar.ar_all_reduce(comm, xs, xs, n, dt, gar.AR_MEAN, stream),
+                              10)
+                    out["all_reduce"].append({"P": P, "dtype": "f32" if s == 4 else "bf16",
+                                              "MiB_per_replica": mib, "us": t * 1e6,
+                                              "GBps": 2 * P * n * s / t / 1e9})
+                    del xs
+            if P in (4, 8):
+                n = (256 << 20) // 4
+                shard = n // P
+                xs = [torch.empty(n, dtype=torch.float32, device=device) for _ in range(P)]
+                for r, x in enumerate(xs):
+                    wgpu.fill(x, "uniform", r)
+                rs = [torch.empty(shard, dtype=torch.float32, device=device) for _ in range(P)]
+                t = timed(lambda: gar.ar_reduce_scatter(comm, xs, rs, n, gar.AR_F32, gar.AR_SUM,
+                                                        stream), 10)
+                out["reduce_scatter"].append({"P": P, "MiB_per_replica": 256, "us": t * 1e6,
+                                              "GBps": (P + 1) * shard * P * 4 / t / 1e9})
+                ins = [x[r * shard:(r + 1) * shard] for r, x in enumerate(xs)]
+                t = timed(lambda: gar.ar_all_gather(comm, ins, xs, n, gar.AR_F32, stream), 10)
+                out["all_gather"].append({"P": P, "MiB_per_replica": 256, "us": t * 1e6,
+                                          "GBps": P * n * 4 / t / 1e9})
+                t = timed(lambda: gar.ar_broadcast(comm, xs, n, gar.AR_F32, 0, stream), 10)
+                out["broadcast"].append({"P": P, "MiB_per_replica": 256, "us": t * 1e6,
+                                         "GBps": P * n * 4 / t / 1e9})
+                del xs, rs, ins
+            if P == 8:
+                for kib in (4, 64, 1024):
+                    n = (kib << 10) // 4
+                    xs = [torch.empty(n, dtype=torch.float32, device=device) for _ in range(P)]
+                    t = timed(lambda: gar.ar_all_reduce(comm, xs, xs, n, gar.AR_F32, gar.AR_MEAN,
+                                                        stream), 50, flush_between=False)
+                    out["small_all_reduce_us"].append({"P": P, "KiB_per_replica": kib,
+                                                       "us": t * 1e6})
+                    del xs
+        finally:
+            gar.ar_destroy(comm)
+    del flush
+    torch.cuda.empty_cache()
+    return out
+
+
+# -------------------------------------------------------------- CPU oracle
+
+def oracle_sample(elems: int, offset: int = 0):
+    """Host inputs of a contiguous sample of the ViT step: ``elems`` gradient
+    elements of every replica starting at ``offset``, with their master
+    weights and zero momentum."""
+    import workloads
+    grads = [workloads.replica_values("normal", "bf16", workloads.VIT_GRAD_SEED + r, elems,
+                                      std=workloads.VIT_GRAD_STD, start=offset)
+             for r in range(P_VIT)]
+    w = workloads.normal_f32(workloads.VIT_MASTER_SEED, elems, std=workloads.VIT_MASTER_STD,
+                             start=offset)
+    return grads, w, np.zeros(elems, np.float32)
+
+
+def cpu_oracle_rate(elems: int, min_seconds: float):
+    """Run the oracle's bucketed Mean + SGD on the sample until at least
+    min_seconds have passed; returns (GB/s, repetitions, seconds)."""
+    import oracle
+    grads, w, v = oracle_sample(elems)
+    reps, spent = 0, 0.0
+    while spent < min_seconds or reps == 0:
+        t0 = time.perf_counter()
+        oracle.bucket_all_reduce([grads], op=oracle.MEAN, sgd=(0.1, 0.9, [w], [v], 1))
+        spent += time.perf_counter() - t0
+        reps += 1
+    return vit_bytes(elems) * reps / spent / 1e9, reps, spent
+
+
+def run_reference(args):
+    """The CPU oracle timed on the host cores, on bounded samples of the ViT
+    step; rank 0 only."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    n_total = sum(vit_layout()[0])
+    probe_elems = 1 << 20
+    rate, _, _ = cpu_oracle_rate(probe_elems, 0.5)
+    budget = 60.0                                   # seconds of oracle work in the timed steps
+    per_step_s = budget / max(1, args.steps + args.warmup)
+    elems = int(max(4096, min(n_total, rate * 1e9 * per_step_s / vit_bytes(1))))
+    grads, w, v = oracle_sample(elems)
+    for _ in range(args.warmup):
+        oracle.bucket_all_reduce([grads], op=oracle.MEAN, sgd=(0.1, 0.9, [w], [v], 1))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.bucket_all_reduce([grads], op=oracle.MEAN, sgd=(0.1, 0.9, [w], [v], 1))
+    el = time.perf_counter() - t0
+    value = vit_bytes(elems) * args.steps / el / 1e9
+    sample = (f"each step: the oracle's Mean + SGD on {elems:,} of the {n_total:,} gradient "
+              f"elements of all {P_VIT} replicas (one contiguous slice), single thread")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample_elements": elems},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------------- main
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    rank, world, local = dist_env()
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    import gradient_all_reduce_gb300  # noqa: F401  (fails loudly without libgar.so)
+    stream = torch.cuda.Stream(device)
+
+    res = time_vit(args, device, stream, world)
+    elapsed = max_over_ranks(res["elapsed"], world, device)
+    total_bytes = res["step_bytes"] * args.steps * world
+    value = total_bytes / elapsed / 1e9
+    peak, peak_kind = measured_peak()
+    achieved = res["launch_bytes"] / res["launch_s"] / 1e9
+    traffic = committed_traffic()
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "P": P_VIT, "params": res["n"], "buckets": 8,
+                   "bucket_cap_mib": 25, "grad_dtype": "bf16", "accumulate": "fp32",
+                   "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (4.155 GB moved per step, no flush)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "kernel": "k_reduce<BF16, P=8, SGD> (one launch per bucket)",
+                     "traffic": traffic["dram_bytes_per_step"] / 8 if traffic else None},
+        "gpu_launches": res["launches"],
+        "clocks": res["clocks"],
+    }
+    if traffic:
+        line["roofline"]["traffic_note"] = ("DRAM bytes per launch, mean over the 8 bucket "
+                                            "launches of one step, from " + traffic["source"])
+    if rank == 0 and not args.no_e2e:
+        line["e2e"] = time_e2e(args, device, stream)
+    if rank == 0 and not args.no_sweep:
+        line["sweep"] = time_sweep(device, stream)
+    if rank == 0 and not args.no_cpu:
+        import oracle
+        oracle.build()
+        elems = 8 << 20
+        rate, reps, spent = cpu_oracle_rate(elems, 10.0)
+        line["cpu_baseline"] = {
+            "value": rate, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": (f"{reps} runs of the oracle's Mean + SGD on the first {elems:,} of the "
+                       f"{res['n']:,} gradient elements of all {P_VIT} replicas, single "
+                       f"thread, {spent:.1f} s")}
+    barrier(world)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,205 @@
+"""Python binding of libgar.so, the GB300 gradient all-reduce library.
+
+Argument marshalling only: every function forwards to the C entry point of
+the same name declared in ``include/gar.h``; all work runs in the library's
+CUDA kernels.  Buffers may be given as raw device addresses (int) or as
+objects with ``data_ptr()`` (torch tensors); streams as raw handles (int),
+objects with ``cuda_stream`` (torch.cuda.Stream), or None for the current
+torch stream (the legacy default stream when torch is not imported).
+
+The library must be built first (``gradient_all_reduce_gb300.build.build()``
+or ``__graft_entry__.build()``); importing this module without it raises
+ImportError -- there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import sys
+from pathlib import Path
+from typing import Sequence
+
+_LIB_PATH = Path(__file__).resolve().parent / "libgar.so"
+
+AR_OK, AR_ERR_INVALID_ARG, AR_ERR_UNSUPPORTED, AR_ERR_CUDA, AR_ERR_TIMEOUT, AR_ERR_STATE = range(6)
+AR_OP_DEFAULT, AR_SUM, AR_MEAN = -1, 0, 1
+AR_F32, AR_BF16 = 0, 1
+AR_MAX_RANKS = 16
+ELEM_BYTES = {AR_F32: 4, AR_BF16: 2}
+
+
+class GarError(RuntimeError):
+    """A non-OK ar_status_t from the library."""
+
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {ar_status_string(status)}")
+
+
+class ar_bucket_t(ctypes.Structure):
+    _fields_ = [("ntensors", ctypes.c_int), ("dev_ptrs", ctypes.POINTER(ctypes.c_void_p)),
+                ("numel", ctypes.POINTER(ctypes.c_size_t)), ("dtype", ctypes.c_int)]
+
+
+class ar_sgd_t(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("momentum", ctypes.c_float),
+                ("master", ctypes.POINTER(ctypes.c_void_p)),
+                ("momentum_buf", ctypes.POINTER(ctypes.c_void_p)),
+                ("write_back_grads", ctypes.c_int)]
+
+
+def _load() -> ctypes.CDLL:
+    if not _LIB_PATH.exists():
+        raise ImportError(f"{_LIB_PATH} is missing: build it with "
+                          "gradient_all_reduce_gb300.build.build()")
+    lib = ctypes.CDLL(str(_LIB_PATH))
+    P = ctypes.c_void_p
+    PP = ctypes.POINTER(ctypes.c_void_p)
+    sigs = {
+        "ar_init": [ctypes.POINTER(P), ctypes.c_int, ctypes.c_int, ctypes.c_int],
+        "ar_destroy": [P],
+        "ar_all_reduce": [P, PP, PP, ctypes.c_size_t, ctypes.c_int, ctypes.c_int, P],
+        "ar_reduce_scatter": [P, PP, PP, ctypes.c_size_t, ctypes.c_int, ctypes.c_int, P],
+        "ar_all_gather": [P, PP, PP, ctypes.c_size_t, ctypes.c_int, P],
+        "ar_broadcast": [P, PP, ctypes.c_size_t, ctypes.c_int, ctypes.c_int, P],
+        "ar_bucket_all_reduce": [P, ctypes.POINTER(ar_bucket_t), ctypes.c_int,
+                                 ctypes.POINTER(ar_sgd_t), P],
+        "ar_bucket_plan": [ctypes.c_int, ctypes.POINTER(ctypes.c_size_t), ctypes.c_size_t,
+                           ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)],
+        "ar_get_async_error": [P],
+    }
+    for name, args in sigs.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.ar_status_string.argtypes = [ctypes.c_int]
+    lib.ar_status_string.restype = ctypes.c_char_p
+    return lib
+
+
+lib = _load()
+
+
+def ar_status_string(status: int) -> str:
+    return lib.ar_status_string(int(status)).decode()
+
+
+def _ok(status: int, what: str) -> None:
+    if status != AR_OK:
+        raise GarError(status, what)
+
+
+def _addr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _ptr_array(xs) -> ctypes.Array:
+    return (ctypes.c_void_p * len(xs))(*[_addr(x) for x in xs])
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        torch = sys.modules.get("torch")
+        return int(torch.cuda.current_stream().cuda_stream) if torch is not None else 0
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def ar_init(nranks: int, cuda_device: int = 0, default_op: int = AR_MEAN) -> int:
+    """Create a device group of ``nranks`` replicas; returns the comm handle."""
+    comm = ctypes.c_void_p()
+    _ok(lib.ar_init(ctypes.byref(comm), int(nranks), int(cuda_device), int(default_op)), "ar_init")
+    return int(comm.value)
+
+
+def ar_destroy(comm: int) -> None:
+    _ok(lib.ar_destroy(comm), "ar_destroy")
+
+
+def ar_all_reduce(comm: int, send: Sequence, recv: Sequence, count: int, dtype: int,
+                  op: int = AR_OP_DEFAULT, stream=None) -> None:
+    _ok(lib.ar_all_reduce(comm, _ptr_array(send), _ptr_array(recv), int(count), int(dtype),
+                          int(op), _stream(stream)), "ar_all_reduce")
+
+
+def ar_reduce_scatter(comm: int, send: Sequence, recv: Sequence, count: int, dtype: int,
+                      op: int = AR_OP_DEFAULT, stream=None) -> None:
+    _ok(lib.ar_reduce_scatter(comm, _ptr_array(send), _ptr_array(recv), int(count), int(dtype),
+                              int(op), _stream(stream)), "ar_reduce_scatter")
+
+
+def ar_all_gather(comm: int, send: Sequence, recv: Sequence, count: int, dtype: int,
+                  stream=None) -> None:
+    _ok(lib.ar_all_gather(comm, _ptr_array(send), _ptr_array(recv), int(count), int(dtype),
+                          _stream(stream)), "ar_all_gather")
+
+
+def ar_broadcast(comm: int, buf: Sequence, count: int, dtype: int, root: int = 0,
+                 stream=None) -> None:
+    _ok(lib.ar_broadcast(comm, _ptr_array(buf), int(count), int(dtype), int(root),
+                         _stream(stream)), "ar_broadcast")
+
+
+def ar_bucket_all_reduce(comm: int, tensors: Sequence[Sequence], numel: Sequence[int], dtype: int,
+                         op: int = AR_OP_DEFAULT, sgd=None, stream=None) -> None:
+    """``tensors[t][r]`` is rank r's replica of tensor t.  ``sgd`` is None or
+    (lr, momentum, master[t], momentum_buf[t], write_back_grads)."""
+    flat = [x for reps in tensors for x in reps]
+    ptrs = _ptr_array(flat)
+    nel = (ctypes.c_size_t * max(len(numel), 1))(*[int(n) for n in numel])
+    b = ar_bucket_t(len(tensors), ctypes.cast(ptrs, ctypes.POINTER(ctypes.c_void_p)),
+                    ctypes.cast(nel, ctypes.POINTER(ctypes.c_size_t)), int(dtype))
+    s = None
+    if sgd is not None:
+        lr, mom, master, mbuf, wb = sgd
+        m, v = _ptr_array(master), _ptr_array(mbuf)
+        s = ar_sgd_t(float(lr), float(mom), ctypes.cast(m, ctypes.POINTER(ctypes.c_void_p)),
+                     ctypes.cast(v, ctypes.POINTER(ctypes.c_void_p)), int(bool(wb)))
+    _ok(lib.ar_bucket_all_reduce(comm, ctypes.byref(b), int(op),
+                                 ctypes.byref(s) if s is not None else None, _stream(stream)),
+        "ar_bucket_all_reduce")
+
+
+def ar_bucket_plan(nbytes: Sequence[int], cap_bytes: int = 25 << 20) -> list[int]:
+    """Bucket index of each tensor (registration order in; reverse-order fill)."""
+    T = len(nbytes)
+    nb = (ctypes.c_size_t * max(T, 1))(*[int(n) for n in nbytes])
+    out = (ctypes.c_int * max(T, 1))()
+    k = ctypes.c_int()
+    _ok(lib.ar_bucket_plan(T, nb, int(cap_bytes), out, ctypes.byref(k)), "ar_bucket_plan")
+    return list(out)[:T]
+
+
+def ar_get_async_error(comm: int) -> int:
+    """The comm's sticky device-side status (an ar_status_t, not raised)."""
+    return int(lib.ar_get_async_error(comm))
+
+
+class PreparedBucket:
+    """An ar_bucket_all_reduce call with its argument structures built once
+    (the pointer and length arrays stay alive with this object), so that a
+    training loop re-issues the same call without rebuilding them."""
+
+    def __init__(self, comm: int, tensors: Sequence[Sequence], numel: Sequence[int], dtype: int,
+                 op: int = AR_OP_DEFAULT, sgd=None):
+        flat = [x for reps in tensors for x in reps]
+        self._ptrs = _ptr_array(flat)
+        self._nel = (ctypes.c_size_t * max(len(numel), 1))(*[int(n) for n in numel])
+        self._bucket = ar_bucket_t(len(tensors), ctypes.cast(self._ptrs, ctypes.POINTER(ctypes.c_void_p)),
+                                   ctypes.cast(self._nel, ctypes.POINTER(ctypes.c_size_t)), int(dtype))
+        self._sgd = None
+        if sgd is not None:
+            lr, mom, master, mbuf, wb = sgd
+            self._m, self._v = _ptr_array(master), _ptr_array(mbuf)
+            self._sgd = ar_sgd_t(float(lr), float(mom),
+                                 ctypes.cast(self._m, ctypes.POINTER(ctypes.c_void_p)),
+                                 ctypes.cast(self._v, ctypes.POINTER(ctypes.c_void_p)), int(bool(wb)))
+        self._args = (comm, ctypes.byref(self._bucket), int(op),
+                      ctypes.byref(self._sgd) if self._sgd is not None else None)
+
+    def __call__(self, stream=None) -> None:
+        _ok(lib.ar_bucket_all_reduce(*self._args, _stream(stream)), "ar_bucket_all_reduce")

@@ -1,0 +1,555 @@
+// gar_api.cu -- the C ABI declared in include/gar.h: comm lifetime, host-side
+// argument validation, segment tables, and dispatch to the kernels.
+#include <algorithm>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <unordered_set>
+#include <vector>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "gar.h"
+#include "gar_launch.h"
+
+struct ar_comm_s {
+  int nranks;
+  int device;
+  int num_sms;
+  ar_op_t default_op;
+  uint32_t* d_status;   // sticky device-side status word (0 = ok)
+  bool check_pointers;  // validate every pointer against its allocation
+};
+
+namespace {
+
+using gar::CapLarge;
+using gar::CapSmall;
+using gar::SegTable;
+
+std::mutex g_live_mu;
+std::unordered_set<const ar_comm_s*> g_live;
+
+bool is_live(const ar_comm_s* c) {
+  std::lock_guard<std::mutex> lock(g_live_mu);
+  return c != nullptr && g_live.count(c) != 0;
+}
+
+// Makes the comm's device current for the duration of a call and restores
+// the caller's device afterwards.
+class DeviceGuard {
+ public:
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev_) != cudaSuccess) prev_ = -1;
+    ok_ = prev_ == dev || cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev_ >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev_) cudaSetDevice(prev_);
+  }
+  bool ok() const { return ok_; }
+
+ private:
+  int prev_ = -1;
+  bool ok_ = false;
+};
+
+size_t elem_bytes(ar_dtype_t dt) { return dt == AR_BF16 ? 2 : 4; }
+bool valid_dtype(ar_dtype_t dt) { return dt == AR_F32 || dt == AR_BF16; }
+
+bool resolve_op(const ar_comm_s* c, ar_op_t op, ar_op_t* out) {
+  if (op == AR_OP_DEFAULT) op = c->default_op;
+  if (op != AR_SUM && op != AR_MEAN) return false;
+  *out = op;
+  return true;
+}
+
+uintptr_t addr(const void* p) { return reinterpret_cast<uintptr_t>(p); }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  if (na == 0 || nb == 0) return false;
+  return addr(a) < addr(b) + nb && addr(b) < addr(a) + na;
+}
+
+bool mul_ok(size_t a, size_t b, size_t* out) {
+  if (a != 0 && b > SIZE_MAX / a) return false;
+  *out = a * b;
+  return true;
+}
+
+// The driver's cuMemGetAddressRange, fetched through the runtime so the
+// library needs no link-time dependency on libcuda.
+using MemGetAddressRangeFn = CUresult (*)(CUdeviceptr*, size_t*, CUdeviceptr);
+
+MemGetAddressRangeFn address_range_fn() {
+  static MemGetAddressRangeFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<MemGetAddressRangeFn>(p);
+  }();
+  return fn;
+}
+
+// A buffer the comm's device may read and write: device memory of this
+// device (the whole range inside one allocation), managed memory, or
+// registered host memory mapped at the same address.  Pageable host memory
+// is refused.
+bool pointer_ok(const ar_comm_s* c, const void* p, size_t bytes) {
+  if (p == nullptr) return false;
+  if (!c->check_pointers || bytes == 0) return true;
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  switch (at.type) {
+    case cudaMemoryTypeDevice: {
+      if (at.device != c->device) return false;
+      MemGetAddressRangeFn range = address_range_fn();
+      if (range != nullptr) {
+        CUdeviceptr base = 0;
+        size_t size = 0;
+        if (range(&base, &size, static_cast<CUdeviceptr>(addr(p))) != CUDA_SUCCESS) return false;
+        if (addr(p) + bytes > static_cast<uintptr_t>(base) + size) return false;
+      }
+      return true;
+    }
+    case cudaMemoryTypeManaged:
+      return true;
+    case cudaMemoryTypeHost:
+      return at.devicePointer == p;
+    default:
+      return false;
+  }
+}
+
+bool aligned(const void* p, size_t a) { return addr(p) % a == 0; }
+
+template <class Cap>
+void init_table(SegTable<Cap>& t, int np, int ndst, int stride, int dst_off, bool mean) {
+  t.nseg = 0;
+  t.ntiles = 0;
+  t.np = np;
+  t.ndst = ndst;
+  t.stride = stride;
+  t.dst_off = dst_off;
+  t.mean = mean ? 1 : 0;
+  t.write_back = 1;
+  t.lr = 0.f;
+  t.mu = 0.f;
+  t.tile0[0] = 0;
+}
+
+// Appends one segment; ptrs holds `stride` pointers.  Returns false when a
+// 32-bit tile count would overflow.
+template <class Cap>
+bool add_segment(SegTable<Cap>& t, void* const* ptrs, uint64_t numel, uint64_t tile,
+                 uint32_t flags, float* master = nullptr, float* mom = nullptr) {
+  const uint32_t s = t.nseg;
+  const uint64_t tiles = (numel + tile - 1) / tile;
+  if (uint64_t(t.ntiles) + tiles > 0xFFFFFFF0ull) return false;
+  for (int k = 0; k < t.stride; ++k) t.ptr[s * t.stride + k] = ptrs[k];
+  t.numel[s] = numel;
+  t.flags[s] = flags;
+  t.master[s] = master;
+  t.mom[s] = mom;
+  t.ntiles += static_cast<uint32_t>(tiles);
+  t.tile0[s + 1] = t.ntiles;
+  t.nseg = s + 1;
+  return true;
+}
+
+uint32_t vec_flag(void* const* ptrs, int n, float* const* extra = nullptr, int nextra = 0) {
+  for (int k = 0; k < n; ++k)
+    if (!aligned(ptrs[k], 16)) return 0;
+  for (int k = 0; k < nextra; ++k)
+    if (!aligned(extra[k], 16)) return 0;
+  return gar::kSegVec;
+}
+
+ar_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? AR_OK : AR_ERR_CUDA; }
+
+template <class Cap>
+ar_status_t run_reduce(const ar_comm_s* c, ar_dtype_t dt, bool sgd, const SegTable<Cap>& t,
+                       cudaStream_t st) {
+  if (t.ntiles == 0) return AR_OK;
+  const gar::LaunchCtx ctx{c->device, c->num_sms, st};
+  return from_cuda(dt == AR_F32 ? gar::launch_reduce_f32<Cap>(ctx, sgd, t)
+                                : gar::launch_reduce_bf16<Cap>(ctx, sgd, t));
+}
+
+template <class Cap>
+ar_status_t run_copy(const ar_comm_s* c, const SegTable<Cap>& t, cudaStream_t st) {
+  if (t.ntiles == 0) return AR_OK;
+  const gar::LaunchCtx ctx{c->device, c->num_sms, st};
+  return from_cuda(gar::launch_copy<Cap>(ctx, t));
+}
+
+// Common checks of a collective call: live comm, dtype, pointer arrays.
+ar_status_t check_call(const ar_comm_s* c, ar_dtype_t dt) {
+  if (!is_live(c)) return AR_ERR_STATE;
+  if (!valid_dtype(dt)) return AR_ERR_INVALID_ARG;
+  return AR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ar_status_string(ar_status_t s) {
+  switch (s) {
+    case AR_OK: return "AR_OK";
+    case AR_ERR_INVALID_ARG: return "AR_ERR_INVALID_ARG: invalid argument";
+    case AR_ERR_UNSUPPORTED: return "AR_ERR_UNSUPPORTED: unsupported device or feature";
+    case AR_ERR_CUDA: return "AR_ERR_CUDA: CUDA call or kernel launch failed";
+    case AR_ERR_TIMEOUT: return "AR_ERR_TIMEOUT: a device-side bounded wait gave up";
+    case AR_ERR_STATE: return "AR_ERR_STATE: comm is not live";
+  }
+  return "unknown ar_status_t";
+}
+
+ar_status_t ar_init(ar_comm_t* comm, int nranks, int cuda_device, ar_op_t default_op) {
+  if (comm == nullptr) return AR_ERR_INVALID_ARG;
+  *comm = nullptr;
+  if (nranks < 1 || nranks > AR_MAX_RANKS) return AR_ERR_INVALID_ARG;
+  if (default_op != AR_SUM && default_op != AR_MEAN) return AR_ERR_INVALID_ARG;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess) {
+    cudaGetLastError();
+    return AR_ERR_CUDA;
+  }
+  if (cuda_device < 0 || cuda_device >= ndev) return AR_ERR_INVALID_ARG;
+  DeviceGuard guard(cuda_device);
+  if (!guard.ok()) return AR_ERR_CUDA;
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, cuda_device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, cuda_device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, cuda_device) != cudaSuccess)
+    return AR_ERR_CUDA;
+  if (major != 10 || minor != 3) return AR_ERR_UNSUPPORTED;  // built for sm_103a only
+  ar_comm_s* c = new (std::nothrow) ar_comm_s();
+  if (c == nullptr) return AR_ERR_CUDA;
+  c->nranks = nranks;
+  c->device = cuda_device;
+  c->num_sms = sms;
+  c->default_op = default_op;
+  const char* env = std::getenv("GAR_POINTER_CHECKS");
+  c->check_pointers = !(env != nullptr && std::strcmp(env, "0") == 0);
+  if (cudaMalloc(&c->d_status, sizeof(uint32_t)) != cudaSuccess) {
+    delete c;
+    return AR_ERR_CUDA;
+  }
+  if (cudaMemset(c->d_status, 0, sizeof(uint32_t)) != cudaSuccess) {
+    cudaFree(c->d_status);
+    delete c;
+    return AR_ERR_CUDA;
+  }
+  {
+    std::lock_guard<std::mutex> lock(g_live_mu);
+    g_live.insert(c);
+  }
+  *comm = c;
+  return AR_OK;
+}
+
+ar_status_t ar_destroy(ar_comm_t comm) {
+  {
+    std::lock_guard<std::mutex> lock(g_live_mu);
+    if (comm == nullptr || g_live.erase(comm) == 0) return AR_ERR_STATE;
+  }
+  ar_status_t st = AR_OK;
+  {
+    DeviceGuard guard(comm->device);
+    if (cudaDeviceSynchronize() != cudaSuccess) st = AR_ERR_CUDA;
+    if (cudaFree(comm->d_status) != cudaSuccess) st = AR_ERR_CUDA;
+  }
+  delete comm;
+  return st;
+}
+
+ar_status_t ar_get_async_error(ar_comm_t comm) {
+  if (!is_live(comm)) return AR_ERR_STATE;
+  DeviceGuard guard(comm->device);
+  uint32_t s = 0;
+  if (cudaMemcpy(&s, comm->d_status, sizeof s, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return AR_ERR_CUDA;
+  if (s != 0) return AR_ERR_TIMEOUT;
+  return cudaPeekAtLastError() == cudaSuccess ? AR_OK : AR_ERR_CUDA;
+}
+
+ar_status_t ar_all_reduce(ar_comm_t comm, const void* const* send, void* const* recv, size_t count,
+                          ar_dtype_t dtype, ar_op_t op, ar_stream_t stream) {
+  ar_status_t st = check_call(comm, dtype);
+  if (st != AR_OK) return st;
+  ar_op_t rop;
+  if (!resolve_op(comm, op, &rop) || send == nullptr || recv == nullptr) return AR_ERR_INVALID_ARG;
+  const int P = comm->nranks;
+  const size_t es = elem_bytes(dtype);
+  size_t bytes;
+  if (!mul_ok(count, es, &bytes)) return AR_ERR_INVALID_ARG;
+  DeviceGuard guard(comm->device);
+  if (!guard.ok()) return AR_ERR_CUDA;
+  for (int r = 0; r < P; ++r) {
+    if (send[r] == nullptr || recv[r] == nullptr) return AR_ERR_INVALID_ARG;
+    if (!aligned(send[r], es) || !aligned(recv[r], es)) return AR_ERR_INVALID_ARG;
+  }
+  for (int r = 0; r < P; ++r)
+    for (int q = 0; q < P; ++q) {
+      if (q != r && overlap(recv[r], bytes, recv[q], bytes)) return AR_ERR_INVALID_ARG;
+      const bool in_place = q == r && recv[r] == send[r];
+      if (!in_place && overlap(recv[r], bytes, send[q], bytes)) return AR_ERR_INVALID_ARG;
+    }
+  if (count == 0) return AR_OK;
+  for (int r = 0; r < P; ++r)
+    if (!pointer_ok(comm, send[r], bytes) || !pointer_ok(comm, recv[r], bytes))
+      return AR_ERR_INVALID_ARG;
+
+  SegTable<CapSmall> t;
+  init_table(t, P, P, 2 * P, P, rop == AR_MEAN);
+  void* ptrs[2 * AR_MAX_RANKS];
+  for (int r = 0; r < P; ++r) {
+    ptrs[r] = const_cast<void*>(send[r]);
+    ptrs[P + r] = recv[r];
+  }
+  if (!add_segment(t, ptrs, count, gar::reduce_tile(P, int(es)), vec_flag(ptrs, 2 * P)))
+    return AR_ERR_INVALID_ARG;
+  return run_reduce(comm, dtype, false, t, static_cast<cudaStream_t>(stream));
+}
+
+ar_status_t ar_reduce_scatter(ar_comm_t comm, const void* const* send, void* const* recv,
+                              size_t count, ar_dtype_t dtype, ar_op_t op, ar_stream_t stream) {
+  ar_status_t st = check_call(comm, dtype);
+  if (st != AR_OK) return st;
+  ar_op_t rop;
+  if (!resolve_op(comm, op, &rop) || send == nullptr || recv == nullptr) return AR_ERR_INVALID_ARG;
+  const int P = comm->nranks;
+  if (count % size_t(P) != 0) return AR_ERR_INVALID_ARG;
+  const size_t es = elem_bytes(dtype), shard = count / size_t(P);
+  size_t bytes;
+  if (!mul_ok(count, es, &bytes)) return AR_ERR_INVALID_ARG;
+  const size_t sbytes = shard * es;
+  DeviceGuard guard(comm->device);
+  if (!guard.ok()) return AR_ERR_CUDA;
+  for (int r = 0; r < P; ++r) {
+    if (send[r] == nullptr || recv[r] == nullptr) return AR_ERR_INVALID_ARG;
+    if (!aligned(send[r], es) || !aligned(recv[r], es)) return AR_ERR_INVALID_ARG;
+  }
+  for (int r = 0; r < P; ++r)
+    for (int q = 0; q < P; ++q) {
+      if (q != r && overlap(recv[r], sbytes, recv[q], sbytes)) return AR_ERR_INVALID_ARG;
+      const bool in_place =
+          q == r && addr(recv[r]) == addr(send[r]) + size_t(r) * sbytes;
+      if (!in_place && overlap(recv[r], sbytes, send[q], bytes)) return AR_ERR_INVALID_ARG;
+    }
+  if (count == 0) return AR_OK;
+  for (int r = 0; r < P; ++r)
+    if (!pointer_ok(comm, send[r], bytes) || !pointer_ok(comm, recv[r], sbytes))
+      return AR_ERR_INVALID_ARG;
+
+  SegTable<CapSmall> t;
+  init_table(t, P, 1, P + 1, P, rop == AR_MEAN);
+  const uint64_t tile = gar::reduce_tile(P, int(es));
+  for (int r = 0; r < P; ++r) {
+    void* ptrs[AR_MAX_RANKS + 1];
+    for (int q = 0; q < P; ++q)
+      ptrs[q] = static_cast<char*>(const_cast<void*>(send[q])) + size_t(r) * sbytes;
+    ptrs[P] = recv[r];
+    if (!add_segment(t, ptrs, shard, tile, vec_flag(ptrs, P + 1))) return AR_ERR_INVALID_ARG;
+  }
+  return run_reduce(comm, dtype, false, t, static_cast<cudaStream_t>(stream));
+}
+
+ar_status_t ar_all_gather(ar_comm_t comm, const void* const* send, void* const* recv, size_t count,
+                          ar_dtype_t dtype, ar_stream_t stream) {
+  ar_status_t st = check_call(comm, dtype);
+  if (st != AR_OK) return st;
+  if (send == nullptr || recv == nullptr) return AR_ERR_INVALID_ARG;
+  const int P = comm->nranks;
+  if (count % size_t(P) != 0) return AR_ERR_INVALID_ARG;
+  const size_t es = elem_bytes(dtype), shard = count / size_t(P);
+  size_t bytes;
+  if (!mul_ok(count, es, &bytes)) return AR_ERR_INVALID_ARG;
+  const size_t sbytes = shard * es;
+  DeviceGuard guard(comm->device);
+  if (!guard.ok()) return AR_ERR_CUDA;
+  for (int r = 0; r < P; ++r) {
+    if (send[r] == nullptr || recv[r] == nullptr) return AR_ERR_INVALID_ARG;
+    if (!aligned(send[r], es) || !aligned(recv[r], es)) return AR_ERR_INVALID_ARG;
+  }
+  for (int r = 0; r < P; ++r)
+    for (int q = 0; q < P; ++q) {
+      if (q != r && overlap(recv[r], bytes, recv[q], bytes)) return AR_ERR_INVALID_ARG;
+      const bool in_place =
+          q == r && addr(send[r]) == addr(recv[r]) + size_t(r) * sbytes;
+      if (!in_place && overlap(recv[r], bytes, send[q], sbytes)) return AR_ERR_INVALID_ARG;
+    }
+  if (count == 0) return AR_OK;
+  for (int r = 0; r < P; ++r)
+    if (!pointer_ok(comm, send[r], sbytes) || !pointer_ok(comm, recv[r], bytes))
+      return AR_ERR_INVALID_ARG;
+
+  SegTable<CapSmall> t;
+  init_table(t, 1, 0, P + 1, 1, false);
+  for (int q = 0; q < P; ++q) {
+    void* ptrs[AR_MAX_RANKS + 1];
+    int nd = 0;
+    ptrs[0] = const_cast<void*>(send[q]);
+    for (int r = 0; r < P; ++r) {
+      void* d = static_cast<char*>(recv[r]) + size_t(q) * sbytes;
+      if (d != send[q]) ptrs[1 + nd++] = d;  // an in-place shard is already there
+    }
+    for (int k = 1 + nd; k < P + 1; ++k) ptrs[k] = ptrs[0];
+    const uint32_t flags = vec_flag(ptrs, 1 + nd) | (uint32_t(nd) << 8);
+    if (!add_segment(t, ptrs, sbytes, gar::copy_tile_bytes(), flags)) return AR_ERR_INVALID_ARG;
+  }
+  return run_copy(comm, t, static_cast<cudaStream_t>(stream));
+}
+
+ar_status_t ar_broadcast(ar_comm_t comm, void* const* buf, size_t count, ar_dtype_t dtype, int root,
+                         ar_stream_t stream) {
+  ar_status_t st = check_call(comm, dtype);
+  if (st != AR_OK) return st;
+  const int P = comm->nranks;
+  if (buf == nullptr || root < 0 || root >= P) return AR_ERR_INVALID_ARG;
+  const size_t es = elem_bytes(dtype);
+  size_t bytes;
+  if (!mul_ok(count, es, &bytes)) return AR_ERR_INVALID_ARG;
+  DeviceGuard guard(comm->device);
+  if (!guard.ok()) return AR_ERR_CUDA;
+  for (int r = 0; r < P; ++r) {
+    if (buf[r] == nullptr || !aligned(buf[r], es)) return AR_ERR_INVALID_ARG;
+    for (int q = 0; q < r; ++q)
+      if (overlap(buf[r], bytes, buf[q], bytes)) return AR_ERR_INVALID_ARG;
+  }
+  if (count == 0 || P == 1) return AR_OK;
+  for (int r = 0; r < P; ++r)
+    if (!pointer_ok(comm, buf[r], bytes)) return AR_ERR_INVALID_ARG;
+
+  SegTable<CapSmall> t;
+  init_table(t, 1, 0, P, 1, false);
+  void* ptrs[AR_MAX_RANKS];
+  int nd = 0;
+  ptrs[0] = buf[root];
+  for (int r = 0; r < P; ++r)
+    if (r != root) ptrs[1 + nd++] = buf[r];
+  const uint32_t flags = vec_flag(ptrs, P) | (uint32_t(nd) << 8);
+  if (!add_segment(t, ptrs, bytes, gar::copy_tile_bytes(), flags)) return AR_ERR_INVALID_ARG;
+  return run_copy(comm, t, static_cast<cudaStream_t>(stream));
+}
+
+ar_status_t ar_bucket_all_reduce(ar_comm_t comm, const ar_bucket_t* bucket, ar_op_t op,
+                                 const ar_sgd_t* sgd, ar_stream_t stream) {
+  if (!is_live(comm)) return AR_ERR_STATE;
+  ar_op_t rop;
+  if (bucket == nullptr || !resolve_op(comm, op, &rop) || !valid_dtype(bucket->dtype) ||
+      bucket->ntensors < 0)
+    return AR_ERR_INVALID_ARG;
+  const int T = bucket->ntensors, P = comm->nranks;
+  if (T == 0) return AR_OK;
+  if (bucket->dev_ptrs == nullptr || bucket->numel == nullptr) return AR_ERR_INVALID_ARG;
+  if (sgd != nullptr && (sgd->master == nullptr || sgd->momentum_buf == nullptr))
+    return AR_ERR_INVALID_ARG;
+  const size_t es = elem_bytes(bucket->dtype);
+  DeviceGuard guard(comm->device);
+  if (!guard.ok()) return AR_ERR_CUDA;
+
+  // Every buffer of the bucket (replicas, and the fp32 master and momentum
+  // arrays) must be pairwise disjoint: sort the ranges and compare
+  // neighbours.
+  struct Range { uintptr_t lo, hi; };
+  std::vector<Range> ranges;
+  ranges.reserve(size_t(T) * (P + 2));
+  for (int t = 0; t < T; ++t) {
+    size_t bytes, fbytes;
+    if (!mul_ok(bucket->numel[t], es, &bytes) || !mul_ok(bucket->numel[t], 4, &fbytes))
+      return AR_ERR_INVALID_ARG;
+    for (int r = 0; r < P; ++r) {
+      const void* p = bucket->dev_ptrs[size_t(t) * P + r];
+      if (p == nullptr || !aligned(p, es)) return AR_ERR_INVALID_ARG;
+      if (bytes) ranges.push_back({addr(p), addr(p) + bytes});
+    }
+    if (sgd != nullptr) {
+      const float* w = sgd->master[t];
+      const float* v = sgd->momentum_buf[t];
+      if (w == nullptr || v == nullptr || !aligned(w, 4) || !aligned(v, 4))
+        return AR_ERR_INVALID_ARG;
+      if (fbytes) {
+        ranges.push_back({addr(w), addr(w) + fbytes});
+        ranges.push_back({addr(v), addr(v) + fbytes});
+      }
+    }
+  }
+  std::sort(ranges.begin(), ranges.end(),
+            [](const Range& a, const Range& b) { return a.lo < b.lo; });
+  for (size_t k = 1; k < ranges.size(); ++k)
+    if (ranges[k].lo < ranges[k - 1].hi) return AR_ERR_INVALID_ARG;
+  for (int t = 0; t < T; ++t) {
+    const size_t n = bucket->numel[t];
+    for (int r = 0; r < P; ++r)
+      if (!pointer_ok(comm, bucket->dev_ptrs[size_t(t) * P + r], n * es)) return AR_ERR_INVALID_ARG;
+    if (sgd != nullptr &&
+        (!pointer_ok(comm, sgd->master[t], n * 4) || !pointer_ok(comm, sgd->momentum_buf[t], n * 4)))
+      return AR_ERR_INVALID_ARG;
+  }
+
+  const uint64_t tile = gar::reduce_tile(P, int(es));
+  const cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  auto fill = [&](auto& tab, int t0, int t1) -> ar_status_t {
+    init_table(tab, P, P, P, 0, rop == AR_MEAN);
+    if (sgd != nullptr) {
+      tab.lr = sgd->lr;
+      tab.mu = sgd->momentum;
+      tab.write_back = sgd->write_back_grads ? 1 : 0;
+    }
+    for (int t = t0; t < t1; ++t) {
+      void* const* ptrs = bucket->dev_ptrs + size_t(t) * P;
+      float* w = sgd ? sgd->master[t] : nullptr;
+      float* v = sgd ? sgd->momentum_buf[t] : nullptr;
+      float* extra[2] = {w, v};
+      const uint32_t flags = vec_flag(ptrs, P, extra, sgd ? 2 : 0);
+      if (!add_segment(tab, ptrs, bucket->numel[t], tile, flags, w, v)) return AR_ERR_INVALID_ARG;
+    }
+    return AR_OK;
+  };
+  // One launch per group of tensors that fits a parameter block.
+  if (T <= CapSmall::kSeg && T * P <= CapSmall::kPtr) {
+    SegTable<CapSmall> tab;
+    ar_status_t s = fill(tab, 0, T);
+    return s != AR_OK ? s : run_reduce(comm, bucket->dtype, sgd != nullptr, tab, strm);
+  }
+  const int per_launch = std::min(CapLarge::kSeg, CapLarge::kPtr / P);
+  std::vector<SegTable<CapLarge>> tabs(1);
+  for (int t0 = 0; t0 < T; t0 += per_launch) {
+    ar_status_t s = fill(tabs[0], t0, std::min(T, t0 + per_launch));
+    if (s == AR_OK) s = run_reduce(comm, bucket->dtype, sgd != nullptr, tabs[0], strm);
+    if (s != AR_OK) return s;
+  }
+  return AR_OK;
+}
+
+ar_status_t ar_bucket_plan(int ntensors, const size_t* nbytes, size_t cap_bytes, int* bucket_of,
+                           int* nbuckets) {
+  if (ntensors < 0 || cap_bytes == 0 || nbuckets == nullptr) return AR_ERR_INVALID_ARG;
+  if (ntensors > 0 && (nbytes == nullptr || bucket_of == nullptr)) return AR_ERR_INVALID_ARG;
+  int b = -1;
+  size_t fill = 0;
+  for (int t = ntensors - 1; t >= 0; --t) {
+    const bool full = fill > 0 && (fill > cap_bytes || nbytes[t] > cap_bytes - fill);
+    if (b < 0 || full) {
+      ++b;
+      fill = 0;
+    }
+    bucket_of[t] = b;
+    fill = nbytes[t] > SIZE_MAX - fill ? SIZE_MAX : fill + nbytes[t];
+  }
+  *nbuckets = b + 1;
+  return AR_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,174 @@
+// gar_device.cuh -- device helpers shared by the GB300 collective kernels:
+// 16-byte streaming loads/stores, bf16 <-> fp32 conversion, and the
+// rank-ordered fp32 reduction of one 16-byte vector position.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace gar {
+
+constexpr int kMaxRanks = 16;
+constexpr int kThreads = 256;  // threads per CTA of every kernel
+
+// ------------------------------------------------------------ memory ops
+// Every replica value is read exactly once and written at most once per
+// call, so loads bypass L1 (no reuse) and stores are streaming.  In place,
+// a thread reads a 16-byte position of every replica before it writes that
+// position and no other thread touches it, so the read-only (.nc) path
+// never sees a value written by the same kernel.
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ void st_stream(void* p, const uint4& v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// fp32 master-weight / momentum arrays are read and written by the same
+// thread (read-modify-write), so they use the coherent path.
+__device__ __forceinline__ float4 ld_f4(const float* p) {
+  float4 r;
+  asm volatile("ld.global.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ void st_f4(float* p, const float4& v) {
+  asm volatile("st.global.cs.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w)
+               : "memory");
+}
+
+// ------------------------------------------------------------- dtypes
+// bf16 is the upper half of an fp32 bit pattern: widening is a shift.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// fp32 -> bf16 by IEEE round-to-nearest-even on the 16 dropped bits: adding
+// 0x7FFF plus the lowest kept bit carries into the kept part exactly when
+// the dropped part is above one half, or exactly one half with an odd kept
+// part.  A carry out of the significand increments the exponent (and turns
+// overflow into infinity).  NaN stays NaN (quiet bit forced).
+__device__ __forceinline__ uint32_t bf16_rne(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (u >> 16) | 0x40u;
+  return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+}
+
+struct F32 {
+  static constexpr int kElems = 4;  // elements per 16-byte vector
+  static constexpr int kBytes = 4;
+  __device__ static __forceinline__ void unpack(const uint4& v, float (&f)[4]) {
+    f[0] = __uint_as_float(v.x);
+    f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z);
+    f[3] = __uint_as_float(v.w);
+  }
+  __device__ static __forceinline__ uint4 pack(const float (&f)[4]) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+  }
+  __device__ static __forceinline__ float load1(const void* p, uint64_t i) {
+    return static_cast<const float*>(p)[i];
+  }
+  __device__ static __forceinline__ void store1(void* p, uint64_t i, float f) {
+    static_cast<float*>(p)[i] = f;
+  }
+};
+
+struct BF16 {
+  static constexpr int kElems = 8;
+  static constexpr int kBytes = 2;
+  // Element 2k of a 32-bit word is its low half (little-endian order).
+  __device__ static __forceinline__ void unpack(const uint4& v, float (&f)[8]) {
+    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+    f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+    f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+  }
+  __device__ static __forceinline__ uint4 pack(const float (&f)[8]) {
+    return make_uint4(bf16_rne(f[0]) | (bf16_rne(f[1]) << 16),
+                      bf16_rne(f[2]) | (bf16_rne(f[3]) << 16),
+                      bf16_rne(f[4]) | (bf16_rne(f[5]) << 16),
+                      bf16_rne(f[6]) | (bf16_rne(f[7]) << 16));
+  }
+  __device__ static __forceinline__ float load1(const void* p, uint64_t i) {
+    return __uint_as_float(uint32_t(static_cast<const uint16_t*>(p)[i]) << 16);
+  }
+  __device__ static __forceinline__ void store1(void* p, uint64_t i, float f) {
+    static_cast<uint16_t*>(p)[i] = static_cast<uint16_t>(bf16_rne(f));
+  }
+};
+
+// ---------------------------------------------------------- reduction
+// PT > 0: P is the compile-time constant PT.  PT == 0: P is the runtime
+// value np (1 <= np <= kMaxRanks); loops run to kMaxRanks under a guard so
+// the operands stay in registers.
+template <int PT>
+struct Ranks {
+  static constexpr int kMax = PT > 0 ? PT : kMaxRanks;
+  __device__ static __forceinline__ bool has(int r, int np) { return PT > 0 ? r < PT : r < np; }
+  __device__ static __forceinline__ int count(int np) { return PT > 0 ? PT : np; }
+};
+
+// Mean: one correctly rounded fp32 division by P.  For P a power of two
+// the product with the exact reciprocal is the same correctly rounded
+// quotient, so the compile-time powers of two multiply instead.
+template <int PT>
+__device__ __forceinline__ float mean_of(float sum, int np) {
+  if constexpr (PT > 0 && (PT & (PT - 1)) == 0) {
+    return __fmul_rn(sum, 1.0f / float(PT));
+  } else {
+    return __fdiv_rn(sum, float(Ranks<PT>::count(np)));
+  }
+}
+
+// acc[e] = in[0][e] + in[1][e] + ... + in[P-1][e], left to right in fp32,
+// seeded with rank 0's value; then divided by P when mean is set.
+template <class D, int PT>
+__device__ __forceinline__ void reduce_vec(const uint4 (&in)[Ranks<PT>::kMax], int np, bool mean,
+                                           float (&acc)[D::kElems]) {
+  D::unpack(in[0], acc);
+#pragma unroll
+  for (int r = 1; r < Ranks<PT>::kMax; ++r) {
+    if (Ranks<PT>::has(r, np)) {
+      float x[D::kElems];
+      D::unpack(in[r], x);
+#pragma unroll
+      for (int e = 0; e < D::kElems; ++e) acc[e] = __fadd_rn(acc[e], x[e]);
+    }
+  }
+  if (mean) {
+#pragma unroll
+    for (int e = 0; e < D::kElems; ++e) acc[e] = mean_of<PT>(acc[e], np);
+  }
+}
+
+// The same for one element read with scalar loads (ragged tails and
+// buffers that are not 16-byte aligned).
+template <class D, int PT>
+__device__ __forceinline__ float reduce_scalar(const void* const* src, uint64_t i, int np,
+                                               bool mean) {
+  float acc = D::load1(src[0], i);
+#pragma unroll
+  for (int r = 1; r < Ranks<PT>::kMax; ++r)
+    if (Ranks<PT>::has(r, np)) acc = __fadd_rn(acc, D::load1(src[r], i));
+  return mean ? mean_of<PT>(acc, np) : acc;
+}
+
+// SGD with momentum on one element: v = fl(fl(mu*v) + g); w = fl(w - fl(lr*v)).
+__device__ __forceinline__ void sgd_step(float g, float lr, float mu, float& w, float& v) {
+  v = __fadd_rn(__fmul_rn(mu, v), g);
+  w = __fsub_rn(w, __fmul_rn(lr, v));
+}
+
+}  // namespace gar

@@ -1,0 +1,210 @@
+// gar_kernels.cuh -- the two kernel families of the library.
+//
+// k_reduce: the rank-ordered reduction over P replica pointers.  One launch
+// covers a list of "segments" -- a flat all-reduce is one segment, a
+// reduce-scatter is P segments (one per shard), a gradient bucket is one
+// segment per tensor.  Each segment has P source pointers and ndst
+// destination pointers (every replica for an all-reduce, the owning rank
+// for a reduce-scatter) and optionally fp32 master-weight / momentum arrays
+// for the fused SGD step.
+//
+// k_copy: one source, several destinations (all-gather: one segment per
+// source shard; broadcast: one segment from the root).
+//
+// Work is cut into tiles of kThreads * U 16-byte vectors of one segment.
+// CTAs are persistent: CTA b takes tiles b, b + G, b + 2G, ...; the host
+// picks G so that every CTA gets the same number of tiles (to within one).
+// The segment table travels by value in the kernel's parameter space
+// (__grid_constant__), so a launch needs no device-side table and no copy.
+#pragma once
+
+#include "gar_device.cuh"
+
+namespace gar {
+
+// Vectors per thread per tile: enough 16-byte loads in flight per thread
+// (P * U * 16 bytes) to cover HBM latency, bounded by registers.
+__host__ __device__ constexpr int unroll_for(int PT) {
+  return PT == 0 ? 1 : (PT <= 4 ? 4 : (PT <= 8 ? 2 : 1));
+}
+constexpr int kCopyUnroll = 4;
+
+// Segment table capacities: small launches (<= 16 segments) use a 4 KB
+// parameter block, large ones (<= 256 segments) about 25 KB, inside the
+// 32,764-byte kernel-parameter limit.
+struct CapSmall { static constexpr int kSeg = 16, kPtr = 512; };
+struct CapLarge { static constexpr int kSeg = 256, kPtr = 2048; };
+
+enum : uint32_t { kSegVec = 1u };  // all pointers of the segment 16-byte aligned
+
+template <class Cap>
+struct SegTable {
+  uint32_t nseg;              // segments in this launch
+  uint32_t ntiles;            // total tiles (= tile0[nseg])
+  int np;                     // P: source pointers per segment (k_reduce)
+  int ndst;                   // destination pointers per segment
+  int stride;                 // pointers per segment in ptr[]
+  int dst_off;                // index of the first destination within a segment
+  int mean;                   // divide by P
+  int write_back;             // SGD: also store the reduced gradient
+  float lr, mu;               // SGD hyper-parameters
+  uint32_t tile0[Cap::kSeg + 1];  // first tile of each segment; tile0[nseg] = ntiles
+  uint64_t numel[Cap::kSeg];      // elements (k_reduce) or bytes (k_copy) per segment
+  uint32_t flags[Cap::kSeg];
+  float* master[Cap::kSeg];       // SGD fp32 weights (k_reduce with SGD)
+  float* mom[Cap::kSeg];          // SGD fp32 momentum
+  void* ptr[Cap::kPtr];           // segment s: ptr[s*stride + 0 .. stride)
+};
+
+// --------------------------------------------------------------- reduce
+
+template <class D, bool SGD>
+__device__ __forceinline__ void epilogue_vec(float (&g)[D::kElems], float* w, float* v,
+                                             uint64_t e0, float lr, float mu) {
+  static_assert(D::kElems % 4 == 0, "vector holds whole float4 groups");
+  if constexpr (SGD) {
+#pragma unroll
+    for (int q = 0; q < D::kElems / 4; ++q) {
+      float4 wq = ld_f4(w + e0 + 4 * q);
+      float4 vq = ld_f4(v + e0 + 4 * q);
+      sgd_step(g[4 * q + 0], lr, mu, wq.x, vq.x);
+      sgd_step(g[4 * q + 1], lr, mu, wq.y, vq.y);
+      sgd_step(g[4 * q + 2], lr, mu, wq.z, vq.z);
+      sgd_step(g[4 * q + 3], lr, mu, wq.w, vq.w);
+      st_f4(v + e0 + 4 * q, vq);
+      st_f4(w + e0 + 4 * q, wq);
+    }
+  }
+}
+
+template <class D, int PT, bool SGD, class Cap>
+__global__ void __launch_bounds__(kThreads)
+    k_reduce(const __grid_constant__ SegTable<Cap> a) {
+  constexpr int U = unroll_for(PT);
+  constexpr int E = D::kElems;
+  constexpr int MAXP = Ranks<PT>::kMax;
+  constexpr uint64_t kTileVec = uint64_t(U) * kThreads;
+  const int np = a.np;
+  const bool mean = a.mean != 0;
+  uint32_t s = 0;
+  for (uint32_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
+    while (tile >= a.tile0[s + 1]) ++s;  // tiles are visited in increasing order
+    const uint64_t n = a.numel[s];
+    void* const* seg = a.ptr + uint64_t(s) * a.stride;
+    void* const* dst = seg + a.dst_off;
+    const uint64_t lt = tile - a.tile0[s];
+    const bool do_store = !SGD || a.write_back;
+    float* w = SGD ? a.master[s] : nullptr;
+    float* v = SGD ? a.mom[s] : nullptr;
+
+    if (a.flags[s] & kSegVec) {
+      const uint64_t nvec = n / E;
+      const uint64_t v0 = lt * kTileVec + threadIdx.x;
+      uint4 in[U][MAXP];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint64_t vi = v0 + uint64_t(u) * kThreads;
+        if (vi < nvec) {
+#pragma unroll
+          for (int r = 0; r < MAXP; ++r)
+            if (Ranks<PT>::has(r, np))
+              in[u][r] = ld_stream(static_cast<const uint4*>(seg[r]) + vi);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint64_t vi = v0 + uint64_t(u) * kThreads;
+        if (vi < nvec) {
+          float g[E];
+          reduce_vec<D, PT>(in[u], np, mean, g);
+          epilogue_vec<D, SGD>(g, w, v, vi * E, a.lr, a.mu);
+          if (do_store) {
+            const uint4 out = D::pack(g);
+            for (int d = 0; d < a.ndst; ++d) st_stream(static_cast<uint4*>(dst[d]) + vi, out);
+          }
+        }
+      }
+      // The last tile of a segment also takes its ragged tail (< E elements).
+      if (lt + 1 == a.tile0[s + 1] - a.tile0[s]) {
+        const uint64_t i = nvec * E + threadIdx.x;
+        if (i < n) {
+          float g = reduce_scalar<D, PT>(seg, i, np, mean);
+          if constexpr (SGD) sgd_step(g, a.lr, a.mu, w[i], v[i]);
+          if (do_store)
+            for (int d = 0; d < a.ndst; ++d) D::store1(dst[d], i, g);
+        }
+      }
+    } else {
+      // Unaligned segment: the same tile of elements with scalar accesses.
+      const uint64_t e0 = lt * kTileVec * E;
+      for (uint64_t k = threadIdx.x; k < kTileVec * E; k += kThreads) {
+        const uint64_t i = e0 + k;
+        if (i >= n) break;
+        float g = reduce_scalar<D, PT>(seg, i, np, mean);
+        if constexpr (SGD) sgd_step(g, a.lr, a.mu, w[i], v[i]);
+        if (do_store)
+          for (int d = 0; d < a.ndst; ++d) D::store1(dst[d], i, g);
+      }
+    }
+  }
+}
+
+// ----------------------------------------------------------------- copy
+// numel[s] is in bytes (always even: elements are 2 or 4 bytes); segment s
+// has flags[s] >> 8 destinations (an in-place all-gather skips the shard
+// that is already in place).
+template <class Cap>
+__global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTable<Cap> a) {
+  constexpr uint64_t kTileVec = uint64_t(kCopyUnroll) * kThreads;
+  uint32_t s = 0;
+  for (uint32_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
+    while (tile >= a.tile0[s + 1]) ++s;
+    const uint64_t nbytes = a.numel[s];
+    void* const* seg = a.ptr + uint64_t(s) * a.stride;
+    const void* src = seg[0];
+    void* const* dst = seg + a.dst_off;
+    const uint64_t lt = tile - a.tile0[s];
+    const int nd = int(a.flags[s] >> 8);
+    if (a.flags[s] & kSegVec) {
+      const uint64_t nvec = nbytes / 16;
+      const uint64_t v0 = lt * kTileVec + threadIdx.x;
+      uint4 x[kCopyUnroll];
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) {
+        const uint64_t vi = v0 + uint64_t(u) * kThreads;
+        if (vi < nvec) x[u] = ld_stream(static_cast<const uint4*>(src) + vi);
+      }
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) {
+        const uint64_t vi = v0 + uint64_t(u) * kThreads;
+        if (vi < nvec)
+          for (int d = 0; d < nd; ++d) st_stream(static_cast<uint4*>(dst[d]) + vi, x[u]);
+      }
+      if (lt + 1 == a.tile0[s + 1] - a.tile0[s]) {
+        const uint64_t h = (nvec * 16) / 2 + threadIdx.x;  // 2-byte units of the tail
+        if (h < nbytes / 2) {
+          const uint16_t x1 = static_cast<const uint16_t*>(src)[h];
+          for (int d = 0; d < nd; ++d) static_cast<uint16_t*>(dst[d])[h] = x1;
+        }
+      }
+    } else {
+      const uint64_t h0 = lt * kTileVec * 8;  // 2-byte units per tile
+      for (uint64_t k = threadIdx.x; k < kTileVec * 8; k += kThreads) {
+        const uint64_t h = h0 + k;
+        if (h >= nbytes / 2) break;
+        const uint16_t x1 = static_cast<const uint16_t*>(src)[h];
+        for (int d = 0; d < nd; ++d) static_cast<uint16_t*>(dst[d])[h] = x1;
+      }
+    }
+  }
+}
+
+// Tiles of one segment, as the kernels above cut it.
+__host__ __device__ constexpr uint64_t reduce_tile_elems(int PT, int elems_per_vec) {
+  return uint64_t(unroll_for(PT)) * kThreads * elems_per_vec;
+}
+__host__ __device__ constexpr uint64_t copy_tile_bytes() {
+  return uint64_t(kCopyUnroll) * kThreads * 16;
+}
+
+}  // namespace gar

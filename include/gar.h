@@ -1,0 +1,214 @@
+/*
+ * gar.h -- C ABI of libgar.so, the GB300 gradient all-reduce library.
+ *
+ * A device group of P participants (ranks) is P replica buffers resident in
+ * the HBM of one GPU.  Each collective is one kernel pass over all P
+ * replicas: it reads every participant's tensor and writes the result for
+ * every participant.  The calls follow the problem as the pages state it:
+ *   - a device group with a default reduction, created before any
+ *     collective and alive while the group is in use (Burn's
+ *     DistributedContext::init(devices, DistributedConfig{all_reduce_op})
+ *     and its Drop; pgsm.cn/news/420861, "Distributed tensor operations" and
+ *     "Lifetime and implementation details");
+ *   - ReduceOperation Sum or Mean (same page, "Reduction configuration";
+ *     "Lecture 8 -- Parallelism", rd.me/cs336/lec8, Part 1 s.2: SUM or AVG);
+ *   - the same tensor on every participant, the result returned to each
+ *     (same page, all_reduce; Lecture 8, dist.all_reduce);
+ *   - results that are asynchronous until synchronised (same page,
+ *     CollectiveTensor::resolve): every call enqueues work on the caller's
+ *     CUDA stream and returns; the output is valid once that stream has
+ *     reached the call (cudaStreamSynchronize, an event, or later work on the
+ *     same stream).
+ * Because one call takes all P participants at once, the pages' rule that
+ * every participant joins the same collectives in a compatible order holds
+ * by construction.
+ *
+ * Numerics (identical to the CPU oracle bit for bit): element i of the
+ * result is x_0[i] + x_1[i] + ... + x_{P-1}[i], added left to right in IEEE
+ * fp32 starting from x_0[i]; Mean then divides once by P in fp32 (correctly
+ * rounded).  bf16 inputs widen exactly to fp32 and the fp32 result is
+ * rounded once to bf16 (nearest, ties to even).  A NaN result is a NaN; its
+ * payload is not specified.
+ *
+ * Ownership: the caller owns every buffer and stream.  The library never
+ * allocates or frees caller memory; a comm owns one small device status
+ * word.  Pointers: device memory (or memory the device can address) on the
+ * comm's device, aligned to the element size; 16-byte alignment selects the
+ * vectorised path, other alignments run a scalar path with the same
+ * results.  Counts are elements per participant; count == 0 is a no-op.
+ * Errors: every call validates its arguments on the host before enqueueing
+ * anything and returns AR_ERR_INVALID_ARG with nothing enqueued when they
+ * are wrong; AR_ERR_CUDA reports a failed CUDA call or launch.
+ * Threading: a comm is not thread-safe; calls on one comm must be
+ * serialised by the caller.  Calls leave the calling thread's current
+ * CUDA device unchanged.
+ */
+#ifndef GAR_H
+#define GAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define AR_MAX_RANKS 16
+
+typedef struct ar_comm_s *ar_comm_t;
+
+typedef enum {
+    AR_OK = 0,
+    AR_ERR_INVALID_ARG = 1, /* bad argument; nothing was enqueued */
+    AR_ERR_UNSUPPORTED = 2, /* no sm_103a device, or a feature not built */
+    AR_ERR_CUDA = 3,        /* a CUDA runtime call or a kernel launch failed */
+    AR_ERR_TIMEOUT = 4,     /* a device-side bounded wait gave up */
+    AR_ERR_STATE = 5        /* a comm used after ar_destroy, or not from ar_init */
+} ar_status_t;
+
+/* ReduceOperation.  AR_OP_DEFAULT selects the comm's default_op. */
+typedef enum { AR_OP_DEFAULT = -1, AR_SUM = 0, AR_MEAN = 1 } ar_op_t;
+
+/* Element types: IEEE binary32, and bfloat16 (the upper half of a binary32). */
+typedef enum { AR_F32 = 0, AR_BF16 = 1 } ar_dtype_t;
+
+/* A CUDA stream handle (cudaStream_t); NULL is the legacy default stream. */
+typedef void *ar_stream_t;
+
+/*
+ * Create a device group of nranks participants (1 <= nranks <= AR_MAX_RANKS)
+ * on CUDA device cuda_device, with default reduction default_op (AR_SUM or
+ * AR_MEAN).  Cites DistributedContext::init and DistributedConfig
+ * (pgsm.cn/news/420861, "Distributed tensor operations").  On success *comm
+ * holds the new handle; it allocates a 4-byte device status word.
+ * Errors: AR_ERR_INVALID_ARG (null comm, nranks or default_op out of range,
+ * no such device), AR_ERR_UNSUPPORTED (the device is not sm_103),
+ * AR_ERR_CUDA.
+ */
+ar_status_t ar_init(ar_comm_t *comm, int nranks, int cuda_device, ar_op_t default_op);
+
+/*
+ * Destroy a group (the Drop of DistributedContext, same page, "Lifetime and
+ * implementation details").  Waits for the device to finish work that may
+ * use the status word, then frees it.  AR_ERR_STATE for a handle that is
+ * not live.
+ */
+ar_status_t ar_destroy(ar_comm_t comm);
+
+/*
+ * All-reduce (Lecture 8, Part 1 s.2, dist.all_reduce; "Distributed
+ * Training", computervisiononline.com, "Data parallelism and all-reduce").
+ * send[r], recv[r] (host arrays of P device pointers): count elements each.
+ * recv[r][i] = reduce_op(send[0][i], ..., send[P-1][i]) for every rank r.
+ * recv[r] == send[r] is in place; otherwise recv[r] must not overlap any
+ * send[q] or recv[q].  recv buffers of different ranks must be disjoint;
+ * send buffers may overlap each other (they are only read).
+ */
+ar_status_t ar_all_reduce(ar_comm_t comm, const void *const *send, void *const *recv,
+                          size_t count, ar_dtype_t dtype, ar_op_t op, ar_stream_t stream);
+
+/*
+ * Reduce-scatter (Lecture 8, Part 1 s.2, dist.reduce_scatter;
+ * burn-distributed, "Collective operations").  count % P == 0; shard
+ * s = count / P.  send[r]: count elements; recv[r]: s elements.
+ * recv[r][j] = reduce_op(send[.][r*s + j]): rank r keeps the contiguous
+ * shard r.  In place iff recv[r] == send[r] + r*s (elements); otherwise
+ * recv[r] must not overlap any send or other recv.
+ */
+ar_status_t ar_reduce_scatter(ar_comm_t comm, const void *const *send, void *const *recv,
+                              size_t count, ar_dtype_t dtype, ar_op_t op, ar_stream_t stream);
+
+/*
+ * All-gather (Lecture 8, Part 1 s.2, dist.all_gather; "Distributed
+ * Training", FSDP paragraphs).  count % P == 0 is the TOTAL length;
+ * s = count / P.  send[r]: s elements; recv[r]: count elements.
+ * recv[r][q*s + j] = send[q][j], a bit copy in rank order.  In place iff
+ * send[r] == recv[r] + r*s; otherwise send and recv must not overlap.
+ */
+ar_status_t ar_all_gather(ar_comm_t comm, const void *const *send, void *const *recv,
+                          size_t count, ar_dtype_t dtype, ar_stream_t stream);
+
+/*
+ * Broadcast (Lecture 8, Part 1 s.2, dist.broadcast; burn-distributed,
+ * "Collective operations"; DDP's broadcast of rank 0's state, "Distributed
+ * Training", "Data parallelism and all-reduce").  buf[r]: count elements;
+ * afterwards every buf[r] holds buf[root]'s bytes; buf[root] is only read.
+ * The P buffers must be disjoint; 0 <= root < P.
+ */
+ar_status_t ar_broadcast(ar_comm_t comm, void *const *buf, size_t count, ar_dtype_t dtype,
+                         int root, ar_stream_t stream);
+
+/*
+ * A gradient bucket: ntensors tensors of one dtype, each with P replicas.
+ * dev_ptrs is a HOST array of ntensors*P device pointers, tensor-major
+ * (dev_ptrs[t*P + r] is rank r's copy of tensor t); numel is a HOST array of
+ * ntensors lengths.  Buckets of about 25 MB, filled in reverse parameter
+ * order, one collective per bucket ("Distributed Training", "Data
+ * parallelism and all-reduce"); see ar_bucket_plan.
+ */
+typedef struct {
+    int ntensors;
+    void *const *dev_ptrs;
+    const size_t *numel;
+    ar_dtype_t dtype;
+} ar_bucket_t;
+
+/*
+ * The optimizer step that follows the all-reduce (Lecture 8, Part 2 s.1,
+ * step 4, optimizer.step()), as SGD with momentum (dampening 0): for each
+ * element, with g the fp32 reduced gradient before any bf16 rounding,
+ *     v = fl(fl(momentum * v) + g),   w = fl(w - fl(lr * v)).
+ * master[t] and momentum_buf[t] (HOST arrays of ntensors device pointers)
+ * are fp32 arrays of numel[t] elements, shared by all replicas (they hold
+ * the same values after the all-reduce).  write_back_grads != 0 also stores
+ * the reduced gradient (rounded to the bucket dtype) into every replica; 0
+ * leaves the gradient replicas untouched.
+ */
+typedef struct {
+    float lr;
+    float momentum;
+    float *const *master;
+    float *const *momentum_buf;
+    int write_back_grads;
+} ar_sgd_t;
+
+/*
+ * Bucketed all-reduce, in place: every tensor of the bucket is all-reduced
+ * exactly as ar_all_reduce would (bucketing cannot change values), in one
+ * kernel launch for buckets of up to 256 tensors at P <= 8 (128 at P <= 16;
+ * larger buckets take one launch per such group).  sgd == NULL: results go
+ * to every replica.  sgd != NULL: the fused SGD-momentum step above.  All
+ * buffers (replicas, master, momentum) must be pairwise disjoint.
+ */
+ar_status_t ar_bucket_all_reduce(ar_comm_t comm, const ar_bucket_t *bucket, ar_op_t op,
+                                 const ar_sgd_t *sgd, ar_stream_t stream);
+
+/*
+ * Bucket assignment, host only.  nbytes[t] is tensor t's size in
+ * registration order.  Tensors are taken from the last to the first and
+ * added to the open bucket; one that would take a non-empty bucket past
+ * cap_bytes opens a new bucket first, so a tensor larger than the cap sits
+ * alone ("Distributed Training", "Data parallelism and all-reduce": 25 MB
+ * buckets, reverse parameter order).  bucket_of[t] receives tensor t's
+ * bucket index (buckets numbered in fill order); *nbuckets their number.
+ * Errors: AR_ERR_INVALID_ARG for ntensors < 0, cap_bytes == 0, or null
+ * outputs (bucket_of may be null when ntensors == 0).
+ */
+ar_status_t ar_bucket_plan(int ntensors, const size_t *nbytes, size_t cap_bytes,
+                           int *bucket_of, int *nbuckets);
+
+/*
+ * Sticky device-side status of a comm: AR_ERR_TIMEOUT once a kernel's
+ * bounded wait has given up, AR_ERR_CUDA for a sticky CUDA error on the
+ * device, else AR_OK.  Synchronises the device (it reads the status word).
+ */
+ar_status_t ar_get_async_error(ar_comm_t comm);
+
+/* A static, human-readable name for a status code. */
+const char *ar_status_string(ar_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GAR_H */

@@ -1,0 +1,129 @@
+"""GPU parity of the bucketed all-reduce and its fused SGD-momentum step
+through the C ABI, against the CPU oracle, bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import gradient_all_reduce_gb300 as gar
+import oracle
+import workloads
+from gpucase import (DT, OP, ORACLE_OP, assert_bits_equal, dev, empty, replicas, to_np)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _bucket(P, sizes, dt, seed0, offset=0):
+    """Tensor t's replica r: draws of stream seed0 + 100 t + r (device)."""
+    return [replicas(P, n, dt, "normal", seed0 + 100 * t, offset=offset)
+            for t, n in enumerate(sizes)]
+
+
+def _host(P, sizes, dt, seed0):
+    return [[workloads.replica_values("normal", dt, seed0 + 100 * t + r, n) for r in range(P)]
+            for t, n in enumerate(sizes)]
+
+
+SHAPES = [(1,), (7,), (768,), (1000,), (2304, 768), (3,), (65_536 + 13,)]
+
+
+@pytest.mark.parametrize("P", [2, 3, 4, 8])
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("op", ["sum", "mean"])
+def test_bucket_equals_oracle(cuda, P, dt, op):
+    sizes = [int(np.prod(s)) for s in SHAPES]
+    comm = gar.ar_init(P, 0, gar.AR_MEAN)
+    try:
+        ts = _bucket(P, sizes, dt, 1)
+        gar.ar_bucket_all_reduce(comm, ts, sizes, DT[dt], OP[op])
+        torch.cuda.synchronize()
+    finally:
+        gar.ar_destroy(comm)
+    host = _host(P, sizes, dt, 1)
+    oracle.bucket_all_reduce(host, op=ORACLE_OP[op])
+    for t in range(len(sizes)):
+        for r in range(P):
+            assert_bits_equal(to_np(ts[t][r]), host[t][r], f"tensor {t} rank {r}")
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("write_back", [0, 1])
+@pytest.mark.parametrize("aligned", [True, False])
+def test_bucket_sgd_equals_oracle(cuda, dt, write_back, aligned):
+    """Two steps of the fused Mean + SGD(momentum 0.9, lr 0.1) on fp32
+    master weights ~N(0, 0.02) and zero momentum."""
+    P = 8
+    sizes = [int(np.prod(s)) for s in SHAPES]
+    off = 0 if aligned else 1
+    ts = _bucket(P, sizes, dt, 2, offset=off)
+    host = _host(P, sizes, dt, 2)
+    ws, vs, hw, hv = [], [], [], []
+    for t, n in enumerate(sizes):
+        w = empty(n, "f32", off)
+        from workloads import gpu as wgpu
+        wgpu.fill(w, "normal", 200 + t, std=0.02)
+        ws.append(w)
+        vs.append(torch.zeros(n + off, dtype=torch.float32, device=dev())[off:])
+        hw.append(workloads.normal_f32(200 + t, n, std=0.02))
+        hv.append(np.zeros(n, np.float32))
+    comm = gar.ar_init(P, 0, gar.AR_MEAN)
+    try:
+        for step in range(2):
+            gar.ar_bucket_all_reduce(comm, ts, sizes, DT[dt], gar.AR_MEAN,
+                                     sgd=(0.1, 0.9, ws, vs, write_back))
+            torch.cuda.synchronize()
+            oracle.bucket_all_reduce(host, op=oracle.MEAN,
+                                     sgd=(0.1, 0.9, hw, hv, write_back))
+            for t in range(len(sizes)):
+                assert_bits_equal(to_np(ws[t]), hw[t], f"step {step} w {t}")
+                assert_bits_equal(to_np(vs[t]), hv[t], f"step {step} v {t}")
+                for r in (0, P - 1):
+                    assert_bits_equal(to_np(ts[t][r]), host[t][r], f"step {step} g {t}/{r}")
+    finally:
+        gar.ar_destroy(comm)
+
+
+def test_bucket_larger_than_one_parameter_block(cuda):
+    """600 small tensors at P=4 (more than one launch's segment table):
+    results equal the per-tensor oracle."""
+    P = 4
+    rng = np.random.default_rng(0)
+    sizes = [int(s) for s in rng.integers(1, 3000, size=600)]
+    flat = sum(sizes)
+    base = replicas(P, flat, "bf16", "normal", 300)
+    ts, off = [], 0
+    for n in sizes:
+        ts.append([b[off:off + n] for b in base])
+        off += n
+    comm = gar.ar_init(P, 0, gar.AR_MEAN)
+    try:
+        gar.ar_bucket_all_reduce(comm, ts, sizes, gar.AR_BF16)
+        torch.cuda.synchronize()
+    finally:
+        gar.ar_destroy(comm)
+    host = [workloads.replica_values("normal", "bf16", 300 + r, flat) for r in range(P)]
+    want = oracle.all_reduce(host, op=oracle.MEAN)
+    for r in range(P):
+        assert_bits_equal(to_np(base[r]), want[r], f"rank {r}")
+
+
+def test_bucket_rejects_overlap(cuda):
+    P = 2
+    x = replicas(P, 1000, "f32", "uniform", 1)
+    comm = gar.ar_init(P, 0, gar.AR_SUM)
+    try:
+        with pytest.raises(gar.GarError) as e:
+            gar.ar_bucket_all_reduce(comm, [[x[0][:600], x[1][:600]], [x[0][500:], x[1][500:]]],
+                                     [600, 500], gar.AR_F32)
+        assert e.value.status == gar.AR_ERR_INVALID_ARG
+        w = torch.zeros(1000, device=dev())
+        with pytest.raises(gar.GarError):
+            gar.ar_bucket_all_reduce(comm, [x], [1000], gar.AR_F32,
+                                     sgd=(0.1, 0.9, [w], [w], 1))   # master aliases momentum
+    finally:
+        gar.ar_destroy(comm)
