@@ -8,8 +8,8 @@ objects with ``cuda_stream`` (torch.cuda.Stream), or None for the current
 torch stream (the legacy default stream when torch is not imported).
 
 The library must be built first (``gradient_all_reduce_gb300.build.build()``
-or ``__graft_entry__.build()``); importing this module without it raises
-ImportError -- there is no fallback implementation.
+or ``__graft_entry__.build()``).  It is loaded on first use; without it
+every call raises ImportError -- there is no fallback implementation.
 """
 from __future__ import annotations
 
@@ -76,11 +76,25 @@ def _load() -> ctypes.CDLL:
     return lib
 
 
-lib = _load()
+_HANDLE: ctypes.CDLL | None = None
+
+
+def load() -> ctypes.CDLL:
+    """The loaded libgar.so (loaded on first call; ImportError if missing)."""
+    global _HANDLE
+    if _HANDLE is None:
+        _HANDLE = _load()
+    return _HANDLE
+
+
+def __getattr__(name):
+    if name == "lib":
+        return load()
+    raise AttributeError(name)
 
 
 def ar_status_string(status: int) -> str:
-    return lib.ar_status_string(int(status)).decode()
+    return load().ar_status_string(int(status)).decode()
 
 
 def _ok(status: int, what: str) -> None:
@@ -112,35 +126,35 @@ def _stream(stream) -> int:
 def ar_init(nranks: int, cuda_device: int = 0, default_op: int = AR_MEAN) -> int:
     """Create a device group of ``nranks`` replicas; returns the comm handle."""
     comm = ctypes.c_void_p()
-    _ok(lib.ar_init(ctypes.byref(comm), int(nranks), int(cuda_device), int(default_op)), "ar_init")
+    _ok(load().ar_init(ctypes.byref(comm), int(nranks), int(cuda_device), int(default_op)), "ar_init")
     return int(comm.value)
 
 
 def ar_destroy(comm: int) -> None:
-    _ok(lib.ar_destroy(comm), "ar_destroy")
+    _ok(load().ar_destroy(comm), "ar_destroy")
 
 
 def ar_all_reduce(comm: int, send: Sequence, recv: Sequence, count: int, dtype: int,
                   op: int = AR_OP_DEFAULT, stream=None) -> None:
-    _ok(lib.ar_all_reduce(comm, _ptr_array(send), _ptr_array(recv), int(count), int(dtype),
+    _ok(load().ar_all_reduce(comm, _ptr_array(send), _ptr_array(recv), int(count), int(dtype),
                           int(op), _stream(stream)), "ar_all_reduce")
 
 
 def ar_reduce_scatter(comm: int, send: Sequence, recv: Sequence, count: int, dtype: int,
                       op: int = AR_OP_DEFAULT, stream=None) -> None:
-    _ok(lib.ar_reduce_scatter(comm, _ptr_array(send), _ptr_array(recv), int(count), int(dtype),
+    _ok(load().ar_reduce_scatter(comm, _ptr_array(send), _ptr_array(recv), int(count), int(dtype),
                               int(op), _stream(stream)), "ar_reduce_scatter")
 
 
 def ar_all_gather(comm: int, send: Sequence, recv: Sequence, count: int, dtype: int,
                   stream=None) -> None:
-    _ok(lib.ar_all_gather(comm, _ptr_array(send), _ptr_array(recv), int(count), int(dtype),
+    _ok(load().ar_all_gather(comm, _ptr_array(send), _ptr_array(recv), int(count), int(dtype),
                           _stream(stream)), "ar_all_gather")
 
 
 def ar_broadcast(comm: int, buf: Sequence, count: int, dtype: int, root: int = 0,
                  stream=None) -> None:
-    _ok(lib.ar_broadcast(comm, _ptr_array(buf), int(count), int(dtype), int(root),
+    _ok(load().ar_broadcast(comm, _ptr_array(buf), int(count), int(dtype), int(root),
                          _stream(stream)), "ar_broadcast")
 
 
@@ -159,7 +173,7 @@ def ar_bucket_all_reduce(comm: int, tensors: Sequence[Sequence], numel: Sequence
         m, v = _ptr_array(master), _ptr_array(mbuf)
         s = ar_sgd_t(float(lr), float(mom), ctypes.cast(m, ctypes.POINTER(ctypes.c_void_p)),
                      ctypes.cast(v, ctypes.POINTER(ctypes.c_void_p)), int(bool(wb)))
-    _ok(lib.ar_bucket_all_reduce(comm, ctypes.byref(b), int(op),
+    _ok(load().ar_bucket_all_reduce(comm, ctypes.byref(b), int(op),
                                  ctypes.byref(s) if s is not None else None, _stream(stream)),
         "ar_bucket_all_reduce")
 
@@ -170,13 +184,13 @@ def ar_bucket_plan(nbytes: Sequence[int], cap_bytes: int = 25 << 20) -> list[int
     nb = (ctypes.c_size_t * max(T, 1))(*[int(n) for n in nbytes])
     out = (ctypes.c_int * max(T, 1))()
     k = ctypes.c_int()
-    _ok(lib.ar_bucket_plan(T, nb, int(cap_bytes), out, ctypes.byref(k)), "ar_bucket_plan")
+    _ok(load().ar_bucket_plan(T, nb, int(cap_bytes), out, ctypes.byref(k)), "ar_bucket_plan")
     return list(out)[:T]
 
 
 def ar_get_async_error(comm: int) -> int:
     """The comm's sticky device-side status (an ar_status_t, not raised)."""
-    return int(lib.ar_get_async_error(comm))
+    return int(load().ar_get_async_error(comm))
 
 
 class PreparedBucket:
@@ -198,8 +212,9 @@ class PreparedBucket:
             self._sgd = ar_sgd_t(float(lr), float(mom),
                                  ctypes.cast(self._m, ctypes.POINTER(ctypes.c_void_p)),
                                  ctypes.cast(self._v, ctypes.POINTER(ctypes.c_void_p)), int(bool(wb)))
+        self._fn = load().ar_bucket_all_reduce
         self._args = (comm, ctypes.byref(self._bucket), int(op),
                       ctypes.byref(self._sgd) if self._sgd is not None else None)
 
     def __call__(self, stream=None) -> None:
-        _ok(lib.ar_bucket_all_reduce(*self._args, _stream(stream)), "ar_bucket_all_reduce")
+        _ok(self._fn(*self._args, _stream(stream)), "ar_bucket_all_reduce")
