@@ -293,6 +293,7 @@ ar_status_t ar_all_reduce(ar_comm_t comm, const void* const* send, void* const* 
   const size_t es = elem_bytes(dtype);
   size_t bytes;
   if (!mul_ok(count, es, &bytes)) return AR_ERR_INVALID_ARG;
+  if (count == 0) return AR_OK;
   DeviceGuard guard(comm->device);
   if (!guard.ok()) return AR_ERR_CUDA;
   for (int r = 0; r < P; ++r) {
@@ -305,7 +306,6 @@ ar_status_t ar_all_reduce(ar_comm_t comm, const void* const* send, void* const* 
       const bool in_place = q == r && recv[r] == send[r];
       if (!in_place && overlap(recv[r], bytes, send[q], bytes)) return AR_ERR_INVALID_ARG;
     }
-  if (count == 0) return AR_OK;
   for (int r = 0; r < P; ++r)
     if (!pointer_ok(comm, send[r], bytes) || !pointer_ok(comm, recv[r], bytes))
       return AR_ERR_INVALID_ARG;
@@ -334,6 +334,7 @@ ar_status_t ar_reduce_scatter(ar_comm_t comm, const void* const* send, void* con
   size_t bytes;
   if (!mul_ok(count, es, &bytes)) return AR_ERR_INVALID_ARG;
   const size_t sbytes = shard * es;
+  if (count == 0) return AR_OK;
   DeviceGuard guard(comm->device);
   if (!guard.ok()) return AR_ERR_CUDA;
   for (int r = 0; r < P; ++r) {
@@ -347,7 +348,6 @@ ar_status_t ar_reduce_scatter(ar_comm_t comm, const void* const* send, void* con
           q == r && addr(recv[r]) == addr(send[r]) + size_t(r) * sbytes;
       if (!in_place && overlap(recv[r], sbytes, send[q], bytes)) return AR_ERR_INVALID_ARG;
     }
-  if (count == 0) return AR_OK;
   for (int r = 0; r < P; ++r)
     if (!pointer_ok(comm, send[r], bytes) || !pointer_ok(comm, recv[r], sbytes))
       return AR_ERR_INVALID_ARG;
@@ -376,6 +376,7 @@ ar_status_t ar_all_gather(ar_comm_t comm, const void* const* send, void* const* 
   size_t bytes;
   if (!mul_ok(count, es, &bytes)) return AR_ERR_INVALID_ARG;
   const size_t sbytes = shard * es;
+  if (count == 0) return AR_OK;
   DeviceGuard guard(comm->device);
   if (!guard.ok()) return AR_ERR_CUDA;
   for (int r = 0; r < P; ++r) {
@@ -389,7 +390,6 @@ ar_status_t ar_all_gather(ar_comm_t comm, const void* const* send, void* const* 
           q == r && addr(send[r]) == addr(recv[r]) + size_t(r) * sbytes;
       if (!in_place && overlap(recv[r], bytes, send[q], sbytes)) return AR_ERR_INVALID_ARG;
     }
-  if (count == 0) return AR_OK;
   for (int r = 0; r < P; ++r)
     if (!pointer_ok(comm, send[r], sbytes) || !pointer_ok(comm, recv[r], bytes))
       return AR_ERR_INVALID_ARG;
@@ -420,6 +420,7 @@ ar_status_t ar_broadcast(ar_comm_t comm, void* const* buf, size_t count, ar_dtyp
   const size_t es = elem_bytes(dtype);
   size_t bytes;
   if (!mul_ok(count, es, &bytes)) return AR_ERR_INVALID_ARG;
+  if (count == 0) return AR_OK;
   DeviceGuard guard(comm->device);
   if (!guard.ok()) return AR_ERR_CUDA;
   for (int r = 0; r < P; ++r) {
@@ -427,7 +428,7 @@ ar_status_t ar_broadcast(ar_comm_t comm, void* const* buf, size_t count, ar_dtyp
     for (int q = 0; q < r; ++q)
       if (overlap(buf[r], bytes, buf[q], bytes)) return AR_ERR_INVALID_ARG;
   }
-  if (count == 0 || P == 1) return AR_OK;
+  if (P == 1) return AR_OK;
   for (int r = 0; r < P; ++r)
     if (!pointer_ok(comm, buf[r], bytes)) return AR_ERR_INVALID_ARG;
 
@@ -469,10 +470,11 @@ ar_status_t ar_bucket_all_reduce(ar_comm_t comm, const ar_bucket_t* bucket, ar_o
     size_t bytes, fbytes;
     if (!mul_ok(bucket->numel[t], es, &bytes) || !mul_ok(bucket->numel[t], 4, &fbytes))
       return AR_ERR_INVALID_ARG;
+    if (bytes == 0) continue;  // an empty tensor's pointers are not inspected
     for (int r = 0; r < P; ++r) {
       const void* p = bucket->dev_ptrs[size_t(t) * P + r];
       if (p == nullptr || !aligned(p, es)) return AR_ERR_INVALID_ARG;
-      if (bytes) ranges.push_back({addr(p), addr(p) + bytes});
+      ranges.push_back({addr(p), addr(p) + bytes});
     }
     if (sgd != nullptr) {
       const float* w = sgd->master[t];
@@ -491,6 +493,7 @@ ar_status_t ar_bucket_all_reduce(ar_comm_t comm, const ar_bucket_t* bucket, ar_o
     if (ranges[k].lo < ranges[k - 1].hi) return AR_ERR_INVALID_ARG;
   for (int t = 0; t < T; ++t) {
     const size_t n = bucket->numel[t];
+    if (n == 0) continue;
     for (int r = 0; r < P; ++r)
       if (!pointer_ok(comm, bucket->dev_ptrs[size_t(t) * P + r], n * es)) return AR_ERR_INVALID_ARG;
     if (sgd != nullptr &&

@@ -35,7 +35,8 @@
  * word.  Pointers: device memory (or memory the device can address) on the
  * comm's device, aligned to the element size; 16-byte alignment selects the
  * vectorised path, other alignments run a scalar path with the same
- * results.  Counts are elements per participant; count == 0 is a no-op.
+ * results.  Counts are elements per participant; count == 0 is a no-op that
+ * inspects no buffer pointer (they may be NULL).
  * Errors: every call validates its arguments on the host before enqueueing
  * anything and returns AR_ERR_INVALID_ARG with nothing enqueued when they
  * are wrong; AR_ERR_CUDA reports a failed CUDA call or launch.
