@@ -66,6 +66,7 @@ def _load() -> ctypes.CDLL:
         "ar_bucket_plan": [ctypes.c_int, ctypes.POINTER(ctypes.c_size_t), ctypes.c_size_t,
                            ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)],
         "ar_get_async_error": [P],
+        "ar_selftest_wait_timeout": [P, ctypes.c_uint, P],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
@@ -186,6 +187,11 @@ def ar_bucket_plan(nbytes: Sequence[int], cap_bytes: int = 25 << 20) -> list[int
     k = ctypes.c_int()
     _ok(load().ar_bucket_plan(T, nb, int(cap_bytes), out, ctypes.byref(k)), "ar_bucket_plan")
     return list(out)[:T]
+
+
+def ar_selftest_wait_timeout(comm: int, timeout_ms: int = 100, stream=None) -> None:
+    _ok(load().ar_selftest_wait_timeout(comm, int(timeout_ms), _stream(stream)),
+        "ar_selftest_wait_timeout")
 
 
 def ar_get_async_error(comm: int) -> int:

@@ -22,6 +22,8 @@ struct ar_comm_s {
   ar_op_t default_op;
   uint32_t* d_status;   // sticky device-side status word (0 = ok)
   bool check_pointers;  // validate every pointer against its allocation
+  int kernel_mode;      // 0 = by size, 1 = register-staged k_reduce, 2 = bulk-copy k_reduce_tma
+  bool pdl;             // programmatic dependent launch between consecutive kernels
 };
 
 namespace {
@@ -131,8 +133,19 @@ bool pointer_ok(const ar_comm_s* c, const void* p, size_t bytes) {
 
 bool aligned(const void* p, size_t a) { return addr(p) % a == 0; }
 
+// Which reduce kernel a call uses (see ar_comm_s::kernel_mode).  The
+// bulk-copy pipeline needs at least two shared-memory stages.
+bool choose_tma(const ar_comm_s* c, int P, bool sgd, size_t es) {
+  if (c->kernel_mode == 1) return false;
+  if (gar::tma_stages(P, sgd, int(es)) < 2) return false;
+  return c->kernel_mode == 2;
+}
+
 template <class Cap>
 void init_table(SegTable<Cap>& t, int np, int ndst, int stride, int dst_off, bool mean) {
+  t.stages = 0;
+  t.stage_bytes = 0;
+  t.status = nullptr;
   t.nseg = 0;
   t.ntiles = 0;
   t.np = np;
@@ -165,6 +178,14 @@ bool add_segment(SegTable<Cap>& t, void* const* ptrs, uint64_t numel, uint64_t t
   return true;
 }
 
+// Configures the table for the bulk-copy kernel (stages, stage size, status).
+template <class Cap>
+void set_tma(SegTable<Cap>& t, const ar_comm_s* c, bool sgd, size_t es) {
+  t.stages = gar::tma_stages(t.np, sgd, int(es));
+  t.stage_bytes = gar::tma_stage_bytes(t.np, sgd, 16 / int(es));
+  t.status = c->d_status;
+}
+
 uint32_t vec_flag(void* const* ptrs, int n, float* const* extra = nullptr, int nextra = 0) {
   for (int k = 0; k < n; ++k)
     if (!aligned(ptrs[k], 16)) return 0;
@@ -179,7 +200,7 @@ template <class Cap>
 ar_status_t run_reduce(const ar_comm_s* c, ar_dtype_t dt, bool sgd, const SegTable<Cap>& t,
                        cudaStream_t st) {
   if (t.ntiles == 0) return AR_OK;
-  const gar::LaunchCtx ctx{c->device, c->num_sms, st};
+  const gar::LaunchCtx ctx{c->device, c->num_sms, st, t.stages > 0, c->pdl};
   return from_cuda(dt == AR_F32 ? gar::launch_reduce_f32<Cap>(ctx, sgd, t)
                                 : gar::launch_reduce_bf16<Cap>(ctx, sgd, t));
 }
@@ -187,7 +208,7 @@ ar_status_t run_reduce(const ar_comm_s* c, ar_dtype_t dt, bool sgd, const SegTab
 template <class Cap>
 ar_status_t run_copy(const ar_comm_s* c, const SegTable<Cap>& t, cudaStream_t st) {
   if (t.ntiles == 0) return AR_OK;
-  const gar::LaunchCtx ctx{c->device, c->num_sms, st};
+  const gar::LaunchCtx ctx{c->device, c->num_sms, st, false, c->pdl};
   return from_cuda(gar::launch_copy<Cap>(ctx, t));
 }
 
@@ -241,6 +262,12 @@ ar_status_t ar_init(ar_comm_t* comm, int nranks, int cuda_device, ar_op_t defaul
   c->default_op = default_op;
   const char* env = std::getenv("GAR_POINTER_CHECKS");
   c->check_pointers = !(env != nullptr && std::strcmp(env, "0") == 0);
+  env = std::getenv("GAR_KERNEL");
+  c->kernel_mode = 0;
+  if (env != nullptr && std::strcmp(env, "ldg") == 0) c->kernel_mode = 1;
+  if (env != nullptr && std::strcmp(env, "tma") == 0) c->kernel_mode = 2;
+  env = std::getenv("GAR_PDL");
+  c->pdl = !(env != nullptr && std::strcmp(env, "0") == 0);
   if (cudaMalloc(&c->d_status, sizeof(uint32_t)) != cudaSuccess) {
     delete c;
     return AR_ERR_CUDA;
@@ -283,6 +310,15 @@ ar_status_t ar_get_async_error(ar_comm_t comm) {
   return cudaPeekAtLastError() == cudaSuccess ? AR_OK : AR_ERR_CUDA;
 }
 
+ar_status_t ar_selftest_wait_timeout(ar_comm_t comm, unsigned timeout_ms, ar_stream_t stream) {
+  if (!is_live(comm)) return AR_ERR_STATE;
+  if (timeout_ms < 1 || timeout_ms > 2000) return AR_ERR_INVALID_ARG;
+  DeviceGuard guard(comm->device);
+  if (!guard.ok()) return AR_ERR_CUDA;
+  return from_cuda(gar::launch_wait_selftest(static_cast<cudaStream_t>(stream), comm->d_status,
+                                             uint64_t(timeout_ms) * 1000000ull));
+}
+
 ar_status_t ar_all_reduce(ar_comm_t comm, const void* const* send, void* const* recv, size_t count,
                           ar_dtype_t dtype, ar_op_t op, ar_stream_t stream) {
   ar_status_t st = check_call(comm, dtype);
@@ -312,12 +348,14 @@ ar_status_t ar_all_reduce(ar_comm_t comm, const void* const* send, void* const* 
 
   SegTable<CapSmall> t;
   init_table(t, P, P, 2 * P, P, rop == AR_MEAN);
+  const bool tma = choose_tma(comm, P, false, es);
+  if (tma) set_tma(t, comm, false, es);
   void* ptrs[2 * AR_MAX_RANKS];
   for (int r = 0; r < P; ++r) {
     ptrs[r] = const_cast<void*>(send[r]);
     ptrs[P + r] = recv[r];
   }
-  if (!add_segment(t, ptrs, count, gar::reduce_tile(P, int(es)), vec_flag(ptrs, 2 * P)))
+  if (!add_segment(t, ptrs, count, gar::reduce_tile(P, int(es), tma), vec_flag(ptrs, 2 * P)))
     return AR_ERR_INVALID_ARG;
   return run_reduce(comm, dtype, false, t, static_cast<cudaStream_t>(stream));
 }
@@ -354,7 +392,9 @@ ar_status_t ar_reduce_scatter(ar_comm_t comm, const void* const* send, void* con
 
   SegTable<CapSmall> t;
   init_table(t, P, 1, P + 1, P, rop == AR_MEAN);
-  const uint64_t tile = gar::reduce_tile(P, int(es));
+  const bool tma = choose_tma(comm, P, false, es);
+  if (tma) set_tma(t, comm, false, es);
+  const uint64_t tile = gar::reduce_tile(P, int(es), tma);
   for (int r = 0; r < P; ++r) {
     void* ptrs[AR_MAX_RANKS + 1];
     for (int q = 0; q < P; ++q)
@@ -501,10 +541,12 @@ ar_status_t ar_bucket_all_reduce(ar_comm_t comm, const ar_bucket_t* bucket, ar_o
       return AR_ERR_INVALID_ARG;
   }
 
-  const uint64_t tile = gar::reduce_tile(P, int(es));
+  const bool tma = choose_tma(comm, P, sgd != nullptr, es);
+  const uint64_t tile = gar::reduce_tile(P, int(es), tma);
   const cudaStream_t strm = static_cast<cudaStream_t>(stream);
   auto fill = [&](auto& tab, int t0, int t1) -> ar_status_t {
     init_table(tab, P, P, P, 0, rop == AR_MEAN);
+    if (tma) set_tma(tab, comm, sgd != nullptr, es);
     if (sgd != nullptr) {
       tab.lr = sgd->lr;
       tab.mu = sgd->momentum;

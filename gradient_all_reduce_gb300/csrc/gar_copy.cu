@@ -6,25 +6,45 @@
 
 namespace gar {
 
-int resident_ctas(const void* func) {
+int resident_ctas(const void* func, int threads, size_t smem) {
   static std::mutex mu;
-  static std::unordered_map<const void*, int> cache;
+  static std::unordered_map<const void*, std::pair<size_t, int>> cache;
   std::lock_guard<std::mutex> lock(mu);
   auto it = cache.find(func);
-  if (it != cache.end()) return it->second;
+  if (it != cache.end() && it->second.first >= smem) return it->second.second;
+  if (smem > 0) cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, func, kThreads, 0) != cudaSuccess || n < 1)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, func, threads, smem) != cudaSuccess || n < 1) {
+    cudaGetLastError();
     n = 1;
-  cache.emplace(func, n);
+  }
+  cache[func] = {smem, n};
   return n;
 }
 
 template <class Cap>
 cudaError_t launch_copy(const LaunchCtx& ctx, const SegTable<Cap>& tab) {
-  const void* f = reinterpret_cast<const void*>(&k_copy<Cap>);
-  const unsigned grid = grid_for(tab.ntiles, resident_ctas(f) * ctx.num_sms);
+  auto* k = &k_copy<Cap>;
+  const unsigned grid = grid_for(tab.ntiles, resident_ctas(reinterpret_cast<const void*>(k)) * ctx.num_sms);
   if (grid == 0) return cudaSuccess;
-  k_copy<Cap><<<grid, kThreads, 0, ctx.stream>>>(tab);
+  return launch_ex(ctx, k, grid, kThreads, 0, tab);
+}
+
+__global__ void k_wait_selftest(uint32_t* status, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const bool ok = mbar_wait_bounded(smem_u32(&bar), 0, &abort_flag, limit_ns);
+  if (!__all_sync(0xFFFFFFFFu, ok) && threadIdx.x == 0) atomicExch(status, 1u);
+}
+
+cudaError_t launch_wait_selftest(cudaStream_t stream, uint32_t* status, uint64_t limit_ns) {
+  k_wait_selftest<<<1, 32, 0, stream>>>(status, limit_ns);
   return cudaGetLastError();
 }
 

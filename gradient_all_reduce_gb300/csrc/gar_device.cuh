@@ -48,6 +48,14 @@ __device__ __forceinline__ void st_f4(float* p, const float4& v) {
                : "memory");
 }
 
+// Programmatic dependent launch: let the next kernel of the stream start
+// its launch now, and wait until the previous kernel has finished and its
+// writes are visible (both are no-ops when the launch did not opt in).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------- dtypes
 // bf16 is the upper half of an fp32 bit pattern: widening is a shift.
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

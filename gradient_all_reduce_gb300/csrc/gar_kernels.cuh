@@ -48,6 +48,9 @@ struct SegTable {
   int mean;                   // divide by P
   int write_back;             // SGD: also store the reduced gradient
   float lr, mu;               // SGD hyper-parameters
+  int stages;                 // bulk-copy kernel: shared-memory stages
+  uint32_t stage_bytes;       // bulk-copy kernel: bytes per stage
+  uint32_t* status;           // the comm's device status word (bounded waits)
   uint32_t tile0[Cap::kSeg + 1];  // first tile of each segment; tile0[nseg] = ntiles
   uint64_t numel[Cap::kSeg];      // elements (k_reduce) or bytes (k_copy) per segment
   uint32_t flags[Cap::kSeg];
@@ -86,6 +89,8 @@ __global__ void __launch_bounds__(kThreads)
   constexpr uint64_t kTileVec = uint64_t(U) * kThreads;
   const int np = a.np;
   const bool mean = a.mean != 0;
+  griddep_launch_dependents();
+  griddep_wait();
   uint32_t s = 0;
   for (uint32_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
     while (tile >= a.tile0[s + 1]) ++s;  // tiles are visited in increasing order
@@ -156,6 +161,8 @@ __global__ void __launch_bounds__(kThreads)
 template <class Cap>
 __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTable<Cap> a) {
   constexpr uint64_t kTileVec = uint64_t(kCopyUnroll) * kThreads;
+  griddep_launch_dependents();
+  griddep_wait();
   uint32_t s = 0;
   for (uint32_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
     while (tile >= a.tile0[s + 1]) ++s;

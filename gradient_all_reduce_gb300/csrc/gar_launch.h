@@ -4,7 +4,7 @@
 
 #include <cuda_runtime.h>
 
-#include "gar_kernels.cuh"
+#include "gar_tma.cuh"
 
 namespace gar {
 
@@ -12,7 +12,38 @@ struct LaunchCtx {
   int device;
   int num_sms;
   cudaStream_t stream;
+  bool tma;  // k_reduce_tma (bulk-copy pipeline) instead of k_reduce
+  bool pdl;  // launch with programmatic stream serialization
 };
+
+// Launch `kernel<<<grid, block, smem, ctx.stream>>>(tab)`, opting in to
+// programmatic dependent launch when ctx.pdl is set.
+template <class Tab>
+cudaError_t launch_ex(const LaunchCtx& ctx, void (*kernel)(Tab), unsigned grid, unsigned block,
+                      size_t smem, const Tab& tab) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = ctx.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = ctx.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, tab);
+}
+
+// Shared-memory budget of the bulk-copy kernel's stages.
+constexpr uint32_t kTmaSmemBudget = 200 * 1024;
+
+// Stages of k_reduce_tma for P ranks (0 when fewer than two stages fit).
+inline int tma_stages(int P, bool sgd, int elem_bytes) {
+  const uint32_t sb = tma_stage_bytes(P, sgd, 16 / elem_bytes);
+  const uint32_t s = kTmaSmemBudget / sb;
+  if (s < 2) return 0;
+  return s > uint32_t(kTmaMaxStages) ? kTmaMaxStages : int(s);
+}
 
 // Launch k_reduce on the table for fp32 or bf16 replicas, choosing the
 // specialisation for P (2, 4, 8, else the generic runtime-P kernel).
@@ -24,8 +55,13 @@ cudaError_t launch_reduce_bf16(const LaunchCtx& ctx, bool sgd, const SegTable<Ca
 template <class Cap>
 cudaError_t launch_copy(const LaunchCtx& ctx, const SegTable<Cap>& tab);
 
-// Tile size in elements of k_reduce for P ranks and the given element size.
-inline uint64_t reduce_tile(int P, int elem_bytes) {
+// One warp runs the bounded mbarrier wait on a barrier nothing arrives at.
+cudaError_t launch_wait_selftest(cudaStream_t stream, uint32_t* status, uint64_t limit_ns);
+
+// Tile size in elements of k_reduce (or k_reduce_tma when tma is set) for
+// P ranks and the given element size.
+inline uint64_t reduce_tile(int P, int elem_bytes, bool tma = false) {
+  if (tma) return tma_tile_elems(16 / elem_bytes);
   const int PT = (P == 2 || P == 4 || P == 8) ? P : 0;
   return reduce_tile_elems(PT, 16 / elem_bytes);
 }
@@ -39,7 +75,8 @@ inline unsigned grid_for(uint32_t ntiles, int max_ctas) {
   return (ntiles + per_cta - 1) / per_cta;
 }
 
-// Resident CTAs per SM for a kernel (cached per function).
-int resident_ctas(const void* func);
+// Resident CTAs per SM for a kernel (cached per function); smem is the
+// dynamic shared memory per CTA, which is also raised to that size once.
+int resident_ctas(const void* func, int threads = kThreads, size_t smem = 0);
 
 }  // namespace gar

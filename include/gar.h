@@ -205,6 +205,19 @@ ar_status_t ar_bucket_plan(int ntensors, const size_t *nbytes, size_t cap_bytes,
  */
 ar_status_t ar_get_async_error(ar_comm_t comm);
 
+/*
+ * Failure-detection self-test.  Enqueues one warp that waits, with the
+ * bounded mbarrier wait of the bulk-copy pipeline, on a barrier that
+ * nothing ever arrives at; after timeout_ms (1..2000) the wait gives up and
+ * records the timeout in the comm's status word, exactly as a stalled
+ * pipeline stage would.  The GPU context stays usable; afterwards
+ * ar_get_async_error(comm) returns AR_ERR_TIMEOUT for this comm (the status
+ * is sticky: destroy the comm).  The pages have no counterpart: DDP's
+ * collectives simply block until every rank joins ("Distributed Training",
+ * "Data parallelism and all-reduce").
+ */
+ar_status_t ar_selftest_wait_timeout(ar_comm_t comm, unsigned timeout_ms, ar_stream_t stream);
+
 /* A static, human-readable name for a status code. */
 const char *ar_status_string(ar_status_t status);
 

@@ -3,6 +3,8 @@ seeded generator, the same inputs regenerated on the host for the oracle,
 and bitwise comparison."""
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import torch
 
@@ -15,6 +17,23 @@ DT = {"f32": gar.AR_F32, "bf16": gar.AR_BF16}
 OP = {"sum": gar.AR_SUM, "mean": gar.AR_MEAN}
 ORACLE_OP = {"sum": oracle.SUM, "mean": oracle.MEAN}
 TORCH_DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+PATHS = ("ldg", "tma")   # register-staged k_reduce, bulk-copy pipelined k_reduce_tma
+
+
+def init(P: int, op: int = gar.AR_MEAN, path: str | None = None) -> int:
+    """ar_init with the reduce kernel forced to ``path`` (read at init)."""
+    old = os.environ.get("GAR_KERNEL")
+    if path is not None:
+        os.environ["GAR_KERNEL"] = path
+    try:
+        return gar.ar_init(P, 0, op)
+    finally:
+        if old is None:
+            os.environ.pop("GAR_KERNEL", None)
+        else:
+            os.environ["GAR_KERNEL"] = old
 
 
 def dev():

@@ -7,7 +7,8 @@ import torch
 import gradient_all_reduce_gb300 as gar
 import oracle
 import workloads
-from gpucase import (DT, OP, ORACLE_OP, assert_bits_equal, dev, empty, replicas, to_np)
+from gpucase import (DT, OP, ORACLE_OP, PATHS, assert_bits_equal, dev, empty, init, replicas,
+                     to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -16,6 +17,11 @@ pytestmark = pytest.mark.gpu
 def cuda():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
+
+
+@pytest.fixture(params=PATHS)
+def path(request):
+    return request.param
 
 
 def _bucket(P, sizes, dt, seed0, offset=0):
@@ -35,9 +41,9 @@ SHAPES = [(1,), (7,), (768,), (1000,), (2304, 768), (3,), (65_536 + 13,)]
 @pytest.mark.parametrize("P", [2, 3, 4, 8])
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("op", ["sum", "mean"])
-def test_bucket_equals_oracle(cuda, P, dt, op):
+def test_bucket_equals_oracle(cuda, path, P, dt, op):
     sizes = [int(np.prod(s)) for s in SHAPES]
-    comm = gar.ar_init(P, 0, gar.AR_MEAN)
+    comm = init(P, gar.AR_MEAN, path)
     try:
         ts = _bucket(P, sizes, dt, 1)
         gar.ar_bucket_all_reduce(comm, ts, sizes, DT[dt], OP[op])
@@ -54,7 +60,7 @@ def test_bucket_equals_oracle(cuda, P, dt, op):
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("write_back", [0, 1])
 @pytest.mark.parametrize("aligned", [True, False])
-def test_bucket_sgd_equals_oracle(cuda, dt, write_back, aligned):
+def test_bucket_sgd_equals_oracle(cuda, path, dt, write_back, aligned):
     """Two steps of the fused Mean + SGD(momentum 0.9, lr 0.1) on fp32
     master weights ~N(0, 0.02) and zero momentum."""
     P = 8
@@ -71,7 +77,7 @@ def test_bucket_sgd_equals_oracle(cuda, dt, write_back, aligned):
         vs.append(torch.zeros(n + off, dtype=torch.float32, device=dev())[off:])
         hw.append(workloads.normal_f32(200 + t, n, std=0.02))
         hv.append(np.zeros(n, np.float32))
-    comm = gar.ar_init(P, 0, gar.AR_MEAN)
+    comm = init(P, gar.AR_MEAN, path)
     try:
         for step in range(2):
             gar.ar_bucket_all_reduce(comm, ts, sizes, DT[dt], gar.AR_MEAN,
@@ -88,7 +94,7 @@ def test_bucket_sgd_equals_oracle(cuda, dt, write_back, aligned):
         gar.ar_destroy(comm)
 
 
-def test_bucket_larger_than_one_parameter_block(cuda):
+def test_bucket_larger_than_one_parameter_block(cuda, path):
     """600 small tensors at P=4 (more than one launch's segment table):
     results equal the per-tensor oracle."""
     P = 4
@@ -100,7 +106,7 @@ def test_bucket_larger_than_one_parameter_block(cuda):
     for n in sizes:
         ts.append([b[off:off + n] for b in base])
         off += n
-    comm = gar.ar_init(P, 0, gar.AR_MEAN)
+    comm = init(P, gar.AR_MEAN, path)
     try:
         gar.ar_bucket_all_reduce(comm, ts, sizes, gar.AR_BF16)
         torch.cuda.synchronize()

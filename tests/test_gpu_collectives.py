@@ -9,23 +9,24 @@ import torch
 
 import gradient_all_reduce_gb300 as gar
 import oracle
-from gpucase import (DT, OP, ORACLE_OP, assert_bits_equal, bits_equal_device, dev, empty,
-                     host_replicas, replicas, to_np)
+from gpucase import (DT, OP, ORACLE_OP, PATHS, assert_bits_equal, bits_equal_device, dev, empty,
+                     host_replicas, init, replicas, to_np)
 
 pytestmark = pytest.mark.gpu
 
 SIZES = (0, 1, 3, 17, 4097, 200_003)
 
 
-@pytest.fixture(scope="module")
-def comms():
+@pytest.fixture(scope="module", params=PATHS)
+def comms(request):
+    """Comms per P, with the reduce kernel of this run's path."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     made = {}
 
     def get(P):
         if P not in made:
-            made[P] = gar.ar_init(P, 0, gar.AR_MEAN)
+            made[P] = init(P, gar.AR_MEAN, request.param)
         return made[P]
 
     yield get

@@ -16,13 +16,18 @@ import torch
 import gradient_all_reduce_gb300 as gar
 import oracle
 import workloads
-from gpucase import (DT, OP, ORACLE_OP, assert_bits_equal, bits_equal_device, dev, empty, gather,
-                     host_replicas, replicas, sample_indices, to_np)
+from gpucase import (DT, OP, ORACLE_OP, PATHS, assert_bits_equal, bits_equal_device, dev, empty,
+                     gather, host_replicas, init, replicas, sample_indices, to_np)
 from golden import table
 from oracle import mlp
 from workloads import gpu as wgpu
 
 pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(params=PATHS)
+def path(request):
+    return request.param
 
 
 @pytest.fixture(autouse=True)
@@ -34,7 +39,7 @@ def cuda():
     torch.cuda.empty_cache()
 
 
-def test_ddp_equivalence_mlp():
+def test_ddp_equivalence_mlp(path):
     """Per-shard gradients of the 4-layer 1024-wide MLP (8 shards of 128
     rows, computed in fp64 on the host and rounded to fp32) are the P=8
     replicas; the GPU Mean over one 16 MiB bucket equals the oracle's bits
@@ -49,7 +54,7 @@ def test_ddp_equivalence_mlp():
     plan = gar.ar_bucket_plan([4 * n for n in sizes], 25 << 20)
     assert plan == [0, 0, 0, 0]
     P = workloads.MLP_SHARDS
-    comm = gar.ar_init(P, 0, gar.AR_MEAN)
+    comm = init(P, gar.AR_MEAN, path)
     try:
         gar.ar_bucket_all_reduce(comm, dev_t, sizes, gar.AR_F32, gar.AR_MEAN)
         torch.cuda.synchronize()
@@ -82,7 +87,7 @@ def _vit_step(comm, grads, w, v, numels, offs, buckets):
                                       [v[offs[t]:offs[t + 1]] for t in b], 1))
 
 
-def test_vit_b16_bucketed_sgd_full_size_sampled():
+def test_vit_b16_bucketed_sgd_full_size_sampled(path):
     """ViT-B/16: 86,567,656 bf16 gradients per replica ~N(0, 1e-3) (replica
     r from seed 100 + r), P=8, 8 buckets of <= 25 MiB in reverse order,
     Mean fused with SGD (momentum 0.9, lr 0.1) on fp32 master weights
@@ -104,7 +109,7 @@ def test_vit_b16_bucketed_sgd_full_size_sampled():
                          std=workloads.VIT_GRAD_STD, idx=idx)
     hw = workloads.normal_f32(workloads.VIT_MASTER_SEED, 0, std=workloads.VIT_MASTER_STD, idx=idx)
     hv = np.zeros(idx.size, np.float32)
-    comm = gar.ar_init(P, 0, gar.AR_MEAN)
+    comm = init(P, gar.AR_MEAN, path)
     try:
         for step in range(2):
             _vit_step(comm, grads, w, v, numels, offs, buckets)
@@ -121,7 +126,7 @@ def test_vit_b16_bucketed_sgd_full_size_sampled():
         gar.ar_destroy(comm)
 
 
-def test_vit_small_cap_full_check():
+def test_vit_small_cap_full_check(path):
     """The same step with 4 MiB buckets (many more, smaller launches) on the
     first 12,000,000 ViT elements, checked against the oracle on every
     element."""
@@ -139,7 +144,7 @@ def test_vit_small_cap_full_check():
     w = empty(n, "f32")
     wgpu.fill(w, "normal", 200, std=0.02)
     v = torch.zeros(n, dtype=torch.float32, device=dev())
-    comm = gar.ar_init(P, 0, gar.AR_MEAN)
+    comm = init(P, gar.AR_MEAN, path)
     try:
         _vit_step(comm, grads, w, v, numels, offs, buckets)
         torch.cuda.synchronize()
@@ -155,14 +160,14 @@ def test_vit_small_cap_full_check():
         assert_bits_equal(to_np(grads[r]), host[r], f"grad {r}")
 
 
-def test_large_bucket_rs_ag_ar():
+def test_large_bucket_rs_ag_ar(path):
     """P=4 replicas of 2**30 fp32 ~N(0,1) (4 GiB each): reduce-scatter then
     all-gather equals the fused all-reduce (Sum) bit for bit on the device;
     sampled outputs equal the oracle's."""
     P, n = 4, 1 << 30
     shard = n // P
     xs = replicas(P, n, "f32", "normal", 0)
-    comm = gar.ar_init(P, 0, gar.AR_SUM)
+    comm = init(P, gar.AR_SUM, path)
     try:
         ar = [empty(n, "f32") for _ in range(P)]
         gar.ar_all_reduce(comm, xs, ar, n, gar.AR_F32, gar.AR_SUM)
@@ -191,11 +196,11 @@ SWEEP_BYTES = [4096 * 4 ** k for k in range(10)]   # 4 KiB .. 1 GiB per replica
 
 @pytest.mark.parametrize("P", [2, 4, 8])
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
-def test_sweep(P, dt):
+def test_sweep(path, P, dt):
     """Every size of the sweep, Sum and Mean, in place, plus a broadcast
     from rank 0: full oracle check up to 4 MiB per replica, sampled above."""
     s = 4 if dt == "f32" else 2
-    comm = gar.ar_init(P, 0, gar.AR_MEAN)
+    comm = init(P, gar.AR_MEAN, path)
     try:
         for nbytes in SWEEP_BYTES:
             n = nbytes // s
