@@ -67,6 +67,8 @@ def _load() -> ctypes.CDLL:
                            ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)],
         "ar_get_async_error": [P],
         "ar_selftest_wait_timeout": [P, ctypes.c_uint, P],
+        "ar_all_reduce_noalloc": [ctypes.c_int, PP, PP, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
+                                  P],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
@@ -139,6 +141,15 @@ def ar_all_reduce(comm: int, send: Sequence, recv: Sequence, count: int, dtype: 
                   op: int = AR_OP_DEFAULT, stream=None) -> None:
     _ok(load().ar_all_reduce(comm, _ptr_array(send), _ptr_array(recv), int(count), int(dtype),
                           int(op), _stream(stream)), "ar_all_reduce")
+
+
+def ar_all_reduce_noalloc(nranks: int, send: Sequence, recv: Sequence, count: int, dtype: int,
+                          op: int, stream=None) -> None:
+    """All-reduce on the current CUDA device without a comm and without any
+    allocation (see include/gar.h): for callers that may not allocate
+    device memory themselves."""
+    _ok(load().ar_all_reduce_noalloc(int(nranks), _ptr_array(send), _ptr_array(recv), int(count),
+                                     int(dtype), int(op), _stream(stream)), "ar_all_reduce_noalloc")
 
 
 def ar_reduce_scatter(comm: int, send: Sequence, recv: Sequence, count: int, dtype: int,

@@ -218,6 +218,41 @@ ar_status_t ar_get_async_error(ar_comm_t comm);
  */
 ar_status_t ar_selftest_wait_timeout(ar_comm_t comm, unsigned timeout_ms, ar_stream_t stream);
 
+/*
+ * All-reduce that allocates nothing -- for callers that may not allocate
+ * device memory themselves and so cannot call ar_init (it allocates the
+ * comm's status word): plugins whose host framework owns every device
+ * allocation through its own pool, services that reserve all memory at
+ * start-up and forbid allocations while serving (cudaMalloc can stall the
+ * device), code running under a hard memory cap.  The pages have no
+ * counterpart for this entry point.
+ *
+ * Same operation, arguments and checks as ar_all_reduce, for nranks
+ * participants on the CALLER'S CURRENT CUDA device, with op AR_SUM or
+ * AR_MEAN (no comm, so no default op); results are identical bit for bit.
+ * It always runs the bulk-copy pipelined kernel.  The caller passes inputs
+ * and outputs; the kernel's scratch -- one 4-byte status word set when a
+ * bounded wait gives up -- lives in a static 256-byte device array that
+ * every GPU loading the library holds until the process exits.  A call
+ * needing more scratch than that is refused with AR_ERR_INVALID_ARG.  The
+ * call allocates no memory: no cudaMalloc, cudaFree or allocating library
+ * routine.
+ *
+ * The first call on a device sets that device up (checks it is sm_103 and
+ * looks up the array's device address); make that first call before any
+ * stream capture.  Every call clears the status word on `stream` before its
+ * launch.  All calls on a device share the one array, so calls whose work
+ * overlaps on the GPU (different streams, no ordering between them) race on
+ * it; calls on one stream are ordered and do not.  The status word has no
+ * comm to be read through: a wait that gave up (after 2 s) leaves the
+ * outputs incomplete without an error code here; callers who need that
+ * report use ar_init and ar_get_async_error.
+ * Errors: AR_ERR_INVALID_ARG as for ar_all_reduce; AR_ERR_UNSUPPORTED when
+ * the current device is not sm_103 (or has index >= 64); AR_ERR_CUDA.
+ */
+ar_status_t ar_all_reduce_noalloc(int nranks, const void *const *send, void *const *recv,
+                                  size_t count, ar_dtype_t dtype, ar_op_t op, ar_stream_t stream);
+
 /* A static, human-readable name for a status code. */
 const char *ar_status_string(ar_status_t status);
 

@@ -83,3 +83,13 @@ def test_bucket_plan_matches_oracle(gar):
         assert gar.ar_bucket_plan(sizes, cap) == oracle.bucket_plan(sizes, cap)
     huge = [2 ** 62, 2 ** 62, 5]
     assert gar.ar_bucket_plan(huge, 2 ** 63) == oracle.bucket_plan(huge, 2 ** 63)
+
+
+def test_no_alloc_entry_point_source_allocates_nothing():
+    """The allocation-free all-reduce's section of the C ABI source calls
+    no allocating CUDA routine."""
+    src = (ROOT / "gradient_all_reduce_gb300" / "csrc" / "gar_api.cu").read_text()
+    section = src[src.index("// All-reduce without any allocation."):]
+    section = re.sub(r"//[^\n]*", "", section)   # the comments explain why; check the code
+    for word in ("cudaMalloc", "cudaFree", "cudaHostAlloc", "cudaMallocAsync", "new ", "malloc("):
+        assert word not in section, word
