@@ -67,6 +67,13 @@ def _load() -> ctypes.CDLL:
                            ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)],
         "ar_get_async_error": [P],
         "ar_selftest_wait_timeout": [P, ctypes.c_uint, P],
+        "ar_reducer_create": [ctypes.POINTER(P), P, ctypes.POINTER(ar_bucket_t), ctypes.c_size_t,
+                              ctypes.c_int, ctypes.POINTER(ar_sgd_t)],
+        "ar_reducer_mark_ready": [P, ctypes.c_int, P],
+        "ar_reducer_finalize": [P, P],
+        "ar_reducer_set_sgd": [P, ctypes.c_float, ctypes.c_float],
+        "ar_reducer_info": [P, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)],
+        "ar_reducer_destroy": [P],
         "ar_all_reduce_noalloc": [ctypes.c_int, PP, PP, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
                                   P],
     }
@@ -235,3 +242,51 @@ class PreparedBucket:
 
     def __call__(self, stream=None) -> None:
         _ok(self._fn(*self._args, _stream(stream)), "ar_bucket_all_reduce")
+
+
+class Reducer:
+    """A DDP gradient reducer (``ar_reducer_*``): ``grads[t][r]`` is rank
+    r's replica of tensor t, tensors in registration order.  The argument
+    structures stay alive with this object, as the C side keeps only
+    pointers validated at creation."""
+
+    def __init__(self, comm: int, grads: Sequence[Sequence], numel: Sequence[int], dtype: int,
+                 cap_bytes: int = 25 << 20, op: int = AR_OP_DEFAULT, sgd=None):
+        flat = [x for reps in grads for x in reps]
+        self._ptrs = _ptr_array(flat)
+        self._nel = (ctypes.c_size_t * max(len(numel), 1))(*[int(n) for n in numel])
+        self.ntensors = len(grads)
+        b = ar_bucket_t(len(grads), ctypes.cast(self._ptrs, ctypes.POINTER(ctypes.c_void_p)),
+                        ctypes.cast(self._nel, ctypes.POINTER(ctypes.c_size_t)), int(dtype))
+        s = None
+        if sgd is not None:
+            lr, mom, master, mbuf, wb = sgd
+            self._m, self._v = _ptr_array(master), _ptr_array(mbuf)
+            s = ar_sgd_t(float(lr), float(mom), ctypes.cast(self._m, ctypes.POINTER(ctypes.c_void_p)),
+                         ctypes.cast(self._v, ctypes.POINTER(ctypes.c_void_p)), int(bool(wb)))
+        h = ctypes.c_void_p()
+        L = load()
+        _ok(L.ar_reducer_create(ctypes.byref(h), comm, ctypes.byref(b), int(cap_bytes), int(op),
+                                ctypes.byref(s) if s is not None else None), "ar_reducer_create")
+        self.handle = int(h.value)
+        self._mark = L.ar_reducer_mark_ready
+
+    def mark_ready(self, tensor: int, stream=None) -> None:
+        _ok(self._mark(self.handle, int(tensor), _stream(stream)), "ar_reducer_mark_ready")
+
+    def finalize(self, stream=None) -> None:
+        _ok(load().ar_reducer_finalize(self.handle, _stream(stream)), "ar_reducer_finalize")
+
+    def set_sgd(self, lr: float, momentum: float) -> None:
+        _ok(load().ar_reducer_set_sgd(self.handle, float(lr), float(momentum)), "ar_reducer_set_sgd")
+
+    def bucket_of(self) -> list[int]:
+        k = ctypes.c_int()
+        out = (ctypes.c_int * max(self.ntensors, 1))()
+        _ok(load().ar_reducer_info(self.handle, ctypes.byref(k), out), "ar_reducer_info")
+        return list(out)[:self.ntensors]
+
+    def destroy(self) -> None:
+        if self.handle:
+            _ok(load().ar_reducer_destroy(self.handle), "ar_reducer_destroy")
+            self.handle = 0

@@ -21,7 +21,7 @@ CSRC = PKG / "csrc"
 INCLUDE = ROOT / "include"
 LIB = PKG / "libgar.so"
 
-UNITS = ["gar_api.cu", "gar_reduce_f32.cu", "gar_reduce_bf16.cu", "gar_copy.cu"]
+UNITS = ["gar_api.cu", "gar_reducer.cu", "gar_reduce_f32.cu", "gar_reduce_bf16.cu", "gar_copy.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-O2", f"-I{INCLUDE}", f"-I{CSRC}"]

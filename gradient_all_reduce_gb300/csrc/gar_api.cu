@@ -13,24 +13,10 @@
 #include <cuda_runtime.h>
 
 #include "gar.h"
+#include "gar_host.h"
 #include "gar_launch.h"
 
-struct ar_comm_s {
-  int nranks;
-  int device;
-  int num_sms;
-  ar_op_t default_op;
-  uint32_t* d_status;   // sticky device-side status word (0 = ok)
-  bool check_pointers;  // validate every pointer against its allocation
-  int kernel_mode;      // 0 = default (k_reduce), 1 = k_reduce, 2 = bulk-copy k_reduce_tma
-  bool pdl;             // programmatic dependent launch between consecutive kernels
-};
-
-namespace {
-
-using gar::CapLarge;
-using gar::CapSmall;
-using gar::SegTable;
+namespace gar_host {
 
 std::mutex g_live_mu;
 std::unordered_set<const ar_comm_s*> g_live;
@@ -40,188 +26,61 @@ bool is_live(const ar_comm_s* c) {
   return c != nullptr && g_live.count(c) != 0;
 }
 
-// Makes the comm's device current for the duration of a call and restores
-// the caller's device afterwards.
-class DeviceGuard {
- public:
-  explicit DeviceGuard(int dev) {
-    if (cudaGetDevice(&prev_) != cudaSuccess) prev_ = -1;
-    ok_ = prev_ == dev || cudaSetDevice(dev) == cudaSuccess;
-  }
-  ~DeviceGuard() {
-    int cur = -1;
-    if (prev_ >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev_) cudaSetDevice(prev_);
-  }
-  bool ok() const { return ok_; }
-
- private:
-  int prev_ = -1;
-  bool ok_ = false;
-};
-
-size_t elem_bytes(ar_dtype_t dt) { return dt == AR_BF16 ? 2 : 4; }
-bool valid_dtype(ar_dtype_t dt) { return dt == AR_F32 || dt == AR_BF16; }
-
-bool resolve_op(const ar_comm_s* c, ar_op_t op, ar_op_t* out) {
-  if (op == AR_OP_DEFAULT) op = c->default_op;
-  if (op != AR_SUM && op != AR_MEAN) return false;
-  *out = op;
-  return true;
-}
-
-uintptr_t addr(const void* p) { return reinterpret_cast<uintptr_t>(p); }
-
-bool overlap(const void* a, size_t na, const void* b, size_t nb) {
-  if (na == 0 || nb == 0) return false;
-  return addr(a) < addr(b) + nb && addr(b) < addr(a) + na;
-}
-
-bool mul_ok(size_t a, size_t b, size_t* out) {
-  if (a != 0 && b > SIZE_MAX / a) return false;
-  *out = a * b;
-  return true;
-}
-
-// The driver's cuMemGetAddressRange, fetched through the runtime so the
-// library needs no link-time dependency on libcuda.
-using MemGetAddressRangeFn = CUresult (*)(CUdeviceptr*, size_t*, CUdeviceptr);
-
-MemGetAddressRangeFn address_range_fn() {
-  static MemGetAddressRangeFn fn = [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      p = nullptr;
-    return reinterpret_cast<MemGetAddressRangeFn>(p);
-  }();
-  return fn;
-}
-
-// A buffer the comm's device may read and write: device memory of this
-// device (the whole range inside one allocation), managed memory, or
-// registered host memory mapped at the same address.  Pageable host memory
-// is refused.
-bool pointer_ok(const ar_comm_s* c, const void* p, size_t bytes) {
-  if (p == nullptr) return false;
-  if (!c->check_pointers || bytes == 0) return true;
-  cudaPointerAttributes at;
-  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
-    cudaGetLastError();
-    return false;
-  }
-  switch (at.type) {
-    case cudaMemoryTypeDevice: {
-      if (at.device != c->device) return false;
-      MemGetAddressRangeFn range = address_range_fn();
-      if (range != nullptr) {
-        CUdeviceptr base = 0;
-        size_t size = 0;
-        if (range(&base, &size, static_cast<CUdeviceptr>(addr(p))) != CUDA_SUCCESS) return false;
-        if (addr(p) + bytes > static_cast<uintptr_t>(base) + size) return false;
-      }
-      return true;
+// The buffer rules of a bucket: every replica (and, with SGD, every fp32
+// master and momentum array) element-aligned, pairwise disjoint, and inside
+// memory the comm's device may use.  Empty tensors are not inspected.
+ar_status_t check_bucket_buffers(const ar_comm_s* comm, const ar_bucket_t* bucket,
+                                 const ar_sgd_t* sgd) {
+  const int T = bucket->ntensors, P = comm->nranks;
+  const size_t es = elem_bytes(bucket->dtype);
+  // Sort the ranges and compare neighbours.
+  struct Range { uintptr_t lo, hi; };
+  std::vector<Range> ranges;
+  ranges.reserve(size_t(T) * (P + 2));
+  for (int t = 0; t < T; ++t) {
+    size_t bytes, fbytes;
+    if (!mul_ok(bucket->numel[t], es, &bytes) || !mul_ok(bucket->numel[t], 4, &fbytes))
+      return AR_ERR_INVALID_ARG;
+    if (bytes == 0) continue;  // an empty tensor's pointers are not inspected
+    for (int r = 0; r < P; ++r) {
+      const void* p = bucket->dev_ptrs[size_t(t) * P + r];
+      if (p == nullptr || !aligned(p, es)) return AR_ERR_INVALID_ARG;
+      ranges.push_back({addr(p), addr(p) + bytes});
     }
-    case cudaMemoryTypeManaged:
-      return true;
-    case cudaMemoryTypeHost:
-      return at.devicePointer == p;
-    default:
-      return false;
+    if (sgd != nullptr) {
+      const float* w = sgd->master[t];
+      const float* v = sgd->momentum_buf[t];
+      if (w == nullptr || v == nullptr || !aligned(w, 4) || !aligned(v, 4))
+        return AR_ERR_INVALID_ARG;
+      if (fbytes) {
+        ranges.push_back({addr(w), addr(w) + fbytes});
+        ranges.push_back({addr(v), addr(v) + fbytes});
+      }
+    }
   }
-}
+  std::sort(ranges.begin(), ranges.end(),
+            [](const Range& a, const Range& b) { return a.lo < b.lo; });
+  for (size_t k = 1; k < ranges.size(); ++k)
+    if (ranges[k].lo < ranges[k - 1].hi) return AR_ERR_INVALID_ARG;
+  for (int t = 0; t < T; ++t) {
+    const size_t n = bucket->numel[t];
+    if (n == 0) continue;
+    for (int r = 0; r < P; ++r)
+      if (!pointer_ok(comm, bucket->dev_ptrs[size_t(t) * P + r], n * es)) return AR_ERR_INVALID_ARG;
+    if (sgd != nullptr &&
+        (!pointer_ok(comm, sgd->master[t], n * 4) || !pointer_ok(comm, sgd->momentum_buf[t], n * 4)))
+      return AR_ERR_INVALID_ARG;
+  }
 
-bool aligned(const void* p, size_t a) { return addr(p) % a == 0; }
-
-// Which reduce kernel a call uses (see ar_comm_s::kernel_mode).  By default
-// the register-staged k_reduce: on GB300 it measured as fast as the
-// bulk-copy pipeline in isolation and faster back to back.  The bulk-copy
-// pipeline needs at least two shared-memory stages.
-bool choose_tma(const ar_comm_s* c, int P, bool sgd, size_t es) {
-  if (c->kernel_mode == 1) return false;
-  if (gar::tma_stages(P, sgd, int(es)) < 2) return false;
-  return c->kernel_mode == 2;
-}
-
-template <class Cap>
-void init_table(SegTable<Cap>& t, int np, int ndst, int stride, int dst_off, bool mean) {
-  t.stages = 0;
-  t.stage_bytes = 0;
-  t.status = nullptr;
-  t.nseg = 0;
-  t.ntiles = 0;
-  t.np = np;
-  t.ndst = ndst;
-  t.stride = stride;
-  t.dst_off = dst_off;
-  t.mean = mean ? 1 : 0;
-  t.write_back = 1;
-  t.lr = 0.f;
-  t.mu = 0.f;
-  t.tile0[0] = 0;
-}
-
-// Appends one segment; ptrs holds `stride` pointers.  Returns false when a
-// 32-bit tile count would overflow.
-template <class Cap>
-bool add_segment(SegTable<Cap>& t, void* const* ptrs, uint64_t numel, uint64_t tile,
-                 uint32_t flags, float* master = nullptr, float* mom = nullptr) {
-  const uint32_t s = t.nseg;
-  const uint64_t tiles = (numel + tile - 1) / tile;
-  if (uint64_t(t.ntiles) + tiles > 0xFFFFFFF0ull) return false;
-  for (int k = 0; k < t.stride; ++k) t.ptr[s * t.stride + k] = ptrs[k];
-  t.numel[s] = numel;
-  t.flags[s] = flags;
-  t.master[s] = master;
-  t.mom[s] = mom;
-  t.ntiles += static_cast<uint32_t>(tiles);
-  t.tile0[s + 1] = t.ntiles;
-  t.nseg = s + 1;
-  return true;
-}
-
-// Configures the table for the bulk-copy kernel (stages, stage size, status).
-template <class Cap>
-void set_tma(SegTable<Cap>& t, const ar_comm_s* c, bool sgd, size_t es) {
-  t.stages = gar::tma_stages(t.np, sgd, int(es));
-  t.stage_bytes = gar::tma_stage_bytes(t.np, sgd, 16 / int(es));
-  t.status = c->d_status;
-}
-
-uint32_t vec_flag(void* const* ptrs, int n, float* const* extra = nullptr, int nextra = 0) {
-  for (int k = 0; k < n; ++k)
-    if (!aligned(ptrs[k], 16)) return 0;
-  for (int k = 0; k < nextra; ++k)
-    if (!aligned(extra[k], 16)) return 0;
-  return gar::kSegVec;
-}
-
-ar_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? AR_OK : AR_ERR_CUDA; }
-
-template <class Cap>
-ar_status_t run_reduce(const ar_comm_s* c, ar_dtype_t dt, bool sgd, const SegTable<Cap>& t,
-                       cudaStream_t st) {
-  if (t.ntiles == 0) return AR_OK;
-  const gar::LaunchCtx ctx{c->device, c->num_sms, st, t.stages > 0, c->pdl};
-  return from_cuda(dt == AR_F32 ? gar::launch_reduce_f32<Cap>(ctx, sgd, t)
-                                : gar::launch_reduce_bf16<Cap>(ctx, sgd, t));
-}
-
-template <class Cap>
-ar_status_t run_copy(const ar_comm_s* c, const SegTable<Cap>& t, cudaStream_t st) {
-  if (t.ntiles == 0) return AR_OK;
-  const gar::LaunchCtx ctx{c->device, c->num_sms, st, false, c->pdl};
-  return from_cuda(gar::launch_copy<Cap>(ctx, t));
-}
-
-// Common checks of a collective call: live comm, dtype, pointer arrays.
-ar_status_t check_call(const ar_comm_s* c, ar_dtype_t dt) {
-  if (!is_live(c)) return AR_ERR_STATE;
-  if (!valid_dtype(dt)) return AR_ERR_INVALID_ARG;
   return AR_OK;
 }
 
-}  // namespace
+}  // namespace gar_host
+
+using namespace gar_host;
+using gar::CapLarge;
+using gar::CapSmall;
+using gar::SegTable;
 
 extern "C" {
 
@@ -502,46 +361,8 @@ ar_status_t ar_bucket_all_reduce(ar_comm_t comm, const ar_bucket_t* bucket, ar_o
   DeviceGuard guard(comm->device);
   if (!guard.ok()) return AR_ERR_CUDA;
 
-  // Every buffer of the bucket (replicas, and the fp32 master and momentum
-  // arrays) must be pairwise disjoint: sort the ranges and compare
-  // neighbours.
-  struct Range { uintptr_t lo, hi; };
-  std::vector<Range> ranges;
-  ranges.reserve(size_t(T) * (P + 2));
-  for (int t = 0; t < T; ++t) {
-    size_t bytes, fbytes;
-    if (!mul_ok(bucket->numel[t], es, &bytes) || !mul_ok(bucket->numel[t], 4, &fbytes))
-      return AR_ERR_INVALID_ARG;
-    if (bytes == 0) continue;  // an empty tensor's pointers are not inspected
-    for (int r = 0; r < P; ++r) {
-      const void* p = bucket->dev_ptrs[size_t(t) * P + r];
-      if (p == nullptr || !aligned(p, es)) return AR_ERR_INVALID_ARG;
-      ranges.push_back({addr(p), addr(p) + bytes});
-    }
-    if (sgd != nullptr) {
-      const float* w = sgd->master[t];
-      const float* v = sgd->momentum_buf[t];
-      if (w == nullptr || v == nullptr || !aligned(w, 4) || !aligned(v, 4))
-        return AR_ERR_INVALID_ARG;
-      if (fbytes) {
-        ranges.push_back({addr(w), addr(w) + fbytes});
-        ranges.push_back({addr(v), addr(v) + fbytes});
-      }
-    }
-  }
-  std::sort(ranges.begin(), ranges.end(),
-            [](const Range& a, const Range& b) { return a.lo < b.lo; });
-  for (size_t k = 1; k < ranges.size(); ++k)
-    if (ranges[k].lo < ranges[k - 1].hi) return AR_ERR_INVALID_ARG;
-  for (int t = 0; t < T; ++t) {
-    const size_t n = bucket->numel[t];
-    if (n == 0) continue;
-    for (int r = 0; r < P; ++r)
-      if (!pointer_ok(comm, bucket->dev_ptrs[size_t(t) * P + r], n * es)) return AR_ERR_INVALID_ARG;
-    if (sgd != nullptr &&
-        (!pointer_ok(comm, sgd->master[t], n * 4) || !pointer_ok(comm, sgd->momentum_buf[t], n * 4)))
-      return AR_ERR_INVALID_ARG;
-  }
+  ar_status_t chk = check_bucket_buffers(comm, bucket, sgd);
+  if (chk != AR_OK) return chk;
 
   const bool tma = choose_tma(comm, P, sgd != nullptr, es);
   const uint64_t tile = gar::reduce_tile(P, int(es), tma);

@@ -1,0 +1,289 @@
+// gar_reducer.cu -- the DDP gradient reducer: bucketing engine of the C ABI.
+//
+// DDP packs gradients into ~25 MB buckets in reverse parameter order and
+// launches an asynchronous all-reduce on each bucket as soon as all of its
+// gradients are ready, while the backward pass goes on producing the next
+// ones; every rank reduces the buckets in the same order ("Distributed
+// Training", computervisiononline.com, "Data parallelism and all-reduce").
+// Here the P ranks are P replica buffers on one GPU, so a reducer holds the
+// whole group's gradient set:
+//   create:      plan the buckets, validate every buffer once, and build
+//                each bucket's launch table(s) ahead of time;
+//   mark_ready:  a tensor's gradient is final on the caller's stream; when
+//                a bucket's last tensor is marked, the bucket's kernel is
+//                launched on one of two high-priority communication
+//                streams (alternating, so consecutive buckets overlap),
+//                ordered after the marking streams' work by events;
+//   finalize:    launch any bucket still waiting (its unmarked tensors are
+//                taken as ready on the caller's stream), then make the
+//                caller's stream wait for every launched bucket; the marks
+//                reset for the next step.
+#include <mutex>
+#include <new>
+#include <unordered_set>
+#include <vector>
+
+#include "gar_host.h"
+
+using namespace gar_host;
+
+struct ar_reducer_s {
+  struct Bucket {
+    std::vector<int> tensors;                  // in launch-table order
+    std::vector<SegTable<CapSmall>> small;     // launch tables (one of the two lists is used)
+    std::vector<SegTable<CapLarge>> large;
+    int pending = 0;                           // tensors not yet marked this step
+    bool launched = false;
+    std::vector<cudaStream_t> mark_streams;    // distinct streams that marked its tensors
+  };
+
+  ar_comm_s* comm = nullptr;
+  int P = 0;
+  int ntensors = 0;
+  ar_dtype_t dtype = AR_F32;
+  bool sgd = false;
+  std::vector<int> bucket_of;
+  std::vector<char> marked;
+  std::vector<Bucket> buckets;
+  cudaStream_t streams[2] = {nullptr, nullptr};
+  cudaEvent_t done[2] = {nullptr, nullptr};
+  bool used[2] = {false, false};
+  int next = 0;
+  cudaEvent_t join = nullptr;
+};
+
+namespace {
+
+std::mutex g_red_mu;
+std::unordered_set<const ar_reducer_s*> g_reducers;
+
+bool reducer_live(const ar_reducer_s* r) {
+  std::lock_guard<std::mutex> lock(g_red_mu);
+  return r != nullptr && g_reducers.count(r) != 0;
+}
+
+void release(ar_reducer_s* r) {
+  for (int k = 0; k < 2; ++k) {
+    if (r->done[k]) cudaEventDestroy(r->done[k]);
+    if (r->streams[k]) cudaStreamDestroy(r->streams[k]);
+  }
+  if (r->join) cudaEventDestroy(r->join);
+  delete r;
+}
+
+// Launch bucket b on the next communication stream, after the work of
+// every stream that marked one of its tensors.
+ar_status_t launch_bucket(ar_reducer_s* r, int b) {
+  ar_reducer_s::Bucket& bk = r->buckets[b];
+  const int k = r->next;
+  r->next ^= 1;
+  cudaStream_t s = r->streams[k];
+  for (cudaStream_t ms : bk.mark_streams) {
+    if (cudaEventRecord(r->join, ms) != cudaSuccess) return AR_ERR_CUDA;
+    if (cudaStreamWaitEvent(s, r->join, 0) != cudaSuccess) return AR_ERR_CUDA;
+  }
+  for (const auto& t : bk.small) {
+    ar_status_t st = run_reduce(r->comm, r->dtype, r->sgd, t, s);
+    if (st != AR_OK) return st;
+  }
+  for (const auto& t : bk.large) {
+    ar_status_t st = run_reduce(r->comm, r->dtype, r->sgd, t, s);
+    if (st != AR_OK) return st;
+  }
+  if (cudaEventRecord(r->done[k], s) != cudaSuccess) return AR_ERR_CUDA;
+  r->used[k] = true;
+  bk.launched = true;
+  return AR_OK;
+}
+
+void note_stream(ar_reducer_s::Bucket& bk, cudaStream_t s) {
+  for (cudaStream_t x : bk.mark_streams)
+    if (x == s) return;
+  bk.mark_streams.push_back(s);
+}
+
+}  // namespace
+
+extern "C" {
+
+ar_status_t ar_reducer_create(ar_reducer_t* out, ar_comm_t comm, const ar_bucket_t* grads,
+                              size_t cap_bytes, ar_op_t op, const ar_sgd_t* sgd) {
+  if (out == nullptr) return AR_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!is_live(comm)) return AR_ERR_STATE;
+  ar_op_t rop;
+  if (grads == nullptr || cap_bytes == 0 || !resolve_op(comm, op, &rop) ||
+      !valid_dtype(grads->dtype) || grads->ntensors < 0)
+    return AR_ERR_INVALID_ARG;
+  const int T = grads->ntensors, P = comm->nranks;
+  if (T > 0 && (grads->dev_ptrs == nullptr || grads->numel == nullptr)) return AR_ERR_INVALID_ARG;
+  if (sgd != nullptr && T > 0 && (sgd->master == nullptr || sgd->momentum_buf == nullptr))
+    return AR_ERR_INVALID_ARG;
+  const size_t es = elem_bytes(grads->dtype);
+  DeviceGuard guard(comm->device);
+  if (!guard.ok()) return AR_ERR_CUDA;
+
+  // Validate the whole gradient set once (the rules of ar_bucket_all_reduce).
+  ar_status_t st = check_bucket_buffers(comm, grads, sgd);
+  if (st != AR_OK) return st;
+
+  ar_reducer_s* r = new (std::nothrow) ar_reducer_s();
+  if (r == nullptr) return AR_ERR_CUDA;
+  r->comm = comm;
+  r->P = P;
+  r->ntensors = T;
+  r->dtype = grads->dtype;
+  r->sgd = sgd != nullptr;
+  r->bucket_of.assign(size_t(T), 0);
+  r->marked.assign(size_t(T), 0);
+  std::vector<size_t> nbytes(static_cast<size_t>(T));
+  for (int t = 0; t < T; ++t) nbytes[t] = grads->numel[t] * es;
+  int nb = 0;
+  if (ar_bucket_plan(T, nbytes.data(), cap_bytes, r->bucket_of.data(), &nb) != AR_OK) {
+    delete r;
+    return AR_ERR_INVALID_ARG;
+  }
+  r->buckets.resize(size_t(nb));
+  for (int t = T - 1; t >= 0; --t) r->buckets[r->bucket_of[t]].tensors.push_back(t);
+
+  const bool tma = choose_tma(comm, P, r->sgd, es);
+  const uint64_t tile = gar::reduce_tile(P, int(es), tma);
+  auto fill = [&](auto& tab, const std::vector<int>& ts, size_t t0, size_t t1) -> bool {
+    init_table(tab, P, P, P, 0, rop == AR_MEAN);
+    if (tma) set_tma(tab, comm, r->sgd, es);
+    if (sgd != nullptr) {
+      tab.lr = sgd->lr;
+      tab.mu = sgd->momentum;
+      tab.write_back = sgd->write_back_grads ? 1 : 0;
+    }
+    for (size_t i = t0; i < t1; ++i) {
+      const int t = ts[i];
+      void* const* ptrs = grads->dev_ptrs + size_t(t) * P;
+      float* w = sgd ? sgd->master[t] : nullptr;
+      float* v = sgd ? sgd->momentum_buf[t] : nullptr;
+      float* extra[2] = {w, v};
+      if (!add_segment(tab, ptrs, grads->numel[t], tile, vec_flag(ptrs, P, extra, sgd ? 2 : 0), w, v))
+        return false;
+    }
+    return true;
+  };
+  for (auto& bk : r->buckets) {
+    const size_t n = bk.tensors.size();
+    bool ok = true;
+    if (n <= size_t(CapSmall::kSeg) && n * P <= size_t(CapSmall::kPtr)) {
+      bk.small.emplace_back();
+      ok = fill(bk.small.back(), bk.tensors, 0, n);
+    } else {
+      const size_t per = size_t(std::min(CapLarge::kSeg, CapLarge::kPtr / P));
+      for (size_t t0 = 0; t0 < n && ok; t0 += per) {
+        bk.large.emplace_back();
+        ok = fill(bk.large.back(), bk.tensors, t0, std::min(n, t0 + per));
+      }
+    }
+    if (!ok) {
+      delete r;
+      return AR_ERR_INVALID_ARG;
+    }
+    bk.pending = int(n);
+  }
+
+  int lo = 0, hi = 0;
+  if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) hi = 0;
+  for (int k = 0; k < 2; ++k) {
+    if (cudaStreamCreateWithPriority(&r->streams[k], cudaStreamNonBlocking, hi) != cudaSuccess ||
+        cudaEventCreateWithFlags(&r->done[k], cudaEventDisableTiming) != cudaSuccess) {
+      release(r);
+      return AR_ERR_CUDA;
+    }
+  }
+  if (cudaEventCreateWithFlags(&r->join, cudaEventDisableTiming) != cudaSuccess) {
+    release(r);
+    return AR_ERR_CUDA;
+  }
+  {
+    std::lock_guard<std::mutex> lock(g_red_mu);
+    g_reducers.insert(r);
+  }
+  *out = r;
+  return AR_OK;
+}
+
+ar_status_t ar_reducer_mark_ready(ar_reducer_t r, int tensor, ar_stream_t stream) {
+  if (!reducer_live(r) || !is_live(r->comm)) return AR_ERR_STATE;
+  if (tensor < 0 || tensor >= r->ntensors) return AR_ERR_INVALID_ARG;
+  if (r->marked[tensor]) return AR_ERR_STATE;  // a gradient is marked once per step
+  DeviceGuard guard(r->comm->device);
+  if (!guard.ok()) return AR_ERR_CUDA;
+  r->marked[tensor] = 1;
+  ar_reducer_s::Bucket& bk = r->buckets[r->bucket_of[tensor]];
+  note_stream(bk, static_cast<cudaStream_t>(stream));
+  if (--bk.pending == 0) return launch_bucket(r, r->bucket_of[tensor]);
+  return AR_OK;
+}
+
+ar_status_t ar_reducer_finalize(ar_reducer_t r, ar_stream_t stream) {
+  if (!reducer_live(r) || !is_live(r->comm)) return AR_ERR_STATE;
+  DeviceGuard guard(r->comm->device);
+  if (!guard.ok()) return AR_ERR_CUDA;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ar_status_t st = AR_OK;
+  for (size_t b = 0; b < r->buckets.size() && st == AR_OK; ++b) {
+    auto& bk = r->buckets[b];
+    if (!bk.launched && !bk.tensors.empty()) {
+      note_stream(bk, s);
+      st = launch_bucket(r, int(b));
+    }
+  }
+  for (int k = 0; k < 2 && st == AR_OK; ++k)
+    if (r->used[k] && cudaStreamWaitEvent(s, r->done[k], 0) != cudaSuccess) st = AR_ERR_CUDA;
+  for (auto& bk : r->buckets) {
+    bk.pending = int(bk.tensors.size());
+    bk.launched = false;
+    bk.mark_streams.clear();
+  }
+  std::fill(r->marked.begin(), r->marked.end(), 0);
+  r->used[0] = r->used[1] = false;
+  return st;
+}
+
+ar_status_t ar_reducer_set_sgd(ar_reducer_t r, float lr, float momentum) {
+  if (!reducer_live(r)) return AR_ERR_STATE;
+  if (!r->sgd) return AR_ERR_INVALID_ARG;
+  for (auto& bk : r->buckets) {
+    for (auto& t : bk.small) {
+      t.lr = lr;
+      t.mu = momentum;
+    }
+    for (auto& t : bk.large) {
+      t.lr = lr;
+      t.mu = momentum;
+    }
+  }
+  return AR_OK;
+}
+
+ar_status_t ar_reducer_info(ar_reducer_t r, int* nbuckets, int* bucket_of) {
+  if (!reducer_live(r)) return AR_ERR_STATE;
+  if (nbuckets == nullptr) return AR_ERR_INVALID_ARG;
+  *nbuckets = int(r->buckets.size());
+  if (bucket_of != nullptr)
+    for (int t = 0; t < r->ntensors; ++t) bucket_of[t] = r->bucket_of[t];
+  return AR_OK;
+}
+
+ar_status_t ar_reducer_destroy(ar_reducer_t r) {
+  {
+    std::lock_guard<std::mutex> lock(g_red_mu);
+    if (r == nullptr || g_reducers.erase(r) == 0) return AR_ERR_STATE;
+  }
+  ar_status_t st = AR_OK;
+  {
+    DeviceGuard guard(r->comm->device);
+    for (int k = 0; k < 2; ++k)
+      if (r->streams[k] && cudaStreamSynchronize(r->streams[k]) != cudaSuccess) st = AR_ERR_CUDA;
+    release(r);
+  }
+  return st;
+}
+
+}  // extern "C"

@@ -199,6 +199,58 @@ ar_status_t ar_bucket_plan(int ntensors, const size_t *nbytes, size_t cap_bytes,
                            int *bucket_of, int *nbuckets);
 
 /*
+ * DDP gradient reducer: the bucketing engine of DDP.  Gradients are packed
+ * into buckets of about 25 MB in reverse parameter order and an
+ * asynchronous all-reduce is launched on each bucket as soon as all of its
+ * gradients are ready, while the backward pass goes on; every rank reduces
+ * the buckets in the same order ("Distributed Training", "Data parallelism
+ * and all-reduce").  A reducer holds the whole group's gradient set and
+ * does per step what ar_bucket_all_reduce does per bucket, with identical
+ * results, but validates and plans only once.
+ *
+ * ar_reducer_create: grads lists EVERY gradient tensor in registration
+ * order (the layout of ar_bucket_t); buckets are planned with
+ * ar_bucket_plan(cap_bytes); op as for the collectives; sgd NULL, or the
+ * fused SGD-momentum step of ar_sgd_t (per-tensor master / momentum).  All
+ * buffers are validated here with the rules of ar_bucket_all_reduce and
+ * must stay allocated, at the same addresses, while the reducer lives.
+ * Creates two communication streams (the device's highest priority) and
+ * three events on the comm's device; destroy the reducer before its comm.
+ * Not thread-safe.
+ */
+typedef struct ar_reducer_s *ar_reducer_t;
+ar_status_t ar_reducer_create(ar_reducer_t *reducer, ar_comm_t comm, const ar_bucket_t *grads,
+                              size_t cap_bytes, ar_op_t op, const ar_sgd_t *sgd);
+
+/*
+ * Tensor `tensor` (its P replicas) holds its final gradient of this step
+ * once `stream` reaches the call.  When the last tensor of a bucket is
+ * marked, that bucket's kernel is launched on a communication stream,
+ * ordered after every stream that marked one of its tensors (consecutive
+ * buckets alternate between the two streams and may overlap on the GPU).
+ * AR_ERR_INVALID_ARG for an index out of range; AR_ERR_STATE for a tensor
+ * already marked in this step.
+ */
+ar_status_t ar_reducer_mark_ready(ar_reducer_t reducer, int tensor, ar_stream_t stream);
+
+/*
+ * End of the step: launches every bucket not launched yet (its unmarked
+ * tensors are taken as ready on `stream`), makes `stream` wait for all the
+ * step's buckets (no host blocking), and clears the marks for the next step.
+ */
+ar_status_t ar_reducer_finalize(ar_reducer_t reducer, ar_stream_t stream);
+
+/* New SGD learning rate and momentum for the following launches (a
+ * learning-rate schedule); AR_ERR_INVALID_ARG if the reducer has no SGD. */
+ar_status_t ar_reducer_set_sgd(ar_reducer_t reducer, float lr, float momentum);
+
+/* Number of buckets and, if bucket_of is not NULL, each tensor's bucket. */
+ar_status_t ar_reducer_info(ar_reducer_t reducer, int *nbuckets, int *bucket_of);
+
+/* Waits for the reducer's streams, then frees it.  AR_ERR_STATE if not live. */
+ar_status_t ar_reducer_destroy(ar_reducer_t reducer);
+
+/*
  * Sticky device-side status of a comm: AR_ERR_TIMEOUT once a kernel's
  * bounded wait has given up, AR_ERR_CUDA for a sticky CUDA error on the
  * device, else AR_OK.  Synchronises the device (it reads the status word).
