@@ -60,6 +60,9 @@ def parse():
     ap.add_argument("--no-sweep", action="store_true", help="skip the size/replica sweep")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    ap.add_argument("--overlap", action="store_true",
+                    help="measure the all-reduce hidden behind a ViT-B/16 backward pass instead")
+    ap.add_argument("--batch", type=int, default=64, help="images per backward pass (--overlap)")
     return ap.parse_args()
 
 
@@ -195,15 +198,15 @@ class VitStep:
             self.numels, gar.AR_BF16, CAP, gar.AR_MEAN,
             sgd=(0.1, 0.9, [self.w[o[t]:o[t + 1]] for t in range(len(self.numels))],
                  [self.v[o[t]:o[t + 1]] for t in range(len(self.numels))], 1))
+        self.reverse = list(range(len(self.numels) - 1, -1, -1))
 
     def step(self, stream):
         """One step through the reducer: every gradient marked ready in
-        reverse registration order (as a backward pass produces them), then
-        the step is finalized on the caller's stream."""
-        red = self.reducer
-        for t in range(len(self.numels) - 1, -1, -1):
-            red.mark_ready(t, stream)
-        red.finalize(stream)
+        reverse registration order (as a backward pass produces them; each
+        bucket launches as soon as its last tensor is marked), then the step
+        is finalized on the caller's stream."""
+        self.reducer.mark_ready_many(self.reverse, stream)
+        self.reducer.finalize(stream)
 
     def step_serial(self, stream):
         """The same step as eight ar_bucket_all_reduce calls on one stream."""
@@ -519,12 +522,115 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- overlap
+
+def vit_b16_module(device, dtype):
+    """ViT-B/16 as the "Distributed Training" page builds it (patch 16,
+    width 768, 12 pre-norm encoder blocks, MLP 3072, 1000 classes), with
+    random initial weights."""
+    import torch
+    import torch.nn as nn
+    import workloads
+
+    class ViT(nn.Module):
+        def __init__(self):
+            super().__init__()
+            D = workloads.VIT_D
+            self.patch = nn.Conv2d(3, D, workloads.VIT_PATCH, stride=workloads.VIT_PATCH)
+            self.cls = nn.Parameter(torch.zeros(1, 1, D))
+            self.pos = nn.Parameter(torch.randn(1, workloads.VIT_TOKENS, D) * 0.02)
+            self.blocks = nn.ModuleList(
+                nn.TransformerEncoderLayer(D, 12, workloads.VIT_MLP, dropout=0.0, norm_first=True,
+                                           batch_first=True) for _ in range(workloads.VIT_LAYERS))
+            self.norm, self.head = nn.LayerNorm(D), nn.Linear(D, workloads.VIT_CLASSES)
+
+        def forward(self, x):
+            h = self.patch(x).flatten(2).transpose(1, 2)
+            h = torch.cat([self.cls.expand(h.shape[0], -1, -1), h], dim=1) + self.pos
+            for blk in self.blocks:
+                h = blk(h)
+            return self.head(self.norm(h[:, 0]))
+
+    torch.manual_seed(0)
+    return ViT().to(device=device, dtype=dtype)
+
+
+def run_overlap(args):
+    """DDP's point: hide the all-reduce behind the backward pass.  Rank 0's
+    forward + backward of ViT-B/16 (bf16) runs on the GPU while the
+    reducer launches each bucket (P = 8 replicas, Mean + fused SGD) from the
+    autograd hooks as its gradients become final; ranks 1..7's gradients
+    are synthetic.  Reports forward+backward alone, the gradient step
+    alone, and both overlapped."""
+    import torch
+    import gradient_all_reduce_gb300 as gar
+    from gradient_all_reduce_gb300.ddp import ReplicaDDP
+    from workloads import gpu as wgpu
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    model = vit_b16_module(device, torch.bfloat16)
+    comm = gar.ar_init(P_VIT, 0, gar.AR_MEAN)
+    ddp = ReplicaDDP(comm, model, P_VIT, CAP, gar.AR_MEAN, sgd=(0.1, 0.9))
+    try:
+        for r in range(1, P_VIT):
+            wgpu.fill(ddp.flat[r], "normal", 100 + r, std=1e-3)
+        g = torch.Generator(device=device).manual_seed(0)
+        x = torch.randn(args.batch, 3, 224, 224, device=device, dtype=torch.bfloat16, generator=g)
+        y = torch.randint(0, 1000, (args.batch,), device=device, generator=g)
+        reverse = list(range(len(ddp.params) - 1, -1, -1))
+        stream = torch.cuda.current_stream()
+
+        def fwd_bwd(hooks):
+            ddp.hooks_enabled = hooks
+            ddp.flat[0].zero_()
+            torch.nn.functional.cross_entropy(model(x), y).backward()
+            if hooks:
+                ddp.finish()
+
+        def sync_only():
+            ddp.reducer.mark_ready_many(reverse, stream)
+            ddp.finish()
+
+        def timed(fn, reps):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / reps
+
+        reps = max(5, min(args.steps, 50))
+        t_fb = timed(lambda: fwd_bwd(False), reps)
+        t_sync = timed(sync_only, reps)
+        t_ov = timed(lambda: fwd_bwd(True), reps)
+        t_seq = timed(lambda: (fwd_bwd(False), sync_only()), reps)
+        if gar.ar_get_async_error(comm) != gar.AR_OK:
+            raise RuntimeError("device status")
+        print(json.dumps({
+            "mode": "overlap", "model": "ViT-B/16 (bf16, random init)", "batch": args.batch,
+            "P": P_VIT, "buckets": len(set(ddp.reducer.bucket_of())), "reps": reps,
+            "fwd_bwd_ms": t_fb, "grad_step_ms": t_sync, "sequential_ms": t_seq,
+            "overlapped_ms": t_ov,
+            "hidden_fraction": (t_seq - t_ov) / t_sync,
+            "speedup_vs_sequential": t_seq / t_ov}), flush=True)
+    finally:
+        ddp.close()
+        gar.ar_destroy(comm)
+
+
 # -------------------------------------------------------------------- main
 
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.overlap:
+        run_overlap(args)
         return
     rank, world, local = dist_env()
     import torch

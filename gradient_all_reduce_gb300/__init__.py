@@ -70,6 +70,7 @@ def _load() -> ctypes.CDLL:
         "ar_reducer_create": [ctypes.POINTER(P), P, ctypes.POINTER(ar_bucket_t), ctypes.c_size_t,
                               ctypes.c_int, ctypes.POINTER(ar_sgd_t)],
         "ar_reducer_mark_ready": [P, ctypes.c_int, P],
+        "ar_reducer_mark_ready_many": [P, ctypes.POINTER(ctypes.c_int), ctypes.c_int, P],
         "ar_reducer_finalize": [P, P],
         "ar_reducer_set_sgd": [P, ctypes.c_float, ctypes.c_float],
         "ar_reducer_info": [P, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)],
@@ -273,6 +274,11 @@ class Reducer:
 
     def mark_ready(self, tensor: int, stream=None) -> None:
         _ok(self._mark(self.handle, int(tensor), _stream(stream)), "ar_reducer_mark_ready")
+
+    def mark_ready_many(self, tensors: Sequence[int], stream=None) -> None:
+        arr = (ctypes.c_int * max(len(tensors), 1))(*[int(t) for t in tensors])
+        _ok(load().ar_reducer_mark_ready_many(self.handle, arr, len(tensors), _stream(stream)),
+            "ar_reducer_mark_ready_many")
 
     def finalize(self, stream=None) -> None:
         _ok(load().ar_reducer_finalize(self.handle, _stream(stream)), "ar_reducer_finalize")

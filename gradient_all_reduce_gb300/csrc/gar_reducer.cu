@@ -221,6 +221,21 @@ ar_status_t ar_reducer_mark_ready(ar_reducer_t r, int tensor, ar_stream_t stream
   return AR_OK;
 }
 
+ar_status_t ar_reducer_mark_ready_many(ar_reducer_t r, const int* tensors, int n,
+                                       ar_stream_t stream) {
+  if (!reducer_live(r) || !is_live(r->comm)) return AR_ERR_STATE;
+  if (n < 0 || (n > 0 && tensors == nullptr)) return AR_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i) {
+    if (tensors[i] < 0 || tensors[i] >= r->ntensors) return AR_ERR_INVALID_ARG;
+    if (r->marked[tensors[i]]) return AR_ERR_STATE;
+  }
+  for (int i = 0; i < n; ++i) {
+    ar_status_t st = ar_reducer_mark_ready(r, tensors[i], stream);
+    if (st != AR_OK) return st;
+  }
+  return AR_OK;
+}
+
 ar_status_t ar_reducer_finalize(ar_reducer_t r, ar_stream_t stream) {
   if (!reducer_live(r) || !is_live(r->comm)) return AR_ERR_STATE;
   DeviceGuard guard(r->comm->device);

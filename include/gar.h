@@ -233,6 +233,13 @@ ar_status_t ar_reducer_create(ar_reducer_t *reducer, ar_comm_t comm, const ar_bu
  */
 ar_status_t ar_reducer_mark_ready(ar_reducer_t reducer, int tensor, ar_stream_t stream);
 
+/* ar_reducer_mark_ready for tensors[0], tensors[1], ... in that order (one
+ * call for a group of gradients that become final together).  Checks every
+ * index first: nothing is marked when one is out of range or already
+ * marked (a repeated index within the list is refused when reached). */
+ar_status_t ar_reducer_mark_ready_many(ar_reducer_t reducer, const int *tensors, int n,
+                                       ar_stream_t stream);
+
 /*
  * End of the step: launches every bucket not launched yet (its unmarked
  * tensors are taken as ready on `stream`), makes `stream` wait for all the

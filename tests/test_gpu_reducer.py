@@ -166,3 +166,25 @@ def test_reducer_learning_rate_schedule_and_errors():
         red.handle = 1234
         red.finalize()
     assert e.value.status == gar.AR_ERR_STATE
+
+
+def test_reducer_mark_ready_many_checks_first():
+    P = 2
+    numels = [300, 500]
+    offs = np.concatenate([[0], np.cumsum(numels)])
+    n = int(offs[-1])
+    flat, w, v, grads, ws, vs = _setup(P, numels, offs, dt="f32", seed=60)
+    comm = gar.ar_init(P, 0, gar.AR_SUM)
+    red = gar.Reducer(comm, grads, numels, gar.AR_F32, 25 << 20, gar.AR_SUM)
+    try:
+        with pytest.raises(gar.GarError) as e:
+            red.mark_ready_many([1, 7])             # 7 is out of range: nothing is marked
+        assert e.value.status == gar.AR_ERR_INVALID_ARG
+        red.mark_ready_many([1, 0])
+        red.finalize()
+        torch.cuda.synchronize()
+    finally:
+        red.destroy()
+        gar.ar_destroy(comm)
+    want = oracle.all_reduce(host_replicas(P, n, "f32", "normal", 60, std=1e-3), op=oracle.SUM)
+    assert_bits_equal(to_np(flat[0]), want[0], "marked together")
