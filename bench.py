@@ -265,14 +265,20 @@ def time_vit(args, device, stream, world):
         barrier(world)
         torch.cuda.synchronize(device)
         with ClockSampler(device.index) as clocks, torch.cuda.stream(stream):
-            h0 = time.perf_counter()
             start.record(stream)
             for _ in range(K):
                 vs.step(stream)
             stop.record(stream)
-            host_s = time.perf_counter() - h0
             torch.cuda.synchronize(device)
         elapsed = start.elapsed_time(stop) / 1e3
+        # Host time to issue one step, on a burst short enough that the
+        # launch queue never fills (a full queue makes the host wait).
+        with torch.cuda.stream(stream):
+            h0 = time.perf_counter()
+            for _ in range(8):
+                vs.step(stream)
+            host_s = (time.perf_counter() - h0) * K / 8
+            torch.cuda.synchronize(device)
 
         # Serialized launches with per-launch events (kernel roofline).
         nb = len(vs.calls)
@@ -603,20 +609,40 @@ def run_overlap(args):
             torch.cuda.synchronize()
             return e0.elapsed_time(e1) / reps
 
+        def graphed(fn):
+            """fn captured in a CUDA graph (after warm-up on a side stream):
+            replays carry no host overhead, so only GPU-side overlap shows."""
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                for _ in range(3):
+                    fn()
+            torch.cuda.current_stream().wait_stream(side)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                fn()
+            return graph.replay
+
         reps = max(5, min(args.steps, 50))
-        t_fb = timed(lambda: fwd_bwd(False), reps)
-        t_sync = timed(sync_only, reps)
-        t_ov = timed(lambda: fwd_bwd(True), reps)
-        t_seq = timed(lambda: (fwd_bwd(False), sync_only()), reps)
+        eager = {"fwd_bwd_ms": timed(lambda: fwd_bwd(False), reps),
+                 "grad_step_ms": timed(sync_only, reps),
+                 "overlapped_ms": timed(lambda: fwd_bwd(True), reps),
+                 "sequential_ms": timed(lambda: (fwd_bwd(False), sync_only()), reps)}
+        g_fb, g_sync = graphed(lambda: fwd_bwd(False)), graphed(sync_only)
+        g_ov = graphed(lambda: fwd_bwd(True))
+        graphs = {"fwd_bwd_ms": timed(g_fb, reps), "grad_step_ms": timed(g_sync, reps),
+                  "overlapped_ms": timed(g_ov, reps),
+                  "sequential_ms": timed(lambda: (g_fb(), g_sync()), reps)}
+        for d in (eager, graphs):
+            d["hidden_fraction"] = (d["sequential_ms"] - d["overlapped_ms"]) / d["grad_step_ms"]
+            d["speedup_vs_sequential"] = d["sequential_ms"] / d["overlapped_ms"]
         if gar.ar_get_async_error(comm) != gar.AR_OK:
             raise RuntimeError("device status")
         print(json.dumps({
             "mode": "overlap", "model": "ViT-B/16 (bf16, random init)", "batch": args.batch,
             "P": P_VIT, "buckets": len(set(ddp.reducer.bucket_of())), "reps": reps,
-            "fwd_bwd_ms": t_fb, "grad_step_ms": t_sync, "sequential_ms": t_seq,
-            "overlapped_ms": t_ov,
-            "hidden_fraction": (t_seq - t_ov) / t_sync,
-            "speedup_vs_sequential": t_seq / t_ov}), flush=True)
+            "cuda_graphs": graphs, "eager": eager}), flush=True)
     finally:
         ddp.close()
         gar.ar_destroy(comm)

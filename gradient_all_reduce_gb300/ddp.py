@@ -62,6 +62,7 @@ class ReplicaDDP:
         self.reducer = gar.Reducer(comm, grads, self.numels, _AR_DTYPE[dtype], cap_bytes, op,
                                    sgd=sgd_args)
         self.hooks_enabled = True
+        self._stream = None          # handle of the stream the current backward runs on
         self._handles = []
         for t, p in enumerate(self.params):
             self._handles.append(p.register_post_accumulate_grad_hook(self._hook(t)))
@@ -69,7 +70,9 @@ class ReplicaDDP:
     def _hook(self, t: int):
         def hook(_param):
             if self.hooks_enabled:
-                self.reducer.mark_ready(t, torch.cuda.current_stream())
+                if self._stream is None:   # looked up once per step
+                    self._stream = torch.cuda.current_stream().cuda_stream
+                self.reducer.mark_ready(t, self._stream)
         return hook
 
     def replica_grad(self, rank: int, t: int) -> torch.Tensor:
@@ -89,6 +92,7 @@ class ReplicaDDP:
     def finish(self, stream=None) -> None:
         """End of the step: every bucket launched, the stream ordered after them."""
         self.reducer.finalize(torch.cuda.current_stream() if stream is None else stream)
+        self._stream = None
 
     def close(self) -> None:
         for h in self._handles:
