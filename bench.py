@@ -584,7 +584,6 @@ def run_overlap(args):
         x = torch.randn(args.batch, 3, 224, 224, device=device, dtype=torch.bfloat16, generator=g)
         y = torch.randint(0, 1000, (args.batch,), device=device, generator=g)
         reverse = list(range(len(ddp.params) - 1, -1, -1))
-        stream = torch.cuda.current_stream()
 
         def fwd_bwd(hooks):
             ddp.hooks_enabled = hooks
@@ -594,8 +593,9 @@ def run_overlap(args):
                 ddp.finish()
 
         def sync_only():
-            ddp.reducer.mark_ready_many(reverse, stream)
-            ddp.finish()
+            s = torch.cuda.current_stream()     # the capture stream while graphing
+            ddp.reducer.mark_ready_many(reverse, s)
+            ddp.finish(s)
 
         def timed(fn, reps):
             for _ in range(3):
