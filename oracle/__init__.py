@@ -69,8 +69,16 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
         ctypes.c_int, ctypes.c_float, ctypes.c_float, _c_ptrs, _c_ptrs, ctypes.c_int]
     lib.oracle_bucket_plan.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_uint64),
                                        ctypes.c_uint64, ctypes.POINTER(ctypes.c_int)]
+    lib.oracle_bucket_accumulate.argtypes = [
+        ctypes.c_int, ctypes.c_int, _c_ptrs, ctypes.POINTER(ctypes.c_uint64), ctypes.c_int,
+        _c_ptrs, ctypes.c_float, ctypes.c_int]
+    lib.oracle_bucket_all_reduce_accumulated.argtypes = [
+        ctypes.c_int, ctypes.c_int, _c_ptrs, ctypes.POINTER(ctypes.c_uint64), ctypes.c_int,
+        ctypes.c_int, _c_ptrs, ctypes.c_float, ctypes.c_int, ctypes.c_float, ctypes.c_float,
+        _c_ptrs, _c_ptrs, ctypes.c_int]
     for f in ("oracle_all_reduce", "oracle_reduce_scatter", "oracle_all_gather",
-              "oracle_broadcast", "oracle_bucket_all_reduce", "oracle_bucket_plan"):
+              "oracle_broadcast", "oracle_bucket_all_reduce", "oracle_bucket_plan",
+              "oracle_bucket_accumulate", "oracle_bucket_all_reduce_accumulated"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -168,6 +176,45 @@ def bucket_all_reduce(tensors, op: int = MEAN, sgd=None, L=None) -> None:
         rc = L.oracle_bucket_all_reduce(P, T, _ptrs(flat), numel, dt, op, lr, mom,
                                         _ptrs(master), _ptrs(mbuf), int(wb))
     _check(rc, "bucket_all_reduce")
+
+
+def bucket_accumulate(tensors, acc, scale: float, first: bool, L=None) -> None:
+    """A micro-batch before the last: acc[t][r] (fp32) = (first ? 0 : acc) +
+    fl(scale * tensors[t][r]), in place; no all-reduce."""
+    L = L or lib()
+    T = len(tensors)
+    if T == 0:
+        return
+    P = len(tensors[0])
+    flat = [a for reps in tensors for a in reps]
+    accs = [a for reps in acc for a in reps]
+    numel = (ctypes.c_uint64 * T)(*[reps[0].size for reps in tensors])
+    _check(L.oracle_bucket_accumulate(P, T, _ptrs(flat), numel, _dtype_code(flat[0]),
+                                      _ptrs(accs), scale, int(first)), "bucket_accumulate")
+
+
+def bucket_all_reduce_accumulated(tensors, acc, scale: float, first: bool, op: int = MEAN,
+                                  sgd=None, L=None) -> None:
+    """The last micro-batch: all-reduce of every rank's acc + fl(scale * g)
+    (optionally fused with SGD), results into the gradient replicas."""
+    L = L or lib()
+    T = len(tensors)
+    if T == 0:
+        return
+    P = len(tensors[0])
+    flat = [a for reps in tensors for a in reps]
+    accs = [a for reps in acc for a in reps]
+    numel = (ctypes.c_uint64 * T)(*[reps[0].size for reps in tensors])
+    dt = _dtype_code(flat[0])
+    if sgd is None:
+        rc = L.oracle_bucket_all_reduce_accumulated(P, T, _ptrs(flat), numel, dt, op, _ptrs(accs),
+                                                    scale, int(first), 0.0, 0.0, None, None, 1)
+    else:
+        lr, mom, master, mbuf, wb = sgd
+        rc = L.oracle_bucket_all_reduce_accumulated(P, T, _ptrs(flat), numel, dt, op, _ptrs(accs),
+                                                    scale, int(first), lr, mom, _ptrs(master),
+                                                    _ptrs(mbuf), int(wb))
+    _check(rc, "bucket_all_reduce_accumulated")
 
 
 def bucket_plan(nbytes, cap_bytes: int = 25 << 20, L=None) -> list[int]:

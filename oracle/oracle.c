@@ -236,3 +236,77 @@ int oracle_bucket_plan(int ntensors, const uint64_t *nbytes, uint64_t cap_bytes,
     }
     return b + 1;
 }
+
+/*
+ * Gradient accumulation with DDP's no_sync ("Distributed Training",
+ * "Gradient accumulation": a device processes a batch as micro-batches in
+ * sequence and adds their gradients before one optimizer step, each
+ * micro-batch's loss divided by the number of micro-batches M; DDP's
+ * no_sync() skips the all-reduce until the last micro-batch).
+ *
+ * oracle_bucket_accumulate (a micro-batch before the last, no all-reduce):
+ * for every tensor t, rank r and element i, with s = fl(scale * g_r[i]),
+ *     acc_r[i] = first ? s : fl(acc_r[i] + s)
+ * acc is tensor-major like ptrs (acc[t*P + r], fp32, numel[t] elements).
+ *
+ * oracle_bucket_all_reduce_accumulated (the last micro-batch): every rank's
+ * total a_r[i] = first ? s : fl(acc_r[i] + s) is all-reduced exactly as
+ * oracle_bucket_all_reduce reduces the gradients themselves (rank order,
+ * Mean / P, optional SGD, result stored to every gradient replica unless
+ * SGD runs without write-back).  acc is not modified.
+ */
+int oracle_bucket_accumulate(int P, int ntensors, void *const *ptrs, const uint64_t *numel,
+                             int dtype, float *const *acc, float scale, int first)
+{
+    if (P < 1 || ntensors < 0 || (dtype != OR_F32 && dtype != OR_BF16))
+        return OR_BAD;
+    for (int t = 0; t < ntensors; ++t)
+        for (int r = 0; r < P; ++r) {
+            const void *g = ptrs[(size_t)t * (size_t)P + (size_t)r];
+            float *a = acc[(size_t)t * (size_t)P + (size_t)r];
+            for (size_t i = 0; i < numel[t]; ++i) {
+                float s = scale * load(g, i, dtype);
+                a[i] = first ? s : a[i] + s;
+            }
+        }
+    return OR_OK;
+}
+
+int oracle_bucket_all_reduce_accumulated(int P, int ntensors, void *const *ptrs,
+                                         const uint64_t *numel, int dtype, int op,
+                                         float *const *acc, float scale, int first, float lr,
+                                         float momentum, float *const *master,
+                                         float *const *momentum_buf, int write_back)
+{
+    enum { MAXP = 64 };
+    if (bad_args(P, dtype, op) || P > MAXP || ntensors < 0)
+        return OR_BAD;
+    int sgd = master != NULL && momentum_buf != NULL;
+    for (int t = 0; t < ntensors; ++t) {
+        void *const *x = ptrs + (size_t)t * (size_t)P;
+        float *const *a = acc + (size_t)t * (size_t)P;
+        for (size_t i = 0; i < numel[t]; ++i) {
+            float total[MAXP];
+            for (int r = 0; r < P; ++r) {
+                float s = scale * load(x[r], i, dtype);
+                total[r] = first ? s : a[r][i] + s;
+            }
+            float g = total[0];
+            for (int r = 1; r < P; ++r)
+                g = g + total[r];
+            if (op == OR_MEAN)
+                g = g / (float)P;
+            if (sgd) {
+                float *v = momentum_buf[t], *w = master[t];
+                float mv = momentum * v[i];
+                v[i] = mv + g;
+                float step = lr * v[i];
+                w[i] = w[i] - step;
+            }
+            if (!sgd || write_back)
+                for (int r = 0; r < P; ++r)
+                    store(x[r], i, dtype, g);
+        }
+    }
+    return OR_OK;
+}

@@ -340,11 +340,112 @@ def pin_bucket_plan(L):
             assert fill[b] + nb[nxt] > cap
 
 
+# ------------------------------------------------- accumulation (no_sync)
+
+def _accumulate_then_reduce(grads, scale, op, L, sgd=None):
+    """grads[m][t][r]: micro-batch m's gradient.  Accumulate every
+    micro-batch but the last, all-reduce on the last.  Returns (the reduced
+    gradient replicas of the last micro-batch, the accumulators)."""
+    M = len(grads)
+    # stale values from an earlier cycle: the first micro-batch must overwrite them
+    acc = [[np.full(x.size, 7.0, np.float32) for x in reps] for reps in grads[0]]
+    for m in range(M - 1):
+        oracle.bucket_accumulate(grads[m], acc, scale, m == 0, L=L)
+    last = [[x.copy() for x in reps] for reps in grads[M - 1]]
+    oracle.bucket_all_reduce_accumulated(last, acc, scale, M == 1, op=op, sgd=sgd, L=L)
+    return last, acc
+
+
+def pin_accumulation_undivided_is_m_times(L):
+    """The page's check: accumulating M micro-batch gradients without
+    dividing by M gives exactly M times the gradient.  Integer-valued
+    gradients keep every sum exact, so the results equal the exact integer
+    sums (brute force) and differ by exactly the factor M = 4."""
+    rng = np.random.default_rng(10)
+    P, M, sizes = 3, 4, (5, 17)
+    grads = [[[f32(rng.integers(-1000, 1000, n)) for _ in range(P)] for n in sizes]
+             for _ in range(M)]
+    undivided, _ = _accumulate_then_reduce(grads, 1.0, SUM, L)
+    divided, _ = _accumulate_then_reduce(grads, 1.0 / M, SUM, L)
+    for t, n in enumerate(sizes):
+        exact = np.sum([[g[t][r].astype(np.int64) for r in range(P)] for g in grads], axis=(0, 1))
+        for r in range(P):
+            assert np.array_equal(undivided[t][r].astype(np.int64), exact), (t, r)
+            assert np.array_equal(undivided[t][r], np.float32(M) * divided[t][r]), (t, r)
+
+
+def pin_accumulation_matches_numpy(L):
+    """Random gradients, scale 1/3: the accumulators and the reduced result
+    equal NumPy float32 arithmetic taken in the same order, bit for bit."""
+    rng = np.random.default_rng(11)
+    P, M, n = 4, 3, 1001
+    scale = np.float32(1.0 / 3.0)
+    for dt in ("f32", "bf16"):
+        g32 = [[[f32(rng.normal(0, 1, n))] for _ in range(P)] for _ in range(M)]
+        grads = [[[x[0] if dt == "f32" else (x[0].view(np.uint32) >> 16).astype(np.uint16)
+                   for x in reps]] for reps in g32]
+        wide = [[(x if x.dtype == np.float32 else (x.astype(np.uint32) << 16).view(np.float32))
+                 for x in reps[0]] for reps in grads]
+        for op in (SUM, MEAN):
+            out, acc = _accumulate_then_reduce(grads, float(scale), op, L)
+            want_acc = [np.multiply(scale, wide[0][r], dtype=np.float32) for r in range(P)]
+            for m in range(1, M - 1):
+                want_acc = [np.add(want_acc[r], np.multiply(scale, wide[m][r], dtype=np.float32),
+                                   dtype=np.float32) for r in range(P)]
+            totals = [np.add(want_acc[r], np.multiply(scale, wide[M - 1][r], dtype=np.float32),
+                             dtype=np.float32) for r in range(P)]
+            y = numpy_all_reduce(totals, op)
+            want = y if dt == "f32" else _torch_bf16_bits(y)
+            for r in range(P):
+                assert np.array_equal(bits(acc[0][r]), bits(want_acc[r])), (dt, op, r)
+                assert np.array_equal(bits(out[0][r]), bits(want)), (dt, op, r)
+
+
+def pin_accumulation_single_micro_batch_is_all_reduce(L):
+    """M = 1 with scale 1 is the plain all-reduce (and leaves acc alone)."""
+    rng = np.random.default_rng(12)
+    P = 5
+    xs = [f32(rng.normal(0, 1, 77)) for _ in range(P)]
+    want = oracle.all_reduce(xs, op=MEAN, L=L)
+    acc = [[np.full(77, 7.0, np.float32) for _ in range(P)]]
+    last = [[x.copy() for x in xs]]
+    oracle.bucket_all_reduce_accumulated(last, acc, 1.0, True, op=MEAN, L=L)
+    for r in range(P):
+        assert np.array_equal(bits(last[0][r]), bits(want[r])), r
+        assert np.all(acc[0][r] == 7.0)
+
+
+def pin_accumulation_with_sgd(L):
+    """The fused SGD step on the accumulated gradient equals the SGD step of
+    the bucketed all-reduce fed the per-rank totals (acc + scale g), over
+    two optimizer steps (so the momentum term matters)."""
+    rng = np.random.default_rng(13)
+    P, M, n = 2, 2, 300
+    w0 = f32(rng.normal(0, 0.02, n))
+    for wb in (0, 1):
+        w, v = [w0.copy()], [np.zeros(n, np.float32)]
+        w2, v2 = [w0.copy()], [np.zeros(n, np.float32)]
+        for step in range(2):
+            grads = [[[f32(rng.normal(0, 1e-3, n)) for _ in range(P)]] for _ in range(M)]
+            out, _ = _accumulate_then_reduce(grads, 0.5, MEAN, L, sgd=(0.1, 0.9, w, v, wb))
+            totals = [np.add(np.multiply(np.float32(0.5), grads[0][0][r], dtype=np.float32),
+                             np.multiply(np.float32(0.5), grads[1][0][r], dtype=np.float32),
+                             dtype=np.float32) for r in range(P)]
+            ref = [[x.copy() for x in totals]]
+            oracle.bucket_all_reduce(ref, op=MEAN, sgd=(0.1, 0.9, w2, v2, wb), L=L)
+            assert np.array_equal(bits(w[0]), bits(w2[0])), (wb, step)
+            assert np.array_equal(bits(v[0]), bits(v2[0])), (wb, step)
+            want = ref[0][0] if wb else grads[1][0][0]
+            assert np.array_equal(bits(out[0][0]), bits(want)), (wb, step)
+
+
 ALL_PINS = [
     pin_sum_integers_exact, pin_mean_rational_exact, pin_rank_order, pin_signed_zero,
     pin_matches_numpy_f32, pin_bf16_round_matches_torch, pin_bf16_widen_matches_torch,
     pin_bf16_all_reduce, pin_reduce_scatter_by_hand, pin_all_gather_by_hand,
     pin_rs_then_ag_is_all_reduce, pin_broadcast, pin_in_place_all_reduce,
     pin_bucket_equals_per_tensor, pin_sgd_closed_form, pin_sgd_matches_torch,
-    pin_sgd_write_back_flag, pin_bucket_plan,
+    pin_sgd_write_back_flag, pin_bucket_plan, pin_accumulation_undivided_is_m_times,
+    pin_accumulation_matches_numpy, pin_accumulation_single_micro_batch_is_all_reduce,
+    pin_accumulation_with_sgd,
 ]

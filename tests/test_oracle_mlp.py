@@ -92,3 +92,49 @@ def test_ddp_equivalence_full_size_oracle():
     for reps in tensors:                       # every replica holds the same mean
         for r in range(1, len(reps)):
             assert np.array_equal(reps[r], reps[0])
+
+
+def _micro_grads(ws, x, t, P, M):
+    """grads[m][k][r]: micro-batch m of rank r (rows split rank-major, then
+    into M equal micro-batches), each with its own mean loss."""
+    B = x.shape[0]
+    rows = B // (P * M)
+    out = []
+    for m in range(M):
+        per_rank = []
+        for r in range(P):
+            lo = (r * M + m) * rows
+            per_rank.append(mlp.forward_backward(ws, x[lo:lo + rows], t[lo:lo + rows])[1])
+        out.append([[per_rank[r][k] for r in range(P)] for k in range(len(ws))])
+    return out
+
+
+def test_accumulation_and_ddp_identity_fp64():
+    """P ranks x M micro-batches (loss / M each) reproduce the full-batch
+    gradient to fp64 round-off (the page prints 6.7e-16 for accumulation)."""
+    ws, x, t = _small(width=24, batch=32, seed=15)
+    P, M = 4, 2
+    full = mlp.forward_backward(ws, x, t)[1]
+    grads = _micro_grads(ws, x, t, P, M)
+    got = [sum(sum(grads[m][k][r] / M for m in range(M)) for r in range(P)) / P
+           for k in range(len(ws))]
+    assert mlp.linf_rel(got, full) <= 100 * float(table("ddp_equivalence.txt")["f64"])
+
+
+def test_accumulation_full_size_oracle():
+    """The DDP-equivalence MLP with each of the 8 ranks' 128 rows split into
+    2 micro-batches of 64: fp32 gradients accumulated with scale 1/2 and
+    all-reduced (Mean) on the last micro-batch by the oracle are within the
+    1e-5 acceptance bound of the fp64 full-batch gradient."""
+    ws, x, t = workloads.mlp_problem()
+    P, M = workloads.MLP_SHARDS, 2
+    full = mlp.forward_backward(ws, x, t)[1]
+    grads = _micro_grads(ws, x, t, P, M)
+    g32 = [[[np.ascontiguousarray(a, dtype=np.float32).ravel() for a in reps] for reps in gm]
+           for gm in grads]
+    acc = [[np.zeros(a.size, np.float32) for a in reps] for reps in g32[0]]
+    oracle.bucket_accumulate(g32[0], acc, 0.5, True)
+    oracle.bucket_all_reduce_accumulated(g32[1], acc, 0.5, False, op=oracle.MEAN)
+    got = [g32[1][k][0].reshape(full[k].shape) for k in range(len(ws))]
+    err = mlp.linf_rel(got, full)
+    assert err <= float(table("ddp_equivalence.txt")["accept"]), err

@@ -1,6 +1,6 @@
 """Planted mistakes in copies of the oracle must each fail at least one pin.
 
-Each case patches one line of ``oracle/oracle.c`` in a temporary copy (a
+Each case patches one place of ``oracle/oracle.c`` in a temporary copy (a
 dropped term, a reversed order, a wrong divisor, a wrong rounding rule, a
 wrong index or sign), builds it with the same flags, and runs the pins of
 ``pins.py`` until one fails.  The unpatched oracle passes them all
@@ -42,20 +42,39 @@ MUTANTS = {
     "plan_forward_order": ("for (int t = ntensors - 1; t >= 0; --t)",
                            "for (int t = 0; t < ntensors; ++t)"),
     "plan_closes_at_cap": ("fill + nbytes[t] > cap_bytes", "fill + nbytes[t] >= cap_bytes"),
+    "accum_scale_ignored": ("float s = scale * load(g, i, dtype);", "float s = load(g, i, dtype);"),
+    "accum_first_ignored": ("a[i] = first ? s : a[i] + s;", "a[i] = a[i] + s;"),
+    "accum_final_drops_acc": ("total[r] = first ? s : a[r][i] + s;", "total[r] = s;"),
+    "accum_final_scale_ignored": ("float s = scale * load(x[r], i, dtype);",
+                                  "float s = load(x[r], i, dtype);"),
 }
 
 
-@pytest.mark.parametrize("name", sorted(MUTANTS))
-def test_planted_mistake_fails_a_pin(name, tmp_path):
+def _cases():
+    """(mutant name, occurrence): a target that appears in several functions
+    is planted in each of them separately."""
+    src = oracle.SRC.read_text()
+    out = []
+    for name in sorted(MUTANTS):
+        n = src.count(MUTANTS[name][0])
+        out += [(name, k) for k in range(max(n, 1))]
+    return out
+
+
+@pytest.mark.parametrize("name,occurrence", _cases())
+def test_planted_mistake_fails_a_pin(name, occurrence, tmp_path):
     old, new = MUTANTS[name]
     src = oracle.SRC.read_text()
-    assert src.count(old) == 1, f"mutation target of {name} not found exactly once"
+    assert src.count(old) >= 1, f"mutation target of {name} not found"
+    at = -1
+    for _ in range(occurrence + 1):
+        at = src.index(old, at + 1)
     mutant = tmp_path / "oracle_mutant.c"
-    mutant.write_text(src.replace(old, new))
+    mutant.write_text(src[:at] + new + src[at + len(old):])
     L = oracle.load(oracle.build(src=mutant, out=tmp_path / "liboracle_mutant.so"))
     for pin in pins.ALL_PINS:
         try:
             pin(L)
         except AssertionError:
             return
-    pytest.fail(f"planted mistake {name} passed every pin")
+    pytest.fail(f"planted mistake {name} (occurrence {occurrence}) passed every pin")
