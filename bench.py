@@ -458,6 +458,34 @@ def time_sweep(device, stream):
                     del xs
         finally:
             gar.ar_destroy(comm)
+    # No_sync accumulation on one ViT-sized bucket (25 MiB of bf16 per
+    # replica, P = 8): a micro-batch before the last (acc += g / M) and the
+    # last one fused with the all-reduce and the SGD step.
+    comm = gar.ar_init(8, device.index, gar.AR_MEAN)
+    try:
+        P, n = 8, (25 << 20) // 2
+        g = [torch.empty(n, dtype=torch.bfloat16, device=device) for _ in range(P)]
+        for r, x in enumerate(g):
+            wgpu.fill(x, "normal", 100 + r, std=1e-3)
+        acc = [torch.zeros(n, dtype=torch.float32, device=device) for _ in range(P)]
+        w = torch.zeros(n, dtype=torch.float32, device=device)
+        v = torch.zeros(n, dtype=torch.float32, device=device)
+        ts, accs = [[x for x in g]], [[a for a in acc]]
+        t_first = timed(lambda: gar.ar_bucket_accumulate(comm, ts, [n], gar.AR_BF16, accs, 0.25,
+                                                         True, stream), 10)
+        t_mid = timed(lambda: gar.ar_bucket_accumulate(comm, ts, [n], gar.AR_BF16, accs, 0.25,
+                                                       False, stream), 10)
+        t_last = timed(lambda: gar.ar_bucket_all_reduce_accumulated(
+            comm, ts, [n], gar.AR_BF16, accs, 0.25, False, gar.AR_MEAN,
+            sgd=(0.1, 0.9, [w], [v], 1), stream=stream), 10)
+        out["accumulate_bucket_25MiB_P8_bf16"] = {
+            "first_us": t_first * 1e6, "first_GBps": 6 * P * n / t_first / 1e9,
+            "next_us": t_mid * 1e6, "next_GBps": 10 * P * n / t_mid / 1e9,
+            "last_fused_sgd_us": t_last * 1e6,
+            "last_fused_sgd_GBps": (8 * P * n + 16 * n) / t_last / 1e9}
+        del g, acc, w, v
+    finally:
+        gar.ar_destroy(comm)
     del flush
     torch.cuda.empty_cache()
     return out

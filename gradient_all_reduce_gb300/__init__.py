@@ -40,6 +40,11 @@ class ar_bucket_t(ctypes.Structure):
                 ("numel", ctypes.POINTER(ctypes.c_size_t)), ("dtype", ctypes.c_int)]
 
 
+class ar_accum_t(ctypes.Structure):
+    _fields_ = [("acc", ctypes.POINTER(ctypes.c_void_p)), ("scale", ctypes.c_float),
+                ("first", ctypes.c_int)]
+
+
 class ar_sgd_t(ctypes.Structure):
     _fields_ = [("lr", ctypes.c_float), ("momentum", ctypes.c_float),
                 ("master", ctypes.POINTER(ctypes.c_void_p)),
@@ -63,6 +68,10 @@ def _load() -> ctypes.CDLL:
         "ar_broadcast": [P, PP, ctypes.c_size_t, ctypes.c_int, ctypes.c_int, P],
         "ar_bucket_all_reduce": [P, ctypes.POINTER(ar_bucket_t), ctypes.c_int,
                                  ctypes.POINTER(ar_sgd_t), P],
+        "ar_bucket_accumulate": [P, ctypes.POINTER(ar_bucket_t), ctypes.POINTER(ar_accum_t), P],
+        "ar_bucket_all_reduce_accumulated": [P, ctypes.POINTER(ar_bucket_t),
+                                             ctypes.POINTER(ar_accum_t), ctypes.c_int,
+                                             ctypes.POINTER(ar_sgd_t), P],
         "ar_bucket_plan": [ctypes.c_int, ctypes.POINTER(ctypes.c_size_t), ctypes.c_size_t,
                            ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)],
         "ar_get_async_error": [P],
@@ -196,6 +205,45 @@ def ar_bucket_all_reduce(comm: int, tensors: Sequence[Sequence], numel: Sequence
     _ok(load().ar_bucket_all_reduce(comm, ctypes.byref(b), int(op),
                                  ctypes.byref(s) if s is not None else None, _stream(stream)),
         "ar_bucket_all_reduce")
+
+
+def _bucket_struct(tensors, numel, dtype):
+    ptrs = _ptr_array([x for reps in tensors for x in reps])
+    nel = (ctypes.c_size_t * max(len(numel), 1))(*[int(n) for n in numel])
+    b = ar_bucket_t(len(tensors), ctypes.cast(ptrs, ctypes.POINTER(ctypes.c_void_p)),
+                    ctypes.cast(nel, ctypes.POINTER(ctypes.c_size_t)), int(dtype))
+    return b, (ptrs, nel)
+
+
+def ar_bucket_accumulate(comm: int, tensors: Sequence[Sequence], numel: Sequence[int], dtype: int,
+                         acc: Sequence[Sequence], scale: float, first: bool, stream=None) -> None:
+    """A micro-batch before the last (no all-reduce): ``acc[t][r]`` (fp32)
+    gets rank r's ``scale * tensors[t][r]`` (overwritten when ``first``)."""
+    b, keep = _bucket_struct(tensors, numel, dtype)
+    accp = _ptr_array([x for reps in acc for x in reps])
+    a = ar_accum_t(ctypes.cast(accp, ctypes.POINTER(ctypes.c_void_p)), float(scale), int(bool(first)))
+    _ok(load().ar_bucket_accumulate(comm, ctypes.byref(b), ctypes.byref(a), _stream(stream)),
+        "ar_bucket_accumulate")
+
+
+def ar_bucket_all_reduce_accumulated(comm: int, tensors: Sequence[Sequence], numel: Sequence[int],
+                                     dtype: int, acc: Sequence[Sequence], scale: float, first: bool,
+                                     op: int = AR_OP_DEFAULT, sgd=None, stream=None) -> None:
+    """The last micro-batch: all-reduce of every rank's acc + scale * grad
+    (optionally fused with SGD), results into the gradient replicas."""
+    b, keep = _bucket_struct(tensors, numel, dtype)
+    accp = _ptr_array([x for reps in acc for x in reps])
+    a = ar_accum_t(ctypes.cast(accp, ctypes.POINTER(ctypes.c_void_p)), float(scale), int(bool(first)))
+    s = None
+    if sgd is not None:
+        lr, mom, master, mbuf, wb = sgd
+        m, v = _ptr_array(master), _ptr_array(mbuf)
+        s = ar_sgd_t(float(lr), float(mom), ctypes.cast(m, ctypes.POINTER(ctypes.c_void_p)),
+                     ctypes.cast(v, ctypes.POINTER(ctypes.c_void_p)), int(bool(wb)))
+    _ok(load().ar_bucket_all_reduce_accumulated(comm, ctypes.byref(b), ctypes.byref(a), int(op),
+                                                ctypes.byref(s) if s is not None else None,
+                                                _stream(stream)),
+        "ar_bucket_all_reduce_accumulated")
 
 
 def ar_bucket_plan(nbytes: Sequence[int], cap_bytes: int = 25 << 20) -> list[int]:

@@ -401,6 +401,143 @@ ar_status_t ar_bucket_all_reduce(ar_comm_t comm, const ar_bucket_t* bucket, ar_o
   return AR_OK;
 }
 
+// Accumulator rules on top of the bucket's: every accumulator fp32, 4-byte
+// aligned, inside memory the device may use, and disjoint from every
+// gradient replica, master / momentum array and other accumulator.
+static ar_status_t check_acc_buffers(const ar_comm_s* comm, const ar_bucket_t* b,
+                                     const ar_sgd_t* sgd, const ar_accum_t* acc) {
+  if (acc == nullptr || (b->ntensors > 0 && acc->acc == nullptr)) return AR_ERR_INVALID_ARG;
+  const int T = b->ntensors, P = comm->nranks;
+  const size_t es = elem_bytes(b->dtype);
+  struct Range { uintptr_t lo, hi; };
+  std::vector<Range> ranges;
+  for (int t = 0; t < T; ++t) {
+    const size_t n = b->numel[t];
+    if (n == 0) continue;
+    for (int r = 0; r < P; ++r) {
+      const void* g = b->dev_ptrs[size_t(t) * P + r];
+      const float* a = acc->acc[size_t(t) * P + r];
+      if (a == nullptr || !aligned(a, 4)) return AR_ERR_INVALID_ARG;
+      if (!pointer_ok(comm, a, n * 4)) return AR_ERR_INVALID_ARG;
+      ranges.push_back({addr(g), addr(g) + n * es});
+      ranges.push_back({addr(a), addr(a) + n * 4});
+    }
+    if (sgd != nullptr) {
+      ranges.push_back({addr(sgd->master[t]), addr(sgd->master[t]) + n * 4});
+      ranges.push_back({addr(sgd->momentum_buf[t]), addr(sgd->momentum_buf[t]) + n * 4});
+    }
+  }
+  std::sort(ranges.begin(), ranges.end(), [](const Range& x, const Range& y) { return x.lo < y.lo; });
+  for (size_t k = 1; k < ranges.size(); ++k)
+    if (ranges[k].lo < ranges[k - 1].hi) return AR_ERR_INVALID_ARG;
+  return AR_OK;
+}
+
+ar_status_t ar_bucket_accumulate(ar_comm_t comm, const ar_bucket_t* grads, const ar_accum_t* acc,
+                                 ar_stream_t stream) {
+  if (!is_live(comm)) return AR_ERR_STATE;
+  if (grads == nullptr || !valid_dtype(grads->dtype) || grads->ntensors < 0) return AR_ERR_INVALID_ARG;
+  const int T = grads->ntensors, P = comm->nranks;
+  if (T == 0) return AR_OK;
+  if (grads->dev_ptrs == nullptr || grads->numel == nullptr) return AR_ERR_INVALID_ARG;
+  DeviceGuard guard(comm->device);
+  if (!guard.ok()) return AR_ERR_CUDA;
+  ar_status_t st = check_bucket_buffers(comm, grads, nullptr);
+  if (st == AR_OK) st = check_acc_buffers(comm, grads, nullptr, acc);
+  if (st != AR_OK) return st;
+  const size_t es = elem_bytes(grads->dtype);
+  const uint64_t tile = gar::accumulate_tile_elems(16 / int(es));
+  const cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  const gar::LaunchCtx ctx{comm->device, comm->num_sms, strm, false, comm->pdl};
+  // One segment per (tensor, rank): ptr = {gradient, accumulator}.
+  auto run = [&](auto& tab, int k0, int k1) -> ar_status_t {
+    init_table(tab, 1, 1, 2, 1, false);
+    tab.scale = acc->scale;
+    tab.first = acc->first ? 1 : 0;
+    for (int k = k0; k < k1; ++k) {
+      void* ptrs[2] = {grads->dev_ptrs[k], acc->acc[k]};
+      if (!add_segment(tab, ptrs, grads->numel[k / P], tile, vec_flag(ptrs, 2)))
+        return AR_ERR_INVALID_ARG;
+    }
+    if (tab.ntiles == 0) return AR_OK;
+    return from_cuda(grads->dtype == AR_F32 ? gar::launch_accumulate_f32(ctx, tab)
+                                            : gar::launch_accumulate_bf16(ctx, tab));
+  };
+  const int segs = T * P;
+  if (segs <= CapSmall::kSeg) {
+    SegTable<CapSmall> tab;
+    return run(tab, 0, segs);
+  }
+  std::vector<SegTable<CapLarge>> tabs(1);
+  for (int k0 = 0; k0 < segs; k0 += CapLarge::kSeg) {
+    ar_status_t s2 = run(tabs[0], k0, std::min(segs, k0 + CapLarge::kSeg));
+    if (s2 != AR_OK) return s2;
+  }
+  return AR_OK;
+}
+
+ar_status_t ar_bucket_all_reduce_accumulated(ar_comm_t comm, const ar_bucket_t* grads,
+                                             const ar_accum_t* acc, ar_op_t op,
+                                             const ar_sgd_t* sgd, ar_stream_t stream) {
+  if (!is_live(comm)) return AR_ERR_STATE;
+  ar_op_t rop;
+  if (grads == nullptr || !resolve_op(comm, op, &rop) || !valid_dtype(grads->dtype) ||
+      grads->ntensors < 0)
+    return AR_ERR_INVALID_ARG;
+  const int T = grads->ntensors, P = comm->nranks;
+  if (T == 0) return AR_OK;
+  if (grads->dev_ptrs == nullptr || grads->numel == nullptr) return AR_ERR_INVALID_ARG;
+  if (sgd != nullptr && (sgd->master == nullptr || sgd->momentum_buf == nullptr))
+    return AR_ERR_INVALID_ARG;
+  DeviceGuard guard(comm->device);
+  if (!guard.ok()) return AR_ERR_CUDA;
+  ar_status_t st = check_bucket_buffers(comm, grads, sgd);
+  if (st == AR_OK) st = check_acc_buffers(comm, grads, sgd, acc);
+  if (st != AR_OK) return st;
+  const size_t es = elem_bytes(grads->dtype);
+  const uint64_t tile = gar::reduce_acc_tile_elems(16 / int(es));
+  const cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  const gar::LaunchCtx ctx{comm->device, comm->num_sms, strm, false, comm->pdl};
+  // One segment per tensor: ptr = {P gradient replicas, P accumulators}.
+  auto run = [&](auto& tab, int t0, int t1) -> ar_status_t {
+    init_table(tab, P, P, 2 * P, 0, rop == AR_MEAN);
+    tab.scale = acc->scale;
+    tab.first = acc->first ? 1 : 0;
+    if (sgd != nullptr) {
+      tab.lr = sgd->lr;
+      tab.mu = sgd->momentum;
+      tab.write_back = sgd->write_back_grads ? 1 : 0;
+    }
+    for (int t = t0; t < t1; ++t) {
+      void* ptrs[2 * AR_MAX_RANKS];
+      for (int r = 0; r < P; ++r) {
+        ptrs[r] = grads->dev_ptrs[size_t(t) * P + r];
+        ptrs[P + r] = acc->acc[size_t(t) * P + r];
+      }
+      float* w = sgd ? sgd->master[t] : nullptr;
+      float* v = sgd ? sgd->momentum_buf[t] : nullptr;
+      float* extra[2] = {w, v};
+      if (!add_segment(tab, ptrs, grads->numel[t], tile, vec_flag(ptrs, 2 * P, extra, sgd ? 2 : 0),
+                       w, v))
+        return AR_ERR_INVALID_ARG;
+    }
+    if (tab.ntiles == 0) return AR_OK;
+    return from_cuda(grads->dtype == AR_F32 ? gar::launch_reduce_acc_f32(ctx, sgd != nullptr, tab)
+                                            : gar::launch_reduce_acc_bf16(ctx, sgd != nullptr, tab));
+  };
+  if (T <= CapSmall::kSeg && 2 * T * P <= CapSmall::kPtr) {
+    SegTable<CapSmall> tab;
+    return run(tab, 0, T);
+  }
+  const int per = std::min(CapLarge::kSeg, CapLarge::kPtr / (2 * P));
+  std::vector<SegTable<CapLarge>> tabs(1);
+  for (int t0 = 0; t0 < T; t0 += per) {
+    ar_status_t s2 = run(tabs[0], t0, std::min(T, t0 + per));
+    if (s2 != AR_OK) return s2;
+  }
+  return AR_OK;
+}
+
 ar_status_t ar_bucket_plan(int ntensors, const size_t* nbytes, size_t cap_bytes, int* bucket_of,
                            int* nbuckets) {
   if (ntensors < 0 || cap_bytes == 0 || nbuckets == nullptr) return AR_ERR_INVALID_ARG;

@@ -48,6 +48,8 @@ struct SegTable {
   int mean;                   // divide by P
   int write_back;             // SGD: also store the reduced gradient
   float lr, mu;               // SGD hyper-parameters
+  float scale;                // accumulation: factor on each micro-batch gradient
+  int first;                  // accumulation: 1 = overwrite the accumulators
   int stages;                 // bulk-copy kernel: shared-memory stages
   uint32_t stage_bytes;       // bulk-copy kernel: bytes per stage
   uint32_t* status;           // the comm's device status word (bounded waits)
@@ -204,6 +206,194 @@ __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTa
       }
     }
   }
+}
+
+// ------------------------------------------------------- accumulation
+// DDP's no_sync gradient accumulation.  k_accumulate (a micro-batch before
+// the last, no communication): segment = one (tensor, rank) pair, ptr[0] =
+// the gradient (D), ptr[1] = its fp32 accumulator; per element, with
+// s = fl(scale * g):  acc = first ? s : fl(acc + s).
+constexpr int kAccUnroll = 4;
+
+template <class D>
+__device__ __forceinline__ void acc_vec(const uint4& gv, float* acc, uint64_t e0, float scale,
+                                        bool first) {
+  float g[D::kElems];
+  D::unpack(gv, g);
+#pragma unroll
+  for (int q = 0; q < D::kElems / 4; ++q) {
+    float4 a = first ? make_float4(0.f, 0.f, 0.f, 0.f) : ld_f4(acc + e0 + 4 * q);
+    float* av = &a.x;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float sv = __fmul_rn(scale, g[4 * q + k]);
+      av[k] = first ? sv : __fadd_rn(av[k], sv);
+    }
+    st_f4(acc + e0 + 4 * q, a);
+  }
+}
+
+template <class D, class Cap>
+__global__ void __launch_bounds__(kThreads) k_accumulate(const __grid_constant__ SegTable<Cap> a) {
+  constexpr int E = D::kElems;
+  constexpr uint64_t kTileVec = uint64_t(kAccUnroll) * kThreads;
+  griddep_launch_dependents();
+  griddep_wait();
+  const bool first = a.first != 0;
+  uint32_t s = 0;
+  for (uint32_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
+    while (tile >= a.tile0[s + 1]) ++s;
+    const uint64_t n = a.numel[s];
+    const void* g = a.ptr[uint64_t(s) * a.stride];
+    float* acc = static_cast<float*>(a.ptr[uint64_t(s) * a.stride + 1]);
+    const uint64_t lt = tile - a.tile0[s];
+    if (a.flags[s] & kSegVec) {
+      const uint64_t nvec = n / E;
+      const uint64_t v0 = lt * kTileVec + threadIdx.x;
+      uint4 x[kAccUnroll];
+#pragma unroll
+      for (int u = 0; u < kAccUnroll; ++u) {
+        const uint64_t vi = v0 + uint64_t(u) * kThreads;
+        if (vi < nvec) x[u] = ld_stream(static_cast<const uint4*>(g) + vi);
+      }
+#pragma unroll
+      for (int u = 0; u < kAccUnroll; ++u) {
+        const uint64_t vi = v0 + uint64_t(u) * kThreads;
+        if (vi < nvec) acc_vec<D>(x[u], acc, vi * E, a.scale, first);
+      }
+      if (lt + 1 == a.tile0[s + 1] - a.tile0[s]) {
+        const uint64_t i = nvec * E + threadIdx.x;
+        if (i < n) {
+          const float sv = __fmul_rn(a.scale, D::load1(g, i));
+          acc[i] = first ? sv : __fadd_rn(acc[i], sv);
+        }
+      }
+    } else {
+      const uint64_t e0 = lt * kTileVec * E;
+      for (uint64_t k = threadIdx.x; k < kTileVec * E; k += kThreads) {
+        const uint64_t i = e0 + k;
+        if (i >= n) break;
+        const float sv = __fmul_rn(a.scale, D::load1(g, i));
+        acc[i] = first ? sv : __fadd_rn(acc[i], sv);
+      }
+    }
+  }
+}
+
+// k_reduce_accumulated (the last micro-batch): segment = one tensor, ptr[0
+// .. P) = its gradient replicas (also the destinations), ptr[P .. 2P) = the
+// replicas' fp32 accumulators.  Rank r's total is t_r = first ? s_r :
+// fl(acc_r + s_r) with s_r = fl(scale * g_r); the totals are reduced in rank
+// order exactly as k_reduce reduces gradients, then the optional SGD step
+// and the stores follow as in k_reduce.  The accumulators are only read.
+template <int PT>
+__device__ __forceinline__ float total_of(float g, float acc, float scale, bool first) {
+  const float sv = __fmul_rn(scale, g);
+  return first ? sv : __fadd_rn(acc, sv);
+}
+
+template <class D, int PT, bool SGD, class Cap>
+__global__ void __launch_bounds__(kThreads)
+    k_reduce_accumulated(const __grid_constant__ SegTable<Cap> a) {
+  constexpr int E = D::kElems;
+  constexpr int MAXP = Ranks<PT>::kMax;
+  const int np = a.np;
+  const bool mean = a.mean != 0, first = a.first != 0;
+  griddep_launch_dependents();
+  griddep_wait();
+  uint32_t s = 0;
+  for (uint32_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
+    while (tile >= a.tile0[s + 1]) ++s;
+    const uint64_t n = a.numel[s];
+    void* const* seg = a.ptr + uint64_t(s) * a.stride;
+    const uint64_t lt = tile - a.tile0[s];
+    const bool do_store = !SGD || a.write_back;
+    float* w = SGD ? a.master[s] : nullptr;
+    float* v = SGD ? a.mom[s] : nullptr;
+    if (a.flags[s] & kSegVec) {
+      const uint64_t nvec = n / E;
+      const uint64_t vi = lt * kThreads + threadIdx.x;
+      if (vi < nvec) {
+        uint4 in[MAXP];
+        float4 ac[MAXP][E / 4];
+#pragma unroll
+        for (int r = 0; r < MAXP; ++r)
+          if (Ranks<PT>::has(r, np)) {
+            in[r] = ld_stream(static_cast<const uint4*>(seg[r]) + vi);
+            if (!first) {
+#pragma unroll
+              for (int q = 0; q < E / 4; ++q)
+                ac[r][q] = ld_f4(static_cast<const float*>(seg[np + r]) + vi * E + 4 * q);
+            }
+          }
+        float g[E];
+#pragma unroll
+        for (int r = 0; r < MAXP; ++r) {
+          if (Ranks<PT>::has(r, np)) {
+            float x[E];
+            D::unpack(in[r], x);
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+              const float t = total_of<PT>(x[e], first ? 0.f : (&ac[r][e / 4].x)[e % 4], a.scale, first);
+              g[e] = r == 0 ? t : __fadd_rn(g[e], t);
+            }
+          }
+        }
+        if (mean) {
+#pragma unroll
+          for (int e = 0; e < E; ++e) g[e] = mean_of<PT>(g[e], np);
+        }
+        epilogue_vec<D, SGD>(g, w, v, vi * E, a.lr, a.mu);
+        if (do_store) {
+          const uint4 out = D::pack(g);
+          for (int d = 0; d < np; ++d) st_stream(static_cast<uint4*>(seg[d]) + vi, out);
+        }
+      }
+      if (lt + 1 == a.tile0[s + 1] - a.tile0[s]) {
+        const uint64_t i = nvec * E + threadIdx.x;
+        if (i < n) {
+          float g = 0.f;
+          for (int r = 0; r < MAXP; ++r)
+            if (Ranks<PT>::has(r, np)) {
+              const float t = total_of<PT>(D::load1(seg[r], i),
+                                           first ? 0.f : static_cast<const float*>(seg[np + r])[i],
+                                           a.scale, first);
+              g = r == 0 ? t : __fadd_rn(g, t);
+            }
+          if (mean) g = mean_of<PT>(g, np);
+          if constexpr (SGD) sgd_step(g, a.lr, a.mu, w[i], v[i]);
+          if (do_store)
+            for (int d = 0; d < np; ++d) D::store1(seg[d], i, g);
+        }
+      }
+    } else {
+      const uint64_t e0 = lt * uint64_t(kThreads) * E;
+      for (uint64_t k = threadIdx.x; k < uint64_t(kThreads) * E; k += kThreads) {
+        const uint64_t i = e0 + k;
+        if (i >= n) break;
+        float g = 0.f;
+        for (int r = 0; r < MAXP; ++r)
+          if (Ranks<PT>::has(r, np)) {
+            const float t = total_of<PT>(D::load1(seg[r], i),
+                                         first ? 0.f : static_cast<const float*>(seg[np + r])[i],
+                                         a.scale, first);
+            g = r == 0 ? t : __fadd_rn(g, t);
+          }
+        if (mean) g = mean_of<PT>(g, np);
+        if constexpr (SGD) sgd_step(g, a.lr, a.mu, w[i], v[i]);
+        if (do_store)
+          for (int d = 0; d < np; ++d) D::store1(seg[d], i, g);
+      }
+    }
+  }
+}
+
+// Tile sizes (elements) of the accumulation kernels.
+__host__ __device__ constexpr uint64_t accumulate_tile_elems(int elems_per_vec) {
+  return uint64_t(kAccUnroll) * kThreads * elems_per_vec;
+}
+__host__ __device__ constexpr uint64_t reduce_acc_tile_elems(int elems_per_vec) {
+  return uint64_t(kThreads) * elems_per_vec;
 }
 
 // Tiles of one segment, as the kernels above cut it.

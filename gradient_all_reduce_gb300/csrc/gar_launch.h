@@ -52,6 +52,16 @@ cudaError_t launch_reduce_f32(const LaunchCtx& ctx, bool sgd, const SegTable<Cap
 template <class Cap>
 cudaError_t launch_reduce_bf16(const LaunchCtx& ctx, bool sgd, const SegTable<Cap>& tab);
 
+// The accumulation kernels (DDP's no_sync) for fp32 or bf16 gradients.
+template <class Cap>
+cudaError_t launch_accumulate_f32(const LaunchCtx& ctx, const SegTable<Cap>& tab);
+template <class Cap>
+cudaError_t launch_accumulate_bf16(const LaunchCtx& ctx, const SegTable<Cap>& tab);
+template <class Cap>
+cudaError_t launch_reduce_acc_f32(const LaunchCtx& ctx, bool sgd, const SegTable<Cap>& tab);
+template <class Cap>
+cudaError_t launch_reduce_acc_bf16(const LaunchCtx& ctx, bool sgd, const SegTable<Cap>& tab);
+
 template <class Cap>
 cudaError_t launch_copy(const LaunchCtx& ctx, const SegTable<Cap>& tab);
 

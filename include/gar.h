@@ -185,6 +185,45 @@ ar_status_t ar_bucket_all_reduce(ar_comm_t comm, const ar_bucket_t *bucket, ar_o
                                  const ar_sgd_t *sgd, ar_stream_t stream);
 
 /*
+ * Gradient accumulation with DDP's no_sync ("Distributed Training",
+ * "Gradient accumulation": a batch processed as M micro-batches in sequence,
+ * their gradients added before one optimizer step, each micro-batch's loss
+ * divided by M; DDP's no_sync() skips the all-reduce until the last
+ * micro-batch).  acc is a HOST array of ntensors*P fp32 device pointers,
+ * tensor-major like ar_bucket_t.dev_ptrs (acc[t*P + r]: numel[t] elements,
+ * rank r's accumulator of tensor t).  scale multiplies every micro-batch
+ * gradient (1/M for the mean over M micro-batches; 1 to add them as they
+ * are).  first = 1 starts a cycle: the accumulators are overwritten.
+ */
+typedef struct {
+    float *const *acc;
+    float scale;
+    int first;
+} ar_accum_t;
+
+/*
+ * A micro-batch before the last, with no all-reduce: per tensor t, rank r
+ * and element i, with s = fl(scale * g_r[i]) (the gradient widened to fp32),
+ * acc_r[i] = first ? s : fl(acc_r[i] + s).  The gradients are only read.
+ * Buffer rules as for ar_bucket_all_reduce, plus: every accumulator is
+ * fp32, 4-byte aligned and disjoint from every other buffer.
+ */
+ar_status_t ar_bucket_accumulate(ar_comm_t comm, const ar_bucket_t *grads, const ar_accum_t *acc,
+                                 ar_stream_t stream);
+
+/*
+ * The last micro-batch: rank r's total t_r[i] = first ? s : fl(acc_r[i] + s)
+ * with s = fl(scale * g_r[i]) is all-reduced exactly as ar_bucket_all_reduce
+ * reduces gradients (rank order, Mean / P, the optional fused SGD step), and
+ * the result goes to every gradient replica (unless SGD runs without
+ * write-back).  The accumulators are only read; the next cycle starts with
+ * first = 1.  first = 1 with scale = 1 is exactly ar_bucket_all_reduce.
+ */
+ar_status_t ar_bucket_all_reduce_accumulated(ar_comm_t comm, const ar_bucket_t *grads,
+                                             const ar_accum_t *acc, ar_op_t op,
+                                             const ar_sgd_t *sgd, ar_stream_t stream);
+
+/*
  * Bucket assignment, host only.  nbytes[t] is tensor t's size in
  * registration order.  Tensors are taken from the last to the first and
  * added to the open bucket; one that would take a non-empty bucket past
