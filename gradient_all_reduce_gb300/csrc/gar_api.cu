@@ -129,6 +129,9 @@ ar_status_t ar_init(ar_comm_t* comm, int nranks, int cuda_device, ar_op_t defaul
   if (env != nullptr && std::strcmp(env, "tma") == 0) c->kernel_mode = 2;
   env = std::getenv("GAR_PDL");
   c->pdl = !(env != nullptr && std::strcmp(env, "0") == 0);
+  env = std::getenv("GAR_CTAS_PER_SM");
+  c->ctas_per_sm = env != nullptr ? std::atoi(env) : -1;
+  if (c->ctas_per_sm < -1 || c->ctas_per_sm > 32) c->ctas_per_sm = -1;
   if (cudaMalloc(&c->d_status, sizeof(uint32_t)) != cudaSuccess) {
     delete c;
     return AR_ERR_CUDA;
@@ -365,7 +368,7 @@ ar_status_t ar_bucket_all_reduce(ar_comm_t comm, const ar_bucket_t* bucket, ar_o
   if (chk != AR_OK) return chk;
 
   const bool tma = choose_tma(comm, P, sgd != nullptr, es);
-  const uint64_t tile = gar::reduce_tile(P, int(es), tma);
+  const uint64_t tile = gar::reduce_tile(P, int(es), tma, sgd != nullptr);
   const cudaStream_t strm = static_cast<cudaStream_t>(stream);
   auto fill = [&](auto& tab, int t0, int t1) -> ar_status_t {
     init_table(tab, P, P, P, 0, rop == AR_MEAN);

@@ -48,6 +48,16 @@ __device__ __forceinline__ void st_f4(float* p, const float4& v) {
                : "memory");
 }
 
+// Register fences: an empty volatile asm that "modifies" a loaded value.  It
+// keeps the arithmetic on that value after every earlier volatile load, so
+// a thread issues all of its loads before it waits on any of them.
+__device__ __forceinline__ void reg_fence(uint4& v) {
+  asm volatile("" : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w));
+}
+__device__ __forceinline__ void reg_fence(float4& v) {
+  asm volatile("" : "+f"(v.x), "+f"(v.y), "+f"(v.z), "+f"(v.w));
+}
+
 // Programmatic dependent launch: let the next kernel of the stream start
 // its launch now, and wait until the previous kernel has finished and its
 // writes are visible (both are no-ops when the launch did not opt in).

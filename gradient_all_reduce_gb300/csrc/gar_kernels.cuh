@@ -27,6 +27,14 @@ namespace gar {
 __host__ __device__ constexpr int unroll_for(int PT) {
   return PT == 0 ? 1 : (PT <= 4 ? 4 : (PT <= 8 ? 2 : 1));
 }
+// With the fused SGD step each vector also carries its fp32 master weights
+// and momentum (2 x E floats), all loaded up front: fewer vectors per thread.
+#ifndef GAR_SGD_UNROLL_P8
+#define GAR_SGD_UNROLL_P8 1
+#endif
+__host__ __device__ constexpr int unroll_for_sgd(int PT) {
+  return PT == 0 ? 1 : (PT <= 4 ? 2 : (PT <= 8 ? GAR_SGD_UNROLL_P8 : 1));
+}
 constexpr int kCopyUnroll = 4;
 
 // Segment table capacities: small launches (<= 16 segments) use a 4 KB
@@ -63,31 +71,46 @@ struct SegTable {
 
 // --------------------------------------------------------------- reduce
 
+// SGD on one vector's E elements, w and v already loaded (E / 4 float4
+// each); stores the updated w and v.
+template <class D>
+__device__ __forceinline__ void sgd_vec(const float (&g)[D::kElems], float4 (&w4)[D::kElems / 4],
+                                        float4 (&v4)[D::kElems / 4], float* w, float* v,
+                                        uint64_t e0, float lr, float mu) {
+#pragma unroll
+  for (int q = 0; q < D::kElems / 4; ++q) {
+    float* wq = &w4[q].x;
+    float* vq = &v4[q].x;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) sgd_step(g[4 * q + k], lr, mu, wq[k], vq[k]);
+    st_f4(v + e0 + 4 * q, v4[q]);
+    st_f4(w + e0 + 4 * q, w4[q]);
+  }
+}
+
+// The same when w and v still have to be loaded (one vector at a time).
 template <class D, bool SGD>
 __device__ __forceinline__ void epilogue_vec(float (&g)[D::kElems], float* w, float* v,
                                              uint64_t e0, float lr, float mu) {
   static_assert(D::kElems % 4 == 0, "vector holds whole float4 groups");
   if constexpr (SGD) {
+    float4 w4[D::kElems / 4], v4[D::kElems / 4];
 #pragma unroll
     for (int q = 0; q < D::kElems / 4; ++q) {
-      float4 wq = ld_f4(w + e0 + 4 * q);
-      float4 vq = ld_f4(v + e0 + 4 * q);
-      sgd_step(g[4 * q + 0], lr, mu, wq.x, vq.x);
-      sgd_step(g[4 * q + 1], lr, mu, wq.y, vq.y);
-      sgd_step(g[4 * q + 2], lr, mu, wq.z, vq.z);
-      sgd_step(g[4 * q + 3], lr, mu, wq.w, vq.w);
-      st_f4(v + e0 + 4 * q, vq);
-      st_f4(w + e0 + 4 * q, wq);
+      w4[q] = ld_f4(w + e0 + 4 * q);
+      v4[q] = ld_f4(v + e0 + 4 * q);
     }
+    sgd_vec<D>(g, w4, v4, w, v, e0, lr, mu);
   }
 }
 
 template <class D, int PT, bool SGD, class Cap>
 __global__ void __launch_bounds__(kThreads)
     k_reduce(const __grid_constant__ SegTable<Cap> a) {
-  constexpr int U = unroll_for(PT);
+  constexpr int U = SGD ? unroll_for_sgd(PT) : unroll_for(PT);
   constexpr int E = D::kElems;
   constexpr int MAXP = Ranks<PT>::kMax;
+  constexpr int WV = SGD ? E / 4 : 1;  // float4 groups of w (and of v) per vector
   constexpr uint64_t kTileVec = uint64_t(U) * kThreads;
   const int np = a.np;
   const bool mean = a.mean != 0;
@@ -107,7 +130,10 @@ __global__ void __launch_bounds__(kThreads)
     if (a.flags[s] & kSegVec) {
       const uint64_t nvec = n / E;
       const uint64_t v0 = lt * kTileVec + threadIdx.x;
+      // Every load of the tile (all replicas, and w, v with SGD) is issued
+      // before any arithmetic or store.
       uint4 in[U][MAXP];
+      float4 w4[U][WV], v4[U][WV];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const uint64_t vi = v0 + uint64_t(u) * kThreads;
@@ -116,6 +142,28 @@ __global__ void __launch_bounds__(kThreads)
           for (int r = 0; r < MAXP; ++r)
             if (Ranks<PT>::has(r, np))
               in[u][r] = ld_stream(static_cast<const uint4*>(seg[r]) + vi);
+          if constexpr (SGD) {
+#pragma unroll
+            for (int q = 0; q < WV; ++q) {
+              w4[u][q] = ld_f4(w + vi * E + 4 * q);
+              v4[u][q] = ld_f4(v + vi * E + 4 * q);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (v0 + uint64_t(u) * kThreads < nvec) {
+#pragma unroll
+          for (int r = 0; r < MAXP; ++r)
+            if (Ranks<PT>::has(r, np)) reg_fence(in[u][r]);
+          if constexpr (SGD) {
+#pragma unroll
+            for (int q = 0; q < WV; ++q) {
+              reg_fence(w4[u][q]);
+              reg_fence(v4[u][q]);
+            }
+          }
         }
       }
 #pragma unroll
@@ -124,7 +172,7 @@ __global__ void __launch_bounds__(kThreads)
         if (vi < nvec) {
           float g[E];
           reduce_vec<D, PT>(in[u], np, mean, g);
-          epilogue_vec<D, SGD>(g, w, v, vi * E, a.lr, a.mu);
+          if constexpr (SGD) sgd_vec<D>(g, w4[u], v4[u], w, v, vi * E, a.lr, a.mu);
           if (do_store) {
             const uint4 out = D::pack(g);
             for (int d = 0; d < a.ndst; ++d) st_stream(static_cast<uint4*>(dst[d]) + vi, out);
@@ -216,20 +264,19 @@ __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTa
 constexpr int kAccUnroll = 4;
 
 template <class D>
-__device__ __forceinline__ void acc_vec(const uint4& gv, float* acc, uint64_t e0, float scale,
-                                        bool first) {
+__device__ __forceinline__ void acc_vec(const uint4& gv, float4 (&a4)[D::kElems / 4], float* acc,
+                                        uint64_t e0, float scale, bool first) {
   float g[D::kElems];
   D::unpack(gv, g);
 #pragma unroll
   for (int q = 0; q < D::kElems / 4; ++q) {
-    float4 a = first ? make_float4(0.f, 0.f, 0.f, 0.f) : ld_f4(acc + e0 + 4 * q);
-    float* av = &a.x;
+    float* av = &a4[q].x;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const float sv = __fmul_rn(scale, g[4 * q + k]);
       av[k] = first ? sv : __fadd_rn(av[k], sv);
     }
-    st_f4(acc + e0 + 4 * q, a);
+    st_f4(acc + e0 + 4 * q, a4[q]);
   }
 }
 
@@ -250,16 +297,31 @@ __global__ void __launch_bounds__(kThreads) k_accumulate(const __grid_constant__
     if (a.flags[s] & kSegVec) {
       const uint64_t nvec = n / E;
       const uint64_t v0 = lt * kTileVec + threadIdx.x;
+      // All gradient and accumulator loads first, then the stores.
       uint4 x[kAccUnroll];
+      float4 a4[kAccUnroll][E / 4];
 #pragma unroll
       for (int u = 0; u < kAccUnroll; ++u) {
         const uint64_t vi = v0 + uint64_t(u) * kThreads;
-        if (vi < nvec) x[u] = ld_stream(static_cast<const uint4*>(g) + vi);
+        if (vi < nvec) {
+          x[u] = ld_stream(static_cast<const uint4*>(g) + vi);
+#pragma unroll
+          for (int q = 0; q < E / 4; ++q)
+            a4[u][q] = first ? make_float4(0.f, 0.f, 0.f, 0.f) : ld_f4(acc + vi * E + 4 * q);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kAccUnroll; ++u) {
+        if (v0 + uint64_t(u) * kThreads < nvec) {
+          reg_fence(x[u]);
+#pragma unroll
+          for (int q = 0; q < E / 4; ++q) reg_fence(a4[u][q]);
+        }
       }
 #pragma unroll
       for (int u = 0; u < kAccUnroll; ++u) {
         const uint64_t vi = v0 + uint64_t(u) * kThreads;
-        if (vi < nvec) acc_vec<D>(x[u], acc, vi * E, a.scale, first);
+        if (vi < nvec) acc_vec<D>(x[u], a4[u], acc, vi * E, a.scale, first);
       }
       if (lt + 1 == a.tile0[s + 1] - a.tile0[s]) {
         const uint64_t i = nvec * E + threadIdx.x;
@@ -396,10 +458,7 @@ __host__ __device__ constexpr uint64_t reduce_acc_tile_elems(int elems_per_vec) 
   return uint64_t(kThreads) * elems_per_vec;
 }
 
-// Tiles of one segment, as the kernels above cut it.
-__host__ __device__ constexpr uint64_t reduce_tile_elems(int PT, int elems_per_vec) {
-  return uint64_t(unroll_for(PT)) * kThreads * elems_per_vec;
-}
+// Tile of the copy kernel, in bytes.
 __host__ __device__ constexpr uint64_t copy_tile_bytes() {
   return uint64_t(kCopyUnroll) * kThreads * 16;
 }

@@ -12,9 +12,15 @@ struct LaunchCtx {
   int device;
   int num_sms;
   cudaStream_t stream;
-  bool tma;  // k_reduce_tma (bulk-copy pipeline) instead of k_reduce
-  bool pdl;  // launch with programmatic stream serialization
+  bool tma;             // k_reduce_tma (bulk-copy pipeline) instead of k_reduce
+  bool pdl;             // launch with programmatic stream serialization
+  int ctas_per_sm = 0;  // cap on resident CTAs per SM used to size grids (0: occupancy)
 };
+
+// CTAs per SM a launch may plan for: the occupancy limit, or the comm's cap.
+inline int plan_ctas(const LaunchCtx& ctx, int resident) {
+  return ctx.ctas_per_sm > 0 && ctx.ctas_per_sm < resident ? ctx.ctas_per_sm : resident;
+}
 
 // Launch `kernel<<<grid, block, smem, ctx.stream>>>(tab)`, opting in to
 // programmatic dependent launch when ctx.pdl is set.
@@ -69,11 +75,12 @@ cudaError_t launch_copy(const LaunchCtx& ctx, const SegTable<Cap>& tab);
 cudaError_t launch_wait_selftest(cudaStream_t stream, uint32_t* status, uint64_t limit_ns);
 
 // Tile size in elements of k_reduce (or k_reduce_tma when tma is set) for
-// P ranks and the given element size.
-inline uint64_t reduce_tile(int P, int elem_bytes, bool tma = false) {
+// P ranks, the given element size, and with or without the SGD step.
+inline uint64_t reduce_tile(int P, int elem_bytes, bool tma = false, bool sgd = false) {
   if (tma) return tma_tile_elems(16 / elem_bytes);
   const int PT = (P == 2 || P == 4 || P == 8) ? P : 0;
-  return reduce_tile_elems(PT, 16 / elem_bytes);
+  const int U = sgd ? unroll_for_sgd(PT) : unroll_for(PT);
+  return uint64_t(U) * kThreads * (16 / elem_bytes);
 }
 
 // Persistent grid: at most (resident CTAs per SM) x (SMs), and as few CTAs

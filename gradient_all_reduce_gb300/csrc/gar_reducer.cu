@@ -83,11 +83,11 @@ ar_status_t launch_bucket(ar_reducer_s* r, int b) {
     if (cudaStreamWaitEvent(s, r->join, 0) != cudaSuccess) return AR_ERR_CUDA;
   }
   for (const auto& t : bk.small) {
-    ar_status_t st = run_reduce(r->comm, r->dtype, r->sgd, t, s);
+    ar_status_t st = run_reduce(r->comm, r->dtype, r->sgd, t, s, true);
     if (st != AR_OK) return st;
   }
   for (const auto& t : bk.large) {
-    ar_status_t st = run_reduce(r->comm, r->dtype, r->sgd, t, s);
+    ar_status_t st = run_reduce(r->comm, r->dtype, r->sgd, t, s, true);
     if (st != AR_OK) return st;
   }
   if (cudaEventRecord(r->done[k], s) != cudaSuccess) return AR_ERR_CUDA;
@@ -147,7 +147,7 @@ ar_status_t ar_reducer_create(ar_reducer_t* out, ar_comm_t comm, const ar_bucket
   for (int t = T - 1; t >= 0; --t) r->buckets[r->bucket_of[t]].tensors.push_back(t);
 
   const bool tma = choose_tma(comm, P, r->sgd, es);
-  const uint64_t tile = gar::reduce_tile(P, int(es), tma);
+  const uint64_t tile = gar::reduce_tile(P, int(es), tma, r->sgd);
   auto fill = [&](auto& tab, const std::vector<int>& ts, size_t t0, size_t t1) -> bool {
     init_table(tab, P, P, P, 0, rop == AR_MEAN);
     if (tma) set_tma(tab, comm, r->sgd, es);
