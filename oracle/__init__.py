@@ -76,7 +76,11 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
         ctypes.c_int, ctypes.c_int, _c_ptrs, ctypes.POINTER(ctypes.c_uint64), ctypes.c_int,
         ctypes.c_int, _c_ptrs, ctypes.c_float, ctypes.c_int, ctypes.c_float, ctypes.c_float,
         _c_ptrs, _c_ptrs, ctypes.c_int]
-    for f in ("oracle_all_reduce", "oracle_reduce_scatter", "oracle_all_gather",
+    lib.oracle_sharded_sgd_step.argtypes = [
+        ctypes.c_int, _c_ptrs, _c_ptrs, _c_ptrs, _c_ptrs, ctypes.c_size_t, ctypes.c_int,
+        ctypes.c_int, ctypes.c_float, ctypes.c_float]
+    for f in ("oracle_sharded_sgd_step", "oracle_all_reduce", "oracle_reduce_scatter",
+              "oracle_all_gather",
               "oracle_broadcast", "oracle_bucket_all_reduce", "oracle_bucket_plan",
               "oracle_bucket_accumulate", "oracle_bucket_all_reduce_accumulated"):
         getattr(lib, f).restype = ctypes.c_int
@@ -215,6 +219,18 @@ def bucket_all_reduce_accumulated(tensors, acc, scale: float, first: bool, op: i
                                                     scale, int(first), lr, mom, _ptrs(master),
                                                     _ptrs(mbuf), int(wb))
     _check(rc, "bucket_all_reduce_accumulated")
+
+
+def sharded_sgd_step(grads, params, w_shards, v_shards, lr: float, momentum: float,
+                     op: int = MEAN, L=None) -> None:
+    """ZeRO-1 step: reduce-scatter of grads, each owner's SGD on its fp32
+    shard (in place), all-gather of the updated weights into every params
+    replica (rounded to the replicas' dtype)."""
+    L = L or lib()
+    P, n = len(grads), grads[0].size
+    _check(L.oracle_sharded_sgd_step(P, _ptrs(grads), _ptrs(params), _ptrs(w_shards),
+                                     _ptrs(v_shards), n, _dtype_code(grads[0]), op, lr,
+                                     momentum), "sharded_sgd_step")
 
 
 def bucket_plan(nbytes, cap_bytes: int = 25 << 20, L=None) -> list[int]:

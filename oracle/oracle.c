@@ -310,3 +310,39 @@ int oracle_bucket_all_reduce_accumulated(int P, int ntensors, void *const *ptrs,
     }
     return OR_OK;
 }
+
+/*
+ * Sharded SGD step, ZeRO stage 1 ("Distributed Training", "Sharded data
+ * parallelism: ZeRO and FSDP": the optimizer state is partitioned across the
+ * ranks and each rank updates only its partition; the updated parameters
+ * then go to all ranks -- ZeroRedundancyOptimizer broadcasts them, FSDP
+ * all-gathers the shards).  With s = n / P, rank r owns elements
+ * [r*s, (r+1)*s) and holds that part of the fp32 master weights and
+ * momentum in w_shard[r], v_shard[r] (s elements each).  Three steps:
+ *   1. reduce-scatter: rank r's part of the reduced gradient, g (fp32,
+ *      before any rounding) = reduce(grads[.][r*s + j]);
+ *   2. the owner's SGD step on its shard: v = fl(fl(mu*v) + g),
+ *      w = fl(w - fl(lr*v));
+ *   3. all-gather: every rank's params[q][r*s + j] = w, rounded to dtype.
+ */
+int oracle_sharded_sgd_step(int P, const void *const *grads, void *const *params,
+                            float *const *w_shard, float *const *v_shard, size_t n, int dtype,
+                            int op, float lr, float momentum)
+{
+    if (bad_args(P, dtype, op) || n % (size_t)P != 0)
+        return OR_BAD;
+    size_t s = n / (size_t)P;
+    for (int r = 0; r < P; ++r)
+        for (size_t j = 0; j < s; ++j) {
+            size_t i = (size_t)r * s + j;
+            float g = reduce_one(P, grads, i, dtype, op);
+            float *v = v_shard[r], *w = w_shard[r];
+            float mv = momentum * v[j];
+            v[j] = mv + g;
+            float step = lr * v[j];
+            w[j] = w[j] - step;
+            for (int q = 0; q < P; ++q)
+                store(params[q], i, dtype, w[j]);
+        }
+    return OR_OK;
+}

@@ -439,6 +439,62 @@ def pin_accumulation_with_sgd(L):
             assert np.array_equal(bits(out[0][0]), bits(want)), (wb, step)
 
 
+# ------------------------------------------------------- ZeRO-1 step
+
+def pin_sharded_step_equals_replicated_step(L):
+    """Sharding the optimizer state changes no number: the shards of w and v
+    after the sharded step, laid end to end, equal w and v after the
+    replicated step (every rank updating all of w), and every rank's params
+    equal the rounded w (torch's cast for bf16)."""
+    rng = np.random.default_rng(14)
+    for P in (1, 2, 4, 8):
+        for dt in ("f32", "bf16"):
+            n = 24 * P
+            s = n // P
+            g32 = [f32(rng.normal(0, 1e-3, n)) for _ in range(P)]
+            grads = g32 if dt == "f32" else [(x.view(np.uint32) >> 16).astype(np.uint16)
+                                              for x in g32]
+            w0 = f32(rng.normal(0, 0.02, n))
+            v0 = f32(rng.normal(0, 1e-3, n))
+            ws = [w0[r * s:(r + 1) * s].copy() for r in range(P)]
+            vs = [v0[r * s:(r + 1) * s].copy() for r in range(P)]
+            params = [np.zeros(n, grads[0].dtype) for _ in range(P)]
+            oracle.sharded_sgd_step(grads, params, ws, vs, 0.1, 0.9, op=MEAN, L=L)
+            wf, vf = [w0.copy()], [v0.copy()]
+            oracle.bucket_all_reduce([[x.copy() for x in grads]], op=MEAN,
+                                     sgd=(0.1, 0.9, wf, vf, 0), L=L)
+            assert np.array_equal(bits(np.concatenate(ws)), bits(wf[0])), (P, dt)
+            assert np.array_equal(bits(np.concatenate(vs)), bits(vf[0])), (P, dt)
+            want = wf[0] if dt == "f32" else _torch_bf16_bits(wf[0])
+            for q in range(P):
+                assert np.array_equal(bits(params[q]), bits(want)), (P, dt, q)
+
+
+def pin_sharded_step_is_rs_sgd_ag(L):
+    """For fp32 gradients the step is its three collectives in a row:
+    reduce-scatter, the owner's SGD on its shard (NumPy float32, separate
+    roundings), all-gather of the updated shards."""
+    rng = np.random.default_rng(15)
+    P, n = 4, 64
+    s = n // P
+    grads = [f32(rng.normal(0, 1, n)) for _ in range(P)]
+    w0 = [f32(rng.normal(0, 0.02, s)) for _ in range(P)]
+    ws = [x.copy() for x in w0]
+    vs = [np.zeros(s, np.float32) for _ in range(P)]
+    params = [np.zeros(n, np.float32) for _ in range(P)]
+    oracle.sharded_sgd_step(grads, params, ws, vs, 0.1, 0.9, op=SUM, L=L)
+    shards = oracle.reduce_scatter(grads, op=SUM, L=L)
+    new = []
+    for r in range(P):
+        v = np.add(np.multiply(np.float32(0.9), np.zeros(s, np.float32)), shards[r],
+                   dtype=np.float32)
+        new.append(np.subtract(w0[r], np.multiply(np.float32(0.1), v), dtype=np.float32))
+        assert np.array_equal(bits(vs[r]), bits(v)), r
+    gathered = oracle.all_gather(new, L=L)
+    for q in range(P):
+        assert np.array_equal(bits(params[q]), bits(gathered[q])), q
+
+
 ALL_PINS = [
     pin_sum_integers_exact, pin_mean_rational_exact, pin_rank_order, pin_signed_zero,
     pin_matches_numpy_f32, pin_bf16_round_matches_torch, pin_bf16_widen_matches_torch,
@@ -447,5 +503,6 @@ ALL_PINS = [
     pin_bucket_equals_per_tensor, pin_sgd_closed_form, pin_sgd_matches_torch,
     pin_sgd_write_back_flag, pin_bucket_plan, pin_accumulation_undivided_is_m_times,
     pin_accumulation_matches_numpy, pin_accumulation_single_micro_batch_is_all_reduce,
-    pin_accumulation_with_sgd,
+    pin_accumulation_with_sgd, pin_sharded_step_equals_replicated_step,
+    pin_sharded_step_is_rs_sgd_ag,
 ]

@@ -47,6 +47,12 @@ MUTANTS = {
     "accum_final_drops_acc": ("total[r] = first ? s : a[r][i] + s;", "total[r] = s;"),
     "accum_final_scale_ignored": ("float s = scale * load(x[r], i, dtype);",
                                   "float s = load(x[r], i, dtype);"),
+    "zero1_sgd_wrong_sign": ("w[j] = w[j] - step;", "w[j] = w[j] + step;"),
+    "zero1_sgd_no_momentum": ("float mv = momentum * v[j];", "float mv = 0.0f * v[j];"),
+    "zero1_strided_owner": ("size_t i = (size_t)r * s + j;", "size_t i = j * (size_t)P + (size_t)r;"),
+    "zero1_gathers_gradient": ("store(params[q], i, dtype, w[j]);", "store(params[q], i, dtype, g);"),
+    "zero1_skips_own_rank": ("for (int q = 0; q < P; ++q)\n                store(params[q]",
+                             "for (int q = 0; q < P; ++q)\n                if (q != r) store(params[q]"),
 }
 
 
