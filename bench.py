@@ -486,6 +486,25 @@ def time_sweep(device, stream):
         del g, acc, w, v
     finally:
         gar.ar_destroy(comm)
+    # ZeRO-1 sharded step on the ViT-B/16 gradient set as one flat unit
+    # (P = 8, bf16): reduce-scatter + owner's SGD + all-gather in one pass.
+    comm = gar.ar_init(8, device.index, gar.AR_MEAN)
+    try:
+        P, n = 8, 86_567_656
+        sh = n // P
+        g = [torch.empty(n, dtype=torch.bfloat16, device=device) for _ in range(P)]
+        for r, x in enumerate(g):
+            wgpu.fill(x, "normal", 100 + r, std=1e-3)
+        params = [torch.empty(n, dtype=torch.bfloat16, device=device) for _ in range(P)]
+        ws = [torch.zeros(sh, dtype=torch.float32, device=device) for _ in range(P)]
+        vs = [torch.zeros(sh, dtype=torch.float32, device=device) for _ in range(P)]
+        t = timed(lambda: gar.ar_sharded_sgd_step(comm, g, params, ws, vs, n, gar.AR_BF16, 0.1,
+                                                  0.9, gar.AR_MEAN, stream), 10, flush_between=False)
+        out["zero1_sharded_step_vit_b16_P8_bf16"] = {
+            "us": t * 1e6, "GBps": (4 * P * n + 16 * n) / t / 1e9}
+        del g, params, ws, vs
+    finally:
+        gar.ar_destroy(comm)
     del flush
     torch.cuda.empty_cache()
     return out

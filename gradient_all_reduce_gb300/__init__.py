@@ -72,6 +72,8 @@ def _load() -> ctypes.CDLL:
         "ar_bucket_all_reduce_accumulated": [P, ctypes.POINTER(ar_bucket_t),
                                              ctypes.POINTER(ar_accum_t), ctypes.c_int,
                                              ctypes.POINTER(ar_sgd_t), P],
+        "ar_sharded_sgd_step": [P, PP, PP, PP, PP, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
+                                ctypes.c_float, ctypes.c_float, P],
         "ar_bucket_plan": [ctypes.c_int, ctypes.POINTER(ctypes.c_size_t), ctypes.c_size_t,
                            ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)],
         "ar_get_async_error": [P],
@@ -244,6 +246,17 @@ def ar_bucket_all_reduce_accumulated(comm: int, tensors: Sequence[Sequence], num
                                                 ctypes.byref(s) if s is not None else None,
                                                 _stream(stream)),
         "ar_bucket_all_reduce_accumulated")
+
+
+def ar_sharded_sgd_step(comm: int, grads: Sequence, params: Sequence, master_shards: Sequence,
+                        momentum_shards: Sequence, count: int, dtype: int, lr: float,
+                        momentum: float, op: int = AR_OP_DEFAULT, stream=None) -> None:
+    """ZeRO-1 step: reduce-scatter, each owner's SGD on its fp32 shard, and
+    all-gather of the updated weights into every params replica, in one pass."""
+    _ok(load().ar_sharded_sgd_step(comm, _ptr_array(grads), _ptr_array(params),
+                                   _ptr_array(master_shards), _ptr_array(momentum_shards),
+                                   int(count), int(dtype), int(op), float(lr), float(momentum),
+                                   _stream(stream)), "ar_sharded_sgd_step")
 
 
 def ar_bucket_plan(nbytes: Sequence[int], cap_bytes: int = 25 << 20) -> list[int]:

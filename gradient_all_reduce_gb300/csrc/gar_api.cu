@@ -541,6 +541,74 @@ ar_status_t ar_bucket_all_reduce_accumulated(ar_comm_t comm, const ar_bucket_t* 
   return AR_OK;
 }
 
+ar_status_t ar_sharded_sgd_step(ar_comm_t comm, const void* const* grads, void* const* params,
+                                float* const* master_shards, float* const* momentum_shards,
+                                size_t count, ar_dtype_t dtype, ar_op_t op, float lr,
+                                float momentum, ar_stream_t stream) {
+  ar_status_t st = check_call(comm, dtype);
+  if (st != AR_OK) return st;
+  ar_op_t rop;
+  if (!resolve_op(comm, op, &rop) || grads == nullptr || params == nullptr ||
+      master_shards == nullptr || momentum_shards == nullptr)
+    return AR_ERR_INVALID_ARG;
+  const int P = comm->nranks;
+  if (count % size_t(P) != 0) return AR_ERR_INVALID_ARG;
+  const size_t es = elem_bytes(dtype), shard = count / size_t(P);
+  size_t bytes;
+  if (!mul_ok(count, es, &bytes)) return AR_ERR_INVALID_ARG;
+  if (count == 0) return AR_OK;
+  const size_t sbytes = shard * 4;
+  DeviceGuard guard(comm->device);
+  if (!guard.ok()) return AR_ERR_CUDA;
+  // grads / params: in place (params[r] == grads[r]) or disjoint; shards:
+  // fp32, disjoint from everything.
+  struct Range { uintptr_t lo, hi; };
+  std::vector<Range> ranges;
+  for (int r = 0; r < P; ++r) {
+    const void* g = grads[r];
+    void* p = params[r];
+    const float* w = master_shards[r];
+    const float* v = momentum_shards[r];
+    if (g == nullptr || p == nullptr || w == nullptr || v == nullptr) return AR_ERR_INVALID_ARG;
+    if (!aligned(g, es) || !aligned(p, es) || !aligned(w, 4) || !aligned(v, 4))
+      return AR_ERR_INVALID_ARG;
+    if (!pointer_ok(comm, g, bytes) || !pointer_ok(comm, p, bytes) ||
+        !pointer_ok(comm, w, sbytes) || !pointer_ok(comm, v, sbytes))
+      return AR_ERR_INVALID_ARG;
+    ranges.push_back({addr(g), addr(g) + bytes});
+    if (p != g) ranges.push_back({addr(p), addr(p) + bytes});
+    if (sbytes) {
+      ranges.push_back({addr(w), addr(w) + sbytes});
+      ranges.push_back({addr(v), addr(v) + sbytes});
+    }
+  }
+  std::sort(ranges.begin(), ranges.end(), [](const Range& x, const Range& y) { return x.lo < y.lo; });
+  for (size_t k = 1; k < ranges.size(); ++k)
+    if (ranges[k].lo < ranges[k - 1].hi) return AR_ERR_INVALID_ARG;
+
+  // One segment per shard r: the P replicas' part r of the gradient in, the
+  // P replicas' part r of the parameters out, shard r's w and v.
+  SegTable<CapSmall> t;
+  init_table(t, P, P, 2 * P, P, rop == AR_MEAN);
+  t.lr = lr;
+  t.mu = momentum;
+  t.write_back = 1;
+  t.store_w = 1;
+  const uint64_t tile = gar::reduce_tile(P, int(es), false, true);
+  for (int r = 0; r < P; ++r) {
+    void* ptrs[2 * AR_MAX_RANKS];
+    for (int q = 0; q < P; ++q) {
+      ptrs[q] = static_cast<char*>(const_cast<void*>(grads[q])) + size_t(r) * shard * es;
+      ptrs[P + q] = static_cast<char*>(params[q]) + size_t(r) * shard * es;
+    }
+    float* extra[2] = {master_shards[r], momentum_shards[r]};
+    if (!add_segment(t, ptrs, shard, tile, vec_flag(ptrs, 2 * P, extra, 2), master_shards[r],
+                     momentum_shards[r]))
+      return AR_ERR_INVALID_ARG;
+  }
+  return run_reduce(comm, dtype, true, t, static_cast<cudaStream_t>(stream));
+}
+
 ar_status_t ar_bucket_plan(int ntensors, const size_t* nbytes, size_t cap_bytes, int* bucket_of,
                            int* nbuckets) {
   if (ntensors < 0 || cap_bytes == 0 || nbuckets == nullptr) return AR_ERR_INVALID_ARG;

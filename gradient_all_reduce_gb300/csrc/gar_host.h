@@ -156,6 +156,9 @@ void init_table(SegTable<Cap>& t, int np, int ndst, int stride, int dst_off, boo
   t.dst_off = dst_off;
   t.mean = mean ? 1 : 0;
   t.write_back = 1;
+  t.store_w = 0;
+  t.scale = 1.f;
+  t.first = 0;
   t.lr = 0.f;
   t.mu = 0.f;
   t.tile0[0] = 0;

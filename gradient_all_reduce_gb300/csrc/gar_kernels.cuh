@@ -55,6 +55,7 @@ struct SegTable {
   int dst_off;                // index of the first destination within a segment
   int mean;                   // divide by P
   int write_back;             // SGD: also store the reduced gradient
+  int store_w;                // SGD: store the updated weights (rounded) instead
   float lr, mu;               // SGD hyper-parameters
   float scale;                // accumulation: factor on each micro-batch gradient
   int first;                  // accumulation: 1 = overwrite the accumulators
@@ -172,7 +173,18 @@ __global__ void __launch_bounds__(kThreads)
         if (vi < nvec) {
           float g[E];
           reduce_vec<D, PT>(in[u], np, mean, g);
-          if constexpr (SGD) sgd_vec<D>(g, w4[u], v4[u], w, v, vi * E, a.lr, a.mu);
+          if constexpr (SGD) {
+            sgd_vec<D>(g, w4[u], v4[u], w, v, vi * E, a.lr, a.mu);
+            if (a.store_w) {  // the sharded step: every rank gets the new weights
+#pragma unroll
+              for (int q = 0; q < WV; ++q) {
+                g[4 * q] = w4[u][q].x;
+                g[4 * q + 1] = w4[u][q].y;
+                g[4 * q + 2] = w4[u][q].z;
+                g[4 * q + 3] = w4[u][q].w;
+              }
+            }
+          }
           if (do_store) {
             const uint4 out = D::pack(g);
             for (int d = 0; d < a.ndst; ++d) st_stream(static_cast<uint4*>(dst[d]) + vi, out);
@@ -184,7 +196,10 @@ __global__ void __launch_bounds__(kThreads)
         const uint64_t i = nvec * E + threadIdx.x;
         if (i < n) {
           float g = reduce_scalar<D, PT>(seg, i, np, mean);
-          if constexpr (SGD) sgd_step(g, a.lr, a.mu, w[i], v[i]);
+          if constexpr (SGD) {
+            sgd_step(g, a.lr, a.mu, w[i], v[i]);
+            if (a.store_w) g = w[i];
+          }
           if (do_store)
             for (int d = 0; d < a.ndst; ++d) D::store1(dst[d], i, g);
         }
@@ -196,7 +211,10 @@ __global__ void __launch_bounds__(kThreads)
         const uint64_t i = e0 + k;
         if (i >= n) break;
         float g = reduce_scalar<D, PT>(seg, i, np, mean);
-        if constexpr (SGD) sgd_step(g, a.lr, a.mu, w[i], v[i]);
+        if constexpr (SGD) {
+          sgd_step(g, a.lr, a.mu, w[i], v[i]);
+          if (a.store_w) g = w[i];
+        }
         if (do_store)
           for (int d = 0; d < a.ndst; ++d) D::store1(dst[d], i, g);
       }

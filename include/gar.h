@@ -224,6 +224,26 @@ ar_status_t ar_bucket_all_reduce_accumulated(ar_comm_t comm, const ar_bucket_t *
                                              const ar_sgd_t *sgd, ar_stream_t stream);
 
 /*
+ * Sharded SGD step, ZeRO stage 1 ("Distributed Training", "Sharded data
+ * parallelism: ZeRO and FSDP": the optimizer state is partitioned over the
+ * ranks, each rank updates only its partition, and the updated parameters
+ * go to every rank).  count % P == 0, s = count / P.  grads[r], params[r]:
+ * count elements of dtype; master_shards[r], momentum_shards[r]: rank r's
+ * s fp32 elements of the master weights and momentum, for elements
+ * [r*s, (r+1)*s).  One fused pass does the three collectives of the step:
+ * reduce-scatter of the gradients (g in fp32, before any rounding, reduced
+ * as by ar_all_reduce), the owner's SGD step on its shard
+ * (v = fl(fl(momentum*v) + g), w = fl(w - fl(lr*v))), and the all-gather
+ * of the updated weights, rounded to dtype, into every params[q].
+ * params[r] == grads[r] is in place; otherwise params and grads are
+ * disjoint.  The shards are disjoint from everything.
+ */
+ar_status_t ar_sharded_sgd_step(ar_comm_t comm, const void *const *grads, void *const *params,
+                                float *const *master_shards, float *const *momentum_shards,
+                                size_t count, ar_dtype_t dtype, ar_op_t op, float lr,
+                                float momentum, ar_stream_t stream);
+
+/*
  * Bucket assignment, host only.  nbytes[t] is tensor t's size in
  * registration order.  Tensors are taken from the last to the first and
  * added to the open bucket; one that would take a non-empty bucket past
