@@ -488,9 +488,12 @@ def time_sweep(device, stream):
         gar.ar_destroy(comm)
     # ZeRO-1 sharded step on the ViT-B/16 gradient set as one flat unit
     # (P = 8, bf16): reduce-scatter + owner's SGD + all-gather in one pass.
+    # The unit is padded (86,567,656 -> 86,567,680) so each rank's shard is a
+    # whole number of 16-byte vectors.
     comm = gar.ar_init(8, device.index, gar.AR_MEAN)
     try:
-        P, n = 8, 86_567_656
+        P = 8
+        n = -(-86_567_656 // (P * 8)) * (P * 8)
         sh = n // P
         g = [torch.empty(n, dtype=torch.bfloat16, device=device) for _ in range(P)]
         for r, x in enumerate(g):

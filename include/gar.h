@@ -236,7 +236,10 @@ ar_status_t ar_bucket_all_reduce_accumulated(ar_comm_t comm, const ar_bucket_t *
  * (v = fl(fl(momentum*v) + g), w = fl(w - fl(lr*v))), and the all-gather
  * of the updated weights, rounded to dtype, into every params[q].
  * params[r] == grads[r] is in place; otherwise params and grads are
- * disjoint.  The shards are disjoint from everything.
+ * disjoint.  The shards are disjoint from everything.  The vectorised path
+ * needs every shard to start on a 16-byte boundary: pad the flat unit so
+ * that s * sizeof(dtype) is a multiple of 16 (other sizes run the scalar
+ * path, with the same results).
  */
 ar_status_t ar_sharded_sgd_step(ar_comm_t comm, const void *const *grads, void *const *params,
                                 float *const *master_shards, float *const *momentum_shards,
