@@ -29,6 +29,7 @@ LIB = HERE / "liboracle.so"
 F32, BF16 = 0, 1
 SUM, MEAN = 0, 1
 CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+LDFLAGS = ["-lm"]
 
 
 def _stamp(src: Path) -> str:
@@ -42,7 +43,7 @@ def build(src: Path = SRC, out: Path = LIB) -> Path:
     if out.exists() and stamp.exists() and stamp.read_text() == want:
         return out
     tmp = out.with_name(out.name + f".{os.getpid()}.tmp")
-    subprocess.run(["gcc", *CFLAGS, "-o", str(tmp), str(src)], check=True)
+    subprocess.run(["gcc", *CFLAGS, "-o", str(tmp), str(src), *LDFLAGS], check=True)
     os.replace(tmp, out)
     stamp.write_text(want)
     return out
@@ -76,6 +77,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
         ctypes.c_int, ctypes.c_int, _c_ptrs, ctypes.POINTER(ctypes.c_uint64), ctypes.c_int,
         ctypes.c_int, _c_ptrs, ctypes.c_float, ctypes.c_int, ctypes.c_float, ctypes.c_float,
         _c_ptrs, _c_ptrs, ctypes.c_int]
+    lib.oracle_syncbn_stats.argtypes = [ctypes.c_int, _c_ptrs, _c_ptrs,
+                                        ctypes.POINTER(ctypes.c_uint64), _c_ptrs, _c_ptrs,
+                                        ctypes.c_size_t, ctypes.c_float]
+    lib.oracle_syncbn_stats.restype = ctypes.c_int
     lib.oracle_sharded_sgd_step.argtypes = [
         ctypes.c_int, _c_ptrs, _c_ptrs, _c_ptrs, _c_ptrs, ctypes.c_size_t, ctypes.c_int,
         ctypes.c_int, ctypes.c_float, ctypes.c_float]
@@ -231,6 +236,19 @@ def sharded_sgd_step(grads, params, w_shards, v_shards, lr: float, momentum: flo
     _check(L.oracle_sharded_sgd_step(P, _ptrs(grads), _ptrs(params), _ptrs(w_shards),
                                      _ptrs(v_shards), n, _dtype_code(grads[0]), op, lr,
                                      momentum), "sharded_sgd_step")
+
+
+def syncbn_stats(sums, sqsums, counts, eps: float = 1e-5, L=None):
+    """Pooled batch-norm statistics: every rank's (mean, invstd) per channel
+    from the ranks' per-channel fp32 sums, sums of squares and counts."""
+    L = L or lib()
+    P, C = len(sums), sums[0].size
+    mean = [np.empty(C, np.float32) for _ in range(P)]
+    invstd = [np.empty(C, np.float32) for _ in range(P)]
+    cnt = (ctypes.c_uint64 * P)(*[int(c) for c in counts])
+    _check(L.oracle_syncbn_stats(P, _ptrs(sums), _ptrs(sqsums), cnt, _ptrs(mean), _ptrs(invstd), C,
+                                 eps), "syncbn_stats")
+    return mean, invstd
 
 
 def bucket_plan(nbytes, cap_bytes: int = 25 << 20, L=None) -> list[int]:

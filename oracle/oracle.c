@@ -46,6 +46,7 @@
  * fp32 arithmetic is IEEE binary32 with round-to-nearest-even; no FMA
  * contraction, no flush-to-zero.
  */
+#include <math.h>
 #include <stddef.h>
 #include <stdint.h>
 #include <string.h>
@@ -344,5 +345,48 @@ int oracle_sharded_sgd_step(int P, const void *const *grads, void *const *params
             for (int q = 0; q < P; ++q)
                 store(params[q], i, dtype, w[j]);
         }
+    return OR_OK;
+}
+
+/*
+ * Synchronized batch-normalization statistics ("Distributed Training",
+ * "Synchronized batch normalization": the per-shard statistics are pooled
+ * over the ranks so every rank normalizes with the statistics of the whole
+ * batch; the example pools the per-shard sums and sums of squares with an
+ * all-reduce, mean = s1 / n, var = s2 / n - mean^2, the biased variance of
+ * training mode, and normalizes with sqrt(var + eps)).
+ * sum[r][c], sqsum[r][c]: rank r's fp32 sums of x and x*x over its values of
+ * channel c; count[r]: rank r's number of values per channel.  In fp64,
+ * ranks added in order 0..P-1:
+ *     n = count[0] + ... + count[P-1],  s1 = sum[0][c] + ... , s2 = ...,
+ *     mean = s1 / n,  var = s2 / n - mean * mean,  invstd = 1 / sqrt(var + eps);
+ * every rank receives mean and invstd rounded to fp32.
+ */
+int oracle_syncbn_stats(int P, const float *const *sum, const float *const *sqsum,
+                        const uint64_t *count, float *const *mean, float *const *invstd,
+                        size_t channels, float eps)
+{
+    if (P < 1)
+        return OR_BAD;
+    uint64_t n_total = 0;
+    for (int r = 0; r < P; ++r)
+        n_total += count[r];
+    if (n_total == 0)
+        return OR_BAD;
+    double n = (double)n_total;
+    for (size_t c = 0; c < channels; ++c) {
+        double s1 = (double)sum[0][c], s2 = (double)sqsum[0][c];
+        for (int r = 1; r < P; ++r) {
+            s1 = s1 + (double)sum[r][c];
+            s2 = s2 + (double)sqsum[r][c];
+        }
+        double m = s1 / n;
+        double var = s2 / n - m * m;
+        double is = 1.0 / sqrt(var + (double)eps);
+        for (int r = 0; r < P; ++r) {
+            mean[r][c] = (float)m;
+            invstd[r][c] = (float)is;
+        }
+    }
     return OR_OK;
 }

@@ -495,6 +495,54 @@ def pin_sharded_step_is_rs_sgd_ag(L):
         assert np.array_equal(bits(params[q]), bits(gathered[q])), q
 
 
+# ------------------------------------------------- SyncBN statistics
+
+def _shard_stats(xs):
+    """Per-channel fp32 sums of x and x*x and the count, for shards of shape
+    (N_r, C, H, W) holding integer values (exact in fp32)."""
+    sums = [f32(x.sum(axis=(0, 2, 3))) for x in xs]
+    sq = [f32((x * x).sum(axis=(0, 2, 3))) for x in xs]
+    counts = [x.shape[0] * x.shape[2] * x.shape[3] for x in xs]
+    return sums, sq, counts
+
+
+def pin_syncbn_equals_whole_batch(L):
+    """The page's check: statistics pooled from the shards' sums equal batch
+    normalization's statistics on the whole batch (torch's own batch_norm in
+    fp64, training mode, biased variance) -- here to within one fp32 rounding
+    of the exact values, with uneven shards."""
+    import torch
+    rng = np.random.default_rng(16)
+    C = 8
+    xs = [rng.integers(-20, 20, (n, C, 3, 2)).astype(np.float64) for n in (3, 5, 1, 7)]
+    sums, sq, counts = _shard_stats(xs)
+    mean, invstd = oracle.syncbn_stats(sums, sq, counts, eps=1e-5, L=L)
+    whole = torch.from_numpy(np.concatenate(xs))
+    m = whole.mean(dim=(0, 2, 3)).numpy()
+    v = whole.var(dim=(0, 2, 3), unbiased=False).numpy()
+    want_is = 1.0 / np.sqrt(v + np.float64(np.float32(1e-5)))
+    for r in range(len(xs)):
+        assert np.all(np.abs(mean[r].astype(np.float64) - m) <= np.spacing(np.abs(f32(m)))), r
+        assert np.all(np.abs(invstd[r].astype(np.float64) - want_is)
+                      <= np.spacing(f32(want_is))), r
+    # normalizing the whole batch with the pooled statistics matches batch_norm
+    bn = torch.nn.functional.batch_norm(whole, None, None, training=True,
+                                        eps=float(np.float32(1e-5))).numpy()
+    mine = (np.concatenate(xs) - mean[0].astype(np.float64)[None, :, None, None]) * \
+        invstd[0].astype(np.float64)[None, :, None, None]
+    assert np.max(np.abs(mine - bn)) <= 1e-5
+
+
+def pin_syncbn_exact_sums(L):
+    """Hand case: two ranks, one channel, values {1, 3} and {5, 7}: n = 4,
+    mean = 4, var = (1 + 9 + 25 + 49) / 4 - 16 = 5, invstd = 1/sqrt(5 + eps)."""
+    sums = [f32([4.0]), f32([12.0])]
+    sq = [f32([10.0]), f32([74.0])]
+    mean, invstd = oracle.syncbn_stats(sums, sq, [2, 2], eps=0.0, L=L)
+    assert mean[0][0] == 4.0 and mean[1][0] == 4.0
+    assert invstd[1][0] == np.float32(1.0 / np.sqrt(5.0))
+
+
 ALL_PINS = [
     pin_sum_integers_exact, pin_mean_rational_exact, pin_rank_order, pin_signed_zero,
     pin_matches_numpy_f32, pin_bf16_round_matches_torch, pin_bf16_widen_matches_torch,
@@ -504,5 +552,5 @@ ALL_PINS = [
     pin_sgd_write_back_flag, pin_bucket_plan, pin_accumulation_undivided_is_m_times,
     pin_accumulation_matches_numpy, pin_accumulation_single_micro_batch_is_all_reduce,
     pin_accumulation_with_sgd, pin_sharded_step_equals_replicated_step,
-    pin_sharded_step_is_rs_sgd_ag,
+    pin_sharded_step_is_rs_sgd_ag, pin_syncbn_equals_whole_batch, pin_syncbn_exact_sums,
 ]

@@ -47,6 +47,11 @@ MUTANTS = {
     "accum_final_drops_acc": ("total[r] = first ? s : a[r][i] + s;", "total[r] = s;"),
     "accum_final_scale_ignored": ("float s = scale * load(x[r], i, dtype);",
                                   "float s = load(x[r], i, dtype);"),
+    "syncbn_var_no_mean_sq": ("double var = s2 / n - m * m;", "double var = s2 / n;"),
+    "syncbn_eps_outside": ("double is = 1.0 / sqrt(var + (double)eps);",
+                           "double is = 1.0 / sqrt(var) + (double)eps;"),
+    "syncbn_rank0_count": ("n_total += count[r];", "n_total = count[r];"),
+    "syncbn_drops_rank": ("s1 = s1 + (double)sum[r][c];", "s1 = s1 + 0.0 * (double)sum[r][c];"),
     "zero1_sgd_wrong_sign": ("w[j] = w[j] - step;", "w[j] = w[j] + step;"),
     "zero1_sgd_no_momentum": ("float mv = momentum * v[j];", "float mv = 0.0f * v[j];"),
     "zero1_strided_owner": ("size_t i = (size_t)r * s + j;", "size_t i = j * (size_t)P + (size_t)r;"),
