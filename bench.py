@@ -508,6 +508,35 @@ def time_sweep(device, stream):
         del g, params, ws, vs
     finally:
         gar.ar_destroy(comm)
+    # Synchronized batch-norm statistics (P = 8): latency of one call through
+    # the API, and of the same call replayed from a CUDA graph.
+    comm = gar.ar_init(8, device.index, gar.AR_SUM)
+    try:
+        res = []
+        for C in (64, 512, 2048):
+            P = 8
+            sums = [torch.rand(C, device=device) for _ in range(P)]
+            sq = [torch.rand(C, device=device) + 1 for _ in range(P)]
+            means = [torch.empty(C, device=device) for _ in range(P)]
+            invs = [torch.empty(C, device=device) for _ in range(P)]
+
+            def call(s=None):
+                gar.ar_syncbn_stats(comm, sums, sq, [1000] * P, means, invs, C, 1e-5,
+                                    stream if s is None else s)
+            t_api = timed(call, 200, flush_between=False)
+            side = torch.cuda.Stream(device)
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                call(side)
+            torch.cuda.synchronize(device)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                call(torch.cuda.current_stream())
+            t_graph = timed(graph.replay, 200, flush_between=False)
+            res.append({"P": P, "channels": C, "api_us": t_api * 1e6, "graph_us": t_graph * 1e6})
+        out["syncbn_stats_latency"] = res
+    finally:
+        gar.ar_destroy(comm)
     del flush
     torch.cuda.empty_cache()
     return out

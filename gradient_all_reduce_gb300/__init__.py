@@ -74,6 +74,8 @@ def _load() -> ctypes.CDLL:
                                              ctypes.POINTER(ar_sgd_t), P],
         "ar_sharded_sgd_step": [P, PP, PP, PP, PP, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
                                 ctypes.c_float, ctypes.c_float, P],
+        "ar_syncbn_stats": [P, PP, PP, ctypes.POINTER(ctypes.c_uint64), PP, PP, ctypes.c_size_t,
+                            ctypes.c_float, P],
         "ar_bucket_plan": [ctypes.c_int, ctypes.POINTER(ctypes.c_size_t), ctypes.c_size_t,
                            ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)],
         "ar_get_async_error": [P],
@@ -257,6 +259,17 @@ def ar_sharded_sgd_step(comm: int, grads: Sequence, params: Sequence, master_sha
                                    _ptr_array(master_shards), _ptr_array(momentum_shards),
                                    int(count), int(dtype), int(op), float(lr), float(momentum),
                                    _stream(stream)), "ar_sharded_sgd_step")
+
+
+def ar_syncbn_stats(comm: int, sums: Sequence, sqsums: Sequence, counts: Sequence[int],
+                    means: Sequence, invstds: Sequence, channels: int, eps: float = 1e-5,
+                    stream=None) -> None:
+    """Pooled batch-norm statistics for every rank from the ranks'
+    per-channel sums, sums of squares and value counts."""
+    cnt = (ctypes.c_uint64 * max(len(counts), 1))(*[int(c) for c in counts])
+    _ok(load().ar_syncbn_stats(comm, _ptr_array(sums), _ptr_array(sqsums), cnt, _ptr_array(means),
+                               _ptr_array(invstds), int(channels), float(eps), _stream(stream)),
+        "ar_syncbn_stats")
 
 
 def ar_bucket_plan(nbytes: Sequence[int], cap_bytes: int = 25 << 20) -> list[int]:

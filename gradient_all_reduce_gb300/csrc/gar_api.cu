@@ -609,6 +609,58 @@ ar_status_t ar_sharded_sgd_step(ar_comm_t comm, const void* const* grads, void* 
   return run_reduce(comm, dtype, true, t, static_cast<cudaStream_t>(stream));
 }
 
+ar_status_t ar_syncbn_stats(ar_comm_t comm, const float* const* sum, const float* const* sqsum,
+                            const uint64_t* count, float* const* mean, float* const* invstd,
+                            size_t channels, float eps, ar_stream_t stream) {
+  if (!is_live(comm)) return AR_ERR_STATE;
+  if (sum == nullptr || sqsum == nullptr || count == nullptr || mean == nullptr ||
+      invstd == nullptr)
+    return AR_ERR_INVALID_ARG;
+  const int P = comm->nranks;
+  uint64_t n = 0;
+  for (int r = 0; r < P; ++r) {
+    if (count[r] > (uint64_t(1) << 53) - n) return AR_ERR_INVALID_ARG;  // n stays exact in fp64
+    n += count[r];
+  }
+  if (n == 0) return AR_ERR_INVALID_ARG;
+  if (channels == 0) return AR_OK;
+  size_t bytes;
+  if (!mul_ok(channels, 4, &bytes)) return AR_ERR_INVALID_ARG;
+  DeviceGuard guard(comm->device);
+  if (!guard.ok()) return AR_ERR_CUDA;
+  struct Range { uintptr_t lo, hi; };
+  std::vector<Range> outs;
+  for (int r = 0; r < P; ++r) {
+    const void* ps[4] = {sum[r], sqsum[r], mean[r], invstd[r]};
+    for (const void* p : ps)
+      if (p == nullptr || !aligned(p, 4) || !pointer_ok(comm, p, bytes)) return AR_ERR_INVALID_ARG;
+    outs.push_back({addr(mean[r]), addr(mean[r]) + bytes});
+    outs.push_back({addr(invstd[r]), addr(invstd[r]) + bytes});
+  }
+  std::sort(outs.begin(), outs.end(), [](const Range& x, const Range& y) { return x.lo < y.lo; });
+  for (size_t k = 1; k < outs.size(); ++k)
+    if (outs[k].lo < outs[k - 1].hi) return AR_ERR_INVALID_ARG;
+  for (const Range& o : outs)
+    for (int r = 0; r < P; ++r)
+      if (overlap(reinterpret_cast<const void*>(o.lo), bytes, sum[r], bytes) ||
+          overlap(reinterpret_cast<const void*>(o.lo), bytes, sqsum[r], bytes))
+        return AR_ERR_INVALID_ARG;
+  gar::SyncBnArgs a{};
+  for (int r = 0; r < P; ++r) {
+    a.sum[r] = sum[r];
+    a.sqsum[r] = sqsum[r];
+    a.mean[r] = mean[r];
+    a.invstd[r] = invstd[r];
+  }
+  a.n = double(n);
+  a.eps = double(eps);
+  a.channels = channels;
+  a.np = P;
+  const gar::LaunchCtx ctx{comm->device, comm->num_sms, static_cast<cudaStream_t>(stream), false,
+                           comm->pdl};
+  return from_cuda(gar::launch_syncbn_stats(ctx, a));
+}
+
 ar_status_t ar_bucket_plan(int ntensors, const size_t* nbytes, size_t cap_bytes, int* bucket_of,
                            int* nbuckets) {
   if (ntensors < 0 || cap_bytes == 0 || nbuckets == nullptr) return AR_ERR_INVALID_ARG;

@@ -48,6 +48,38 @@ cudaError_t launch_wait_selftest(cudaStream_t stream, uint32_t* status, uint64_t
   return cudaGetLastError();
 }
 
+// Synchronized batch-norm statistics: one thread per channel pools the
+// ranks' per-channel sums in fp64 (rank order), forms mean, biased
+// variance and invstd with IEEE-rounded fp64 operations, and writes both,
+// rounded to fp32, for every rank.
+__global__ void __launch_bounds__(128) k_syncbn_stats(const __grid_constant__ SyncBnArgs a) {
+  griddep_launch_dependents();
+  griddep_wait();
+  const uint64_t stride = uint64_t(gridDim.x) * blockDim.x;
+  for (uint64_t c = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; c < a.channels; c += stride) {
+    double s1 = double(a.sum[0][c]), s2 = double(a.sqsum[0][c]);
+    for (int r = 1; r < a.np; ++r) {
+      s1 = __dadd_rn(s1, double(a.sum[r][c]));
+      s2 = __dadd_rn(s2, double(a.sqsum[r][c]));
+    }
+    const double m = __ddiv_rn(s1, a.n);
+    const double var = __dsub_rn(__ddiv_rn(s2, a.n), __dmul_rn(m, m));
+    const double is = __ddiv_rn(1.0, __dsqrt_rn(__dadd_rn(var, a.eps)));
+    const float mf = __double2float_rn(m), isf = __double2float_rn(is);
+    for (int r = 0; r < a.np; ++r) {
+      a.mean[r][c] = mf;
+      a.invstd[r][c] = isf;
+    }
+  }
+}
+
+cudaError_t launch_syncbn_stats(const LaunchCtx& ctx, const SyncBnArgs& args) {
+  const uint64_t blocks = (args.channels + 127) / 128;
+  const unsigned grid = unsigned(blocks < uint64_t(ctx.num_sms) * 8 ? blocks : uint64_t(ctx.num_sms) * 8);
+  if (grid == 0) return cudaSuccess;
+  return launch_ex(ctx, &k_syncbn_stats, grid, 128, 0, args);
+}
+
 template cudaError_t launch_copy<CapSmall>(const LaunchCtx&, const SegTable<CapSmall>&);
 template cudaError_t launch_copy<CapLarge>(const LaunchCtx&, const SegTable<CapLarge>&);
 

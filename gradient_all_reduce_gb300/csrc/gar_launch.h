@@ -71,6 +71,19 @@ cudaError_t launch_reduce_acc_bf16(const LaunchCtx& ctx, bool sgd, const SegTabl
 template <class Cap>
 cudaError_t launch_copy(const LaunchCtx& ctx, const SegTable<Cap>& tab);
 
+// Arguments of the synchronized batch-norm statistics kernel.
+struct SyncBnArgs {
+  const float* sum[kMaxRanks];    // rank r's per-channel sums of x
+  const float* sqsum[kMaxRanks];  // ... and of x * x
+  float* mean[kMaxRanks];         // outputs, every rank
+  float* invstd[kMaxRanks];
+  double n;                       // total values per channel over all ranks
+  double eps;
+  uint64_t channels;
+  int np;
+};
+cudaError_t launch_syncbn_stats(const LaunchCtx& ctx, const SyncBnArgs& args);
+
 // One warp runs the bounded mbarrier wait on a barrier nothing arrives at.
 cudaError_t launch_wait_selftest(cudaStream_t stream, uint32_t* status, uint64_t limit_ns);
 

@@ -247,6 +247,26 @@ ar_status_t ar_sharded_sgd_step(ar_comm_t comm, const void *const *grads, void *
                                 float momentum, ar_stream_t stream);
 
 /*
+ * Synchronized batch-normalization statistics ("Distributed Training",
+ * "Synchronized batch normalization": per-shard statistics pooled over the
+ * ranks, so every rank normalizes with the statistics of the whole batch;
+ * the page's example all-reduces the per-shard sums and sums of squares).
+ * sum[r], sqsum[r]: rank r's fp32 per-channel sums of x and of x*x over its
+ * shard (channels values each); count: HOST array of P values, rank r's
+ * number of values per channel (their total must be > 0 and <= 2^53).
+ * For every channel, in fp64 with the ranks added in order 0..P-1:
+ *   n = sum of count, s1 = sum over r of sum[r], s2 = likewise,
+ *   mean = s1 / n,  var = s2 / n - mean^2 (biased, as in training),
+ *   invstd = 1 / sqrt(var + eps);
+ * every rank's mean[r], invstd[r] (fp32, channels values) receive them.  A
+ * negative var + eps gives NaN.  Outputs must be disjoint from each other
+ * and from the inputs.  Latency-bound: one thread per channel.
+ */
+ar_status_t ar_syncbn_stats(ar_comm_t comm, const float *const *sum, const float *const *sqsum,
+                            const uint64_t *count, float *const *mean, float *const *invstd,
+                            size_t channels, float eps, ar_stream_t stream);
+
+/*
  * Bucket assignment, host only.  nbytes[t] is tensor t's size in
  * registration order.  Tensors are taken from the last to the first and
  * added to the open bucket; one that would take a non-empty bucket past

@@ -1,0 +1,71 @@
+"""GPU parity of the synchronized batch-norm statistics (ar_syncbn_stats)
+against the CPU oracle, bit for bit, and end to end against batch_norm on
+the whole batch."""
+import numpy as np
+import pytest
+import torch
+
+import gradient_all_reduce_gb300 as gar
+import oracle
+from gpucase import assert_bits_equal, dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 8, 16])
+@pytest.mark.parametrize("C", [1, 64, 2048, 5001])
+def test_syncbn_stats_equals_oracle(P, C):
+    rng = np.random.default_rng(P * 1000 + C)
+    counts = [int(c) for c in rng.integers(1, 5000, size=P)]
+    sums = [np.float32(rng.normal(0, 1, C) * c) for c in counts]
+    sq = [np.float32(np.abs(rng.normal(1, 0.5, C)) * c + s * s / c) for s, c in zip(sums, counts)]
+    d_s = [torch.from_numpy(x).to(dev()) for x in sums]
+    d_q = [torch.from_numpy(x).to(dev()) for x in sq]
+    d_m = [torch.empty(C, device=dev()) for _ in range(P)]
+    d_i = [torch.empty(C, device=dev()) for _ in range(P)]
+    comm = gar.ar_init(P, 0, gar.AR_SUM)
+    try:
+        gar.ar_syncbn_stats(comm, d_s, d_q, counts, d_m, d_i, C, 1e-5)
+        torch.cuda.synchronize()
+    finally:
+        gar.ar_destroy(comm)
+    want_m, want_i = oracle.syncbn_stats(sums, sq, counts, eps=1e-5)
+    for r in range(P):
+        assert_bits_equal(to_np(d_m[r]), want_m[r], f"mean {r}")
+        nan = np.isnan(want_i[r])
+        assert np.array_equal(nan, np.isnan(to_np(d_i[r])))
+        assert_bits_equal(to_np(d_i[r])[~nan], want_i[r][~nan], f"invstd {r}")
+
+
+def test_syncbn_end_to_end_whole_batch():
+    """Activations of 4 ranks with uneven shards (N = 3, 5, 2, 6, C = 32,
+    8x8); the per-shard sums are taken by torch on the GPU in fp32; the
+    pooled statistics equal the oracle's on the same sums bit for bit and
+    normalize the whole batch like batch_norm within fp32 round-off."""
+    P, C = 4, 32
+    g = torch.Generator(device=dev()).manual_seed(0)
+    xs = [torch.randn(n, C, 8, 8, device=dev(), generator=g) for n in (3, 5, 2, 6)]
+    sums = [x.sum(dim=(0, 2, 3)) for x in xs]
+    sq = [(x * x).sum(dim=(0, 2, 3)) for x in xs]
+    counts = [x.shape[0] * 64 for x in xs]
+    means = [torch.empty(C, device=dev()) for _ in range(P)]
+    invs = [torch.empty(C, device=dev()) for _ in range(P)]
+    comm = gar.ar_init(P, 0, gar.AR_SUM)
+    try:
+        gar.ar_syncbn_stats(comm, sums, sq, counts, means, invs, C, 1e-5)
+        torch.cuda.synchronize()
+    finally:
+        gar.ar_destroy(comm)
+    want_m, want_i = oracle.syncbn_stats([to_np(s) for s in sums], [to_np(q) for q in sq], counts)
+    assert_bits_equal(to_np(means[2]), want_m[2], "mean")
+    assert_bits_equal(to_np(invs[2]), want_i[2], "invstd")
+    whole = torch.cat(xs).double()
+    bn = torch.nn.functional.batch_norm(whole, None, None, training=True, eps=1e-5)
+    mine = (whole - means[0].double()[None, :, None, None]) * invs[0].double()[None, :, None, None]
+    assert float((mine - bn).abs().max()) <= 1e-4
