@@ -317,9 +317,9 @@ def time_e2e(args, device, stream):
     bucket's gradient replicas are copied in (one copy per replica, spread
     over four copy streams) and its tensors marked ready on the copy
     streams, so bucket b's kernel runs while bucket b+1 is still crossing
-    the host link; after finalize the updated fp32 master weights are
-    copied out.  Bytes per step: the P bf16 gradient replicas in, the
-    weights out."""
+    the host link; each bucket's updated fp32 master weights are copied out
+    as soon as its kernel is done.  Bytes per step: the P bf16 gradient
+    replicas in, the weights out."""
     import torch
     import gradient_all_reduce_gb300 as gar
     comm = gar.ar_init(P_VIT, device.index, gar.AR_MEAN)
@@ -334,13 +334,17 @@ def time_e2e(args, device, stream):
         steps = max(3, min(args.steps, 50))
         red = vs.reducer
 
+        out_stream = torch.cuda.Stream(device)
+        bucket_ids = list(range(len(spans)))
+
         def one():
             # The copies of this step overwrite the gradients only after the
             # previous step's kernels and its copy-out have finished.
             for cs in copy_streams:
                 cs.wait_stream(stream)
+            out_stream.wait_stream(stream)
             k = 0
-            for lo, hi, ts in spans:
+            for b, (lo, hi, ts) in zip(bucket_ids, spans):
                 used = []
                 for r in range(P_VIT):
                     cs = copy_streams[k % len(copy_streams)]
@@ -353,10 +357,14 @@ def time_e2e(args, device, stream):
                 # them into one, and mark the bucket's tensors on it.
                 for cs in used[1:]:
                     used[0].wait_stream(cs)
-                for t in ts:
-                    red.mark_ready(t, used[0])
+                red.mark_ready_many(ts, used[0])
+                # As soon as this bucket's kernel is done, its updated
+                # weights go back to the host while later buckets come in.
+                red.wait_bucket(b, out_stream)
+                with torch.cuda.stream(out_stream):
+                    host_w[lo:hi].copy_(vs.w[lo:hi], non_blocking=True)
             red.finalize(stream)
-            host_w.copy_(vs.w, non_blocking=True)
+            stream.wait_stream(out_stream)
 
         with torch.cuda.stream(stream):
             for _ in range(3):
@@ -373,7 +381,8 @@ def time_e2e(args, device, stream):
         return {"value": vs.step_bytes * steps / el / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": 2 * vs.n * P_VIT, "d2h_bytes_per_step": 4 * vs.n,
                 "steps": steps, "ms_per_step": el / steps * 1e3,
-                "path": "ar_reducer_* with per-bucket H2D on 4 copy streams"}
+                "path": ("ar_reducer_* with per-bucket H2D on 4 copy streams and per-bucket D2H "
+                         "of the updated weights after ar_reducer_wait_bucket")}
     finally:
         if vs is not None:
             vs.close()

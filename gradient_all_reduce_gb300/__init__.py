@@ -86,6 +86,7 @@ def _load() -> ctypes.CDLL:
         "ar_reducer_mark_ready_many": [P, ctypes.POINTER(ctypes.c_int), ctypes.c_int, P],
         "ar_reducer_finalize": [P, P],
         "ar_reducer_set_sgd": [P, ctypes.c_float, ctypes.c_float],
+        "ar_reducer_wait_bucket": [P, ctypes.c_int, P],
         "ar_reducer_info": [P, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)],
         "ar_reducer_destroy": [P],
         "ar_all_reduce_noalloc": [ctypes.c_int, PP, PP, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
@@ -356,6 +357,10 @@ class Reducer:
 
     def finalize(self, stream=None) -> None:
         _ok(load().ar_reducer_finalize(self.handle, _stream(stream)), "ar_reducer_finalize")
+
+    def wait_bucket(self, bucket: int, stream=None) -> None:
+        _ok(load().ar_reducer_wait_bucket(self.handle, int(bucket), _stream(stream)),
+            "ar_reducer_wait_bucket")
 
     def set_sgd(self, lr: float, momentum: float) -> None:
         _ok(load().ar_reducer_set_sgd(self.handle, float(lr), float(momentum)), "ar_reducer_set_sgd")

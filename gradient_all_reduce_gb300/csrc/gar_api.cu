@@ -129,6 +129,11 @@ ar_status_t ar_init(ar_comm_t* comm, int nranks, int cuda_device, ar_op_t defaul
   if (env != nullptr && std::strcmp(env, "tma") == 0) c->kernel_mode = 2;
   env = std::getenv("GAR_PDL");
   c->pdl = !(env != nullptr && std::strcmp(env, "0") == 0);
+  // All-gather and broadcast run on the bulk-store copy kernel unless
+  // GAR_COPY=ldg asks for the register-staged one (measured on GB300 within
+  // 2 % of each other; both DRAM-bound at 5.8-6.1 TB/s for 7 destinations).
+  env = std::getenv("GAR_COPY");
+  c->copy_tma = !(env != nullptr && std::strcmp(env, "ldg") == 0);
   env = std::getenv("GAR_CTAS_PER_SM");
   c->ctas_per_sm = env != nullptr ? std::atoi(env) : -1;
   if (c->ctas_per_sm < -1 || c->ctas_per_sm > 32) c->ctas_per_sm = -1;
@@ -300,6 +305,7 @@ ar_status_t ar_all_gather(ar_comm_t comm, const void* const* send, void* const* 
 
   SegTable<CapSmall> t;
   init_table(t, 1, 0, P + 1, 1, false);
+  t.status = comm->d_status;
   for (int q = 0; q < P; ++q) {
     void* ptrs[AR_MAX_RANKS + 1];
     int nd = 0;
@@ -310,7 +316,7 @@ ar_status_t ar_all_gather(ar_comm_t comm, const void* const* send, void* const* 
     }
     for (int k = 1 + nd; k < P + 1; ++k) ptrs[k] = ptrs[0];
     const uint32_t flags = vec_flag(ptrs, 1 + nd) | (uint32_t(nd) << 8);
-    if (!add_segment(t, ptrs, sbytes, gar::copy_tile_bytes(), flags)) return AR_ERR_INVALID_ARG;
+    if (!add_segment(t, ptrs, sbytes, copy_tile(comm), flags)) return AR_ERR_INVALID_ARG;
   }
   return run_copy(comm, t, static_cast<cudaStream_t>(stream));
 }
@@ -338,13 +344,14 @@ ar_status_t ar_broadcast(ar_comm_t comm, void* const* buf, size_t count, ar_dtyp
 
   SegTable<CapSmall> t;
   init_table(t, 1, 0, P, 1, false);
+  t.status = comm->d_status;
   void* ptrs[AR_MAX_RANKS];
   int nd = 0;
   ptrs[0] = buf[root];
   for (int r = 0; r < P; ++r)
     if (r != root) ptrs[1 + nd++] = buf[r];
   const uint32_t flags = vec_flag(ptrs, P) | (uint32_t(nd) << 8);
-  if (!add_segment(t, ptrs, bytes, gar::copy_tile_bytes(), flags)) return AR_ERR_INVALID_ARG;
+  if (!add_segment(t, ptrs, bytes, copy_tile(comm), flags)) return AR_ERR_INVALID_ARG;
   return run_copy(comm, t, static_cast<cudaStream_t>(stream));
 }
 

@@ -24,6 +24,14 @@ int resident_ctas(const void* func, int threads, size_t smem) {
 
 template <class Cap>
 cudaError_t launch_copy(const LaunchCtx& ctx, const SegTable<Cap>& tab) {
+  if (ctx.tma) {
+    auto* k = &k_copy_tma<Cap>;
+    const size_t smem = size_t(kCopyTmaStages) * kCopyTmaTile;
+    const int per_sm = resident_ctas(reinterpret_cast<const void*>(k), 32, smem);
+    const unsigned grid = grid_for(tab.ntiles, per_sm * ctx.num_sms);
+    if (grid == 0) return cudaSuccess;
+    return launch_ex(ctx, k, grid, 32, smem, tab);
+  }
   auto* k = &k_copy<Cap>;
   const unsigned grid = grid_for(tab.ntiles, resident_ctas(reinterpret_cast<const void*>(k)) * ctx.num_sms);
   if (grid == 0) return cudaSuccess;

@@ -18,18 +18,41 @@ constexpr int kThreads = 256;  // threads per CTA of every kernel
 // position and no other thread touches it, so the read-only (.nc) path
 // never sees a value written by the same kernel.
 
+// Cache hints of the streaming accesses (tuning knobs, fixed at build time):
+// GAR_LD_PREFETCH 1 adds an L2 256-byte prefetch hint to the loads;
+// GAR_ST_STREAMING 1 marks the stores evict-first (.cs), 0 leaves them
+// write-back with the default policy.
+#ifndef GAR_LD_PREFETCH
+#define GAR_LD_PREFETCH 0
+#endif
+#ifndef GAR_ST_STREAMING
+#define GAR_ST_STREAMING 1
+#endif
+
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
   uint4 r;
+#if GAR_LD_PREFETCH
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+#else
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p));
+#endif
   return r;
 }
 
 __device__ __forceinline__ void st_stream(void* p, const uint4& v) {
+#if GAR_ST_STREAMING
   asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)
                : "memory");
+#else
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+#endif
 }
 
 // fp32 master-weight / momentum arrays are read and written by the same

@@ -25,6 +25,7 @@ struct ar_comm_s {
   int kernel_mode;      // 0 = default (k_reduce), 1 = k_reduce, 2 = bulk-copy k_reduce_tma
   bool pdl;             // programmatic dependent launch between consecutive kernels
   int ctas_per_sm;      // GAR_CTAS_PER_SM: k_reduce CTAs per SM (-1 = default, 0 = occupancy)
+  bool copy_tma;        // all-gather / broadcast on the bulk-store k_copy_tma (default)
 };
 
 namespace gar_host {
@@ -191,6 +192,11 @@ void set_tma(SegTable<Cap>& t, const ar_comm_s* c, bool sgd, size_t es) {
   t.status = c->d_status;
 }
 
+// Tile (bytes) of the copy kernel a comm uses.
+inline uint64_t copy_tile(const ar_comm_s* c) {
+  return c->copy_tma ? uint64_t(gar::kCopyTmaTile) : gar::copy_tile_bytes();
+}
+
 inline uint32_t vec_flag(void* const* ptrs, int n, float* const* extra = nullptr, int nextra = 0) {
   for (int k = 0; k < n; ++k)
     if (!aligned(ptrs[k], 16)) return 0;
@@ -225,7 +231,7 @@ inline ar_status_t run_reduce(const ar_comm_s* c, ar_dtype_t dt, bool sgd, const
 template <class Cap>
 inline ar_status_t run_copy(const ar_comm_s* c, const SegTable<Cap>& t, cudaStream_t st) {
   if (t.ntiles == 0) return AR_OK;
-  const gar::LaunchCtx ctx{c->device, c->num_sms, st, false, c->pdl};
+  const gar::LaunchCtx ctx{c->device, c->num_sms, st, c->copy_tma, c->pdl};
   return from_cuda(gar::launch_copy<Cap>(ctx, t));
 }
 

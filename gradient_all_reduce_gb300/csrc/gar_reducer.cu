@@ -34,6 +34,7 @@ struct ar_reducer_s {
     std::vector<SegTable<CapLarge>> large;
     int pending = 0;                           // tensors not yet marked this step
     bool launched = false;
+    cudaEvent_t done = nullptr;                // recorded after the bucket's kernel
     std::vector<cudaStream_t> mark_streams;    // distinct streams that marked its tensors
   };
 
@@ -63,6 +64,8 @@ bool reducer_live(const ar_reducer_s* r) {
 }
 
 void release(ar_reducer_s* r) {
+  for (auto& bk : r->buckets)
+    if (bk.done) cudaEventDestroy(bk.done);
   for (int k = 0; k < 2; ++k) {
     if (r->done[k]) cudaEventDestroy(r->done[k]);
     if (r->streams[k]) cudaStreamDestroy(r->streams[k]);
@@ -91,6 +94,7 @@ ar_status_t launch_bucket(ar_reducer_s* r, int b) {
     if (st != AR_OK) return st;
   }
   if (cudaEventRecord(r->done[k], s) != cudaSuccess) return AR_ERR_CUDA;
+  if (cudaEventRecord(bk.done, s) != cudaSuccess) return AR_ERR_CUDA;
   r->used[k] = true;
   bk.launched = true;
   return AR_OK;
@@ -200,6 +204,11 @@ ar_status_t ar_reducer_create(ar_reducer_t* out, ar_comm_t comm, const ar_bucket
     release(r);
     return AR_ERR_CUDA;
   }
+  for (auto& bk : r->buckets)
+    if (cudaEventCreateWithFlags(&bk.done, cudaEventDisableTiming) != cudaSuccess) {
+      release(r);
+      return AR_ERR_CUDA;
+    }
   {
     std::lock_guard<std::mutex> lock(g_red_mu);
     g_reducers.insert(r);
@@ -259,6 +268,18 @@ ar_status_t ar_reducer_finalize(ar_reducer_t r, ar_stream_t stream) {
   std::fill(r->marked.begin(), r->marked.end(), 0);
   r->used[0] = r->used[1] = false;
   return st;
+}
+
+ar_status_t ar_reducer_wait_bucket(ar_reducer_t r, int bucket, ar_stream_t stream) {
+  if (!reducer_live(r) || !is_live(r->comm)) return AR_ERR_STATE;
+  if (bucket < 0 || bucket >= int(r->buckets.size())) return AR_ERR_INVALID_ARG;
+  if (!r->buckets[bucket].launched) return AR_ERR_STATE;
+  DeviceGuard guard(r->comm->device);
+  if (!guard.ok()) return AR_ERR_CUDA;
+  return cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), r->buckets[bucket].done, 0) ==
+                 cudaSuccess
+             ? AR_OK
+             : AR_ERR_CUDA;
 }
 
 ar_status_t ar_reducer_set_sgd(ar_reducer_t r, float lr, float momentum) {

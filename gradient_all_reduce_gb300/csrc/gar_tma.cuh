@@ -297,6 +297,127 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   }
 }
 
+// ------------------------------------------------------- bulk-store copy
+// k_copy_tma: the copy collectives (all-gather, broadcast) on the bulk-copy
+// engine.  Lane 0 of each CTA runs a pipeline over its tiles (kCopyTmaTile
+// bytes of one segment): a bulk load of tile j into stage j % S, then, once it has
+// landed, one bulk store of the stage to every destination of the segment
+// (a bulk group per tile).  The load of tile j + S - 1 reuses the stage of
+// tile j - 1 after that tile's stores have finished reading it, so S - 1
+// loads stay in flight while the stores drain.  Tiles without a 16-byte
+// part (a ragged tail only) or of unaligned segments still take their
+// pipeline slot, with nothing to load; their bytes are copied with 2-byte
+// accesses by the warp.  Every wait is bounded.
+#ifndef GAR_COPY_STAGES
+#define GAR_COPY_STAGES 4
+#endif
+#ifndef GAR_COPY_TILE_KB
+#define GAR_COPY_TILE_KB 16
+#endif
+constexpr int kCopyTmaStages = GAR_COPY_STAGES;
+constexpr uint32_t kCopyTmaTile = GAR_COPY_TILE_KB * 1024;
+
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+template <class Cap>
+__global__ void __launch_bounds__(32, 1) k_copy_tma(const __grid_constant__ SegTable<Cap> a) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kCopyTmaStages];
+  const uint32_t smem0 = smem_u32(smem_raw);
+  const int lane = threadIdx.x;
+  if (lane == 0) {
+    for (int k = 0; k < kCopyTmaStages; ++k) mbar_init(smem_u32(&full_bar[k]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+  griddep_launch_dependents();
+  griddep_wait();
+
+  // My tiles: blockIdx.x, blockIdx.x + G, ...; mine = how many.
+  const uint32_t G = gridDim.x;
+  const uint32_t mine = a.ntiles > blockIdx.x ? (a.ntiles - blockIdx.x + G - 1) / G : 0;
+
+  // Where tile `tile` lives: segment, byte offset, bytes of its 16-byte part.
+  struct Tile { uint32_t seg; uint64_t off; uint32_t vbytes; };
+  auto locate = [&](uint32_t tile, uint32_t& segc) {
+    while (tile >= a.tile0[segc + 1]) ++segc;
+    Tile t;
+    t.seg = segc;
+    t.off = uint64_t(tile - a.tile0[segc]) * kCopyTmaTile;
+    const uint64_t vb = (a.flags[segc] & kSegVec) ? (a.numel[segc] / 16) * 16 : 0;
+    t.vbytes = t.off < vb ? uint32_t(vb - t.off < kCopyTmaTile ? vb - t.off : kCopyTmaTile) : 0u;
+    return t;
+  };
+
+  bool ok = true;
+  uint32_t seg_load = 0, seg_store = 0;
+  if (lane == 0) {
+    // Prologue: loads of my tiles 0 .. S-2.
+    for (uint32_t j = 0; j + 1 < kCopyTmaStages && j < mine; ++j) {
+      const Tile t = locate(blockIdx.x + j * G, seg_load);
+      const uint32_t full = smem_u32(&full_bar[j % kCopyTmaStages]);
+      mbar_expect_tx(full, t.vbytes);
+      if (t.vbytes)
+        bulk_g2s(smem0 + (j % kCopyTmaStages) * kCopyTmaTile,
+                 static_cast<const char*>(a.ptr[uint64_t(t.seg) * a.stride]) + t.off, t.vbytes, full);
+    }
+  }
+  for (uint32_t j = 0; j < mine; ++j) {
+    const uint32_t tile = blockIdx.x + j * G;
+    const uint32_t stage = j % kCopyTmaStages;
+    uint32_t segc = seg_store;
+    const Tile t = locate(tile, segc);
+    seg_store = segc;
+    void* const* seg = a.ptr + uint64_t(t.seg) * a.stride;
+    const int nd = int(a.flags[t.seg] >> 8);
+    if (lane == 0 && ok) {
+      if (!mbar_wait_bounded(smem_u32(&full_bar[stage]), (j / kCopyTmaStages) & 1u, nullptr)) {
+        atomicExch(a.status, 1u);
+        ok = false;
+      } else {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (t.vbytes)
+          for (int d = 0; d < nd; ++d)
+            bulk_s2g(static_cast<char*>(seg[a.dst_off + d]) + t.off,
+                     smem0 + stage * kCopyTmaTile, t.vbytes);
+        bulk_commit();
+        // Load tile j + S - 1 into the stage of tile j - 1, once that
+        // tile's stores have read it (all groups but the newest).
+        const uint32_t jn = j + kCopyTmaStages - 1;
+        if (jn < mine) {
+          bulk_wait_read_1();
+          const Tile tn = locate(blockIdx.x + jn * G, seg_load);
+          const uint32_t full = smem_u32(&full_bar[jn % kCopyTmaStages]);
+          mbar_expect_tx(full, tn.vbytes);
+          if (tn.vbytes)
+            bulk_g2s(smem0 + (jn % kCopyTmaStages) * kCopyTmaTile,
+                     static_cast<const char*>(a.ptr[uint64_t(tn.seg) * a.stride]) + tn.off,
+                     tn.vbytes, full);
+        }
+      }
+    }
+    // The bytes of the tile that the bulk copies do not cover (a ragged
+    // tail, or the whole tile of an unaligned segment), 2 bytes at a time.
+    const uint64_t nbytes = a.numel[t.seg];
+    const uint64_t end = t.off + kCopyTmaTile < nbytes ? t.off + kCopyTmaTile : nbytes;
+    const uint16_t* src = static_cast<const uint16_t*>(seg[0]);
+    for (uint64_t h = (t.off + t.vbytes) / 2 + lane; h < end / 2; h += 32) {
+      const uint16_t x = src[h];
+      for (int d = 0; d < nd; ++d) static_cast<uint16_t*>(seg[a.dst_off + d])[h] = x;
+    }
+  }
+  if (lane == 0) bulk_wait_all();
+}
+
 // Failure-detection self-test: one warp waits on an mbarrier that nothing
 // ever arrives at, with the pipeline's bounded wait; when the wait gives up
 // it records status 1, exactly as a stalled pipeline stage would.

@@ -329,6 +329,15 @@ ar_status_t ar_reducer_mark_ready_many(ar_reducer_t reducer, const int *tensors,
  */
 ar_status_t ar_reducer_finalize(ar_reducer_t reducer, ar_stream_t stream);
 
+/*
+ * Makes `stream` wait (no host blocking) for bucket `bucket` of the current
+ * step -- e.g. to copy that bucket's results out while later buckets are
+ * still being produced (DDP's per-bucket completion).  AR_ERR_STATE if the
+ * bucket has not been launched in this step; AR_ERR_INVALID_ARG for an
+ * index outside 0 .. nbuckets-1 (see ar_reducer_info).
+ */
+ar_status_t ar_reducer_wait_bucket(ar_reducer_t reducer, int bucket, ar_stream_t stream);
+
 /* New SGD learning rate and momentum for the following launches (a
  * learning-rate schedule); AR_ERR_INVALID_ARG if the reducer has no SGD. */
 ar_status_t ar_reducer_set_sgd(ar_reducer_t reducer, float lr, float momentum);

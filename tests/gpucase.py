@@ -23,17 +23,22 @@ PATHS = ("ldg", "tma")   # register-staged k_reduce, bulk-copy pipelined k_reduc
 
 
 def init(P: int, op: int = gar.AR_MEAN, path: str | None = None) -> int:
-    """ar_init with the reduce kernel forced to ``path`` (read at init)."""
-    old = os.environ.get("GAR_KERNEL")
+    """ar_init with the reduce and copy kernels forced to ``path`` (read at
+    init): "ldg" for the register-staged kernels, "tma" for the bulk-copy
+    pipelines."""
+    keys = ("GAR_KERNEL", "GAR_COPY")
+    old = {k: os.environ.get(k) for k in keys}
     if path is not None:
-        os.environ["GAR_KERNEL"] = path
+        for k in keys:
+            os.environ[k] = path
     try:
         return gar.ar_init(P, 0, op)
     finally:
-        if old is None:
-            os.environ.pop("GAR_KERNEL", None)
-        else:
-            os.environ["GAR_KERNEL"] = old
+        for k in keys:
+            if old[k] is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = old[k]
 
 
 def dev():

@@ -188,3 +188,32 @@ def test_reducer_mark_ready_many_checks_first():
         gar.ar_destroy(comm)
     want = oracle.all_reduce(host_replicas(P, n, "f32", "normal", 60, std=1e-3), op=oracle.SUM)
     assert_bits_equal(to_np(flat[0]), want[0], "marked together")
+
+
+def test_reducer_wait_bucket_orders_copy_out():
+    """A side stream that waits for bucket b sees that bucket's results; a
+    bucket not launched yet is refused."""
+    P = 4
+    numels = [1 << 20, 1 << 20]
+    offs = np.concatenate([[0], np.cumsum(numels)])
+    n = int(offs[-1])
+    flat, w, v, grads, ws, vs = _setup(P, numels, offs, dt="f32", seed=70)
+    comm = gar.ar_init(P, 0, gar.AR_SUM)
+    red = gar.Reducer(comm, grads, numels, gar.AR_F32, 4 << 20, gar.AR_SUM)
+    side = torch.cuda.Stream()
+    try:
+        assert red.bucket_of() == [1, 0]
+        with pytest.raises(gar.GarError) as e:
+            red.wait_bucket(0, side)
+        assert e.value.status == gar.AR_ERR_STATE
+        red.mark_ready(1)                     # bucket 0 (the last tensor) launches
+        red.wait_bucket(0, side)
+        with torch.cuda.stream(side):
+            got = flat[2][offs[1]:offs[2]].clone()
+        red.finalize()
+        torch.cuda.synchronize()
+    finally:
+        red.destroy()
+        gar.ar_destroy(comm)
+    want = oracle.all_reduce(host_replicas(P, n, "f32", "normal", 70, std=1e-3), op=oracle.SUM)
+    assert_bits_equal(to_np(got), want[2][offs[1]:offs[2]], "copied after wait_bucket")
