@@ -63,6 +63,9 @@ def parse():
     ap.add_argument("--overlap", action="store_true",
                     help="measure the all-reduce hidden behind a ViT-B/16 backward pass instead")
     ap.add_argument("--batch", type=int, default=64, help="images per backward pass (--overlap)")
+    ap.add_argument("--case", choices=["ar", "rs", "ag", "bc", "zero1", "acc", "syncbn"],
+                    help="time one collective alone (P=8, 256 MiB per replica; ViT-sized for "
+                         "zero1/acc) and print its GB/s; for profiling single kernels")
     return ap.parse_args()
 
 
@@ -736,6 +739,82 @@ def run_overlap(args):
         gar.ar_destroy(comm)
 
 
+# ------------------------------------------------------------------ cases
+
+def run_case(args):
+    """One collective alone, K timed calls after W warm-up calls, one JSON
+    line: the workloads of the sweep (P = 8, fp32, 256 MiB per replica) or,
+    for zero1 and acc, of the ViT-B/16 gradient set (bf16)."""
+    import torch
+    import gradient_all_reduce_gb300 as gar
+    from workloads import gpu as wgpu
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.current_stream()
+    P = 8
+    comm = gar.ar_init(P, 0, gar.AR_MEAN)
+    try:
+        if args.case in ("ar", "rs", "ag", "bc"):
+            n = (256 << 20) // 4
+            xs = [torch.empty(n, device=device) for _ in range(P)]
+            for r, x in enumerate(xs):
+                wgpu.fill(x, "uniform", r)
+            sh = n // P
+            rs = [torch.empty(sh, device=device) for _ in range(P)]
+            ins = [x[r * sh:(r + 1) * sh] for r, x in enumerate(xs)]
+            fn, nbytes = {
+                "ar": (lambda: gar.ar_all_reduce(comm, xs, xs, n, gar.AR_F32, gar.AR_MEAN, stream),
+                       2 * P * n * 4),
+                "rs": (lambda: gar.ar_reduce_scatter(comm, xs, rs, n, gar.AR_F32, gar.AR_SUM, stream),
+                       (P + 1) * n * 4),
+                "ag": (lambda: gar.ar_all_gather(comm, ins, xs, n, gar.AR_F32, stream), P * n * 4),
+                "bc": (lambda: gar.ar_broadcast(comm, xs, n, gar.AR_F32, 0, stream), P * n * 4),
+            }[args.case]
+            what = f"P=8 fp32 256 MiB per replica"
+        elif args.case == "zero1":
+            n = -(-86_567_656 // (P * 8)) * (P * 8)
+            g = [torch.empty(n, dtype=torch.bfloat16, device=device) for _ in range(P)]
+            for r, x in enumerate(g):
+                wgpu.fill(x, "normal", 100 + r, std=1e-3)
+            params = [torch.empty(n, dtype=torch.bfloat16, device=device) for _ in range(P)]
+            ws = [torch.zeros(n // P, device=device) for _ in range(P)]
+            vs = [torch.zeros(n // P, device=device) for _ in range(P)]
+            fn = lambda: gar.ar_sharded_sgd_step(comm, g, params, ws, vs, n, gar.AR_BF16, 0.1, 0.9,
+                                                 gar.AR_MEAN, stream)
+            nbytes, what = 4 * P * n + 16 * n, "ViT-B/16 flat unit, P=8 bf16"
+        elif args.case == "acc":
+            n = (25 << 20) // 2
+            g = [torch.empty(n, dtype=torch.bfloat16, device=device) for _ in range(P)]
+            for r, x in enumerate(g):
+                wgpu.fill(x, "normal", 100 + r, std=1e-3)
+            acc = [[torch.zeros(n, device=device) for _ in range(P)]]
+            fn = lambda: gar.ar_bucket_accumulate(comm, [g], [n], gar.AR_BF16, acc, 0.25, False,
+                                                  stream)
+            nbytes, what = 10 * P * n, "one 25 MiB bf16 bucket, P=8, a micro-batch before the last"
+        else:
+            C = 2048
+            sums = [torch.rand(C, device=device) for _ in range(P)]
+            sq = [torch.rand(C, device=device) + 1 for _ in range(P)]
+            mo = [torch.empty(C, device=device) for _ in range(P)]
+            io = [torch.empty(C, device=device) for _ in range(P)]
+            fn = lambda: gar.ar_syncbn_stats(comm, sums, sq, [1000] * P, mo, io, C, 1e-5, stream)
+            nbytes, what = 4 * P * C * 4, "P=8, 2048 channels"
+        for _ in range(max(1, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) / 1e3 / args.steps
+        print(json.dumps({"case": args.case, "workload": what, "us": t * 1e6,
+                          "GBps": nbytes / t / 1e9}), flush=True)
+    finally:
+        gar.ar_destroy(comm)
+
+
 # -------------------------------------------------------------------- main
 
 def main():
@@ -745,6 +824,9 @@ def main():
         return
     if args.overlap:
         run_overlap(args)
+        return
+    if args.case:
+        run_case(args)
         return
     rank, world, local = dist_env()
     import torch
