@@ -60,7 +60,11 @@ cudaError_t launch_wait_selftest(cudaStream_t stream, uint32_t* status, uint64_t
 // ranks' per-channel sums in fp64 (rank order), forms mean, biased
 // variance and invstd with IEEE-rounded fp64 operations, and writes both,
 // rounded to fp32, for every rank.
-__global__ void __launch_bounds__(128) k_syncbn_stats(const __grid_constant__ SyncBnArgs a) {
+// One warp per CTA: the fp64 divide and square root are long dependent
+// chains, so the channels are spread over as many SMs as possible.
+constexpr int kSyncBnThreads = 32;
+
+__global__ void __launch_bounds__(kSyncBnThreads) k_syncbn_stats(const __grid_constant__ SyncBnArgs a) {
   griddep_launch_dependents();
   griddep_wait();
   const uint64_t stride = uint64_t(gridDim.x) * blockDim.x;
@@ -82,10 +86,11 @@ __global__ void __launch_bounds__(128) k_syncbn_stats(const __grid_constant__ Sy
 }
 
 cudaError_t launch_syncbn_stats(const LaunchCtx& ctx, const SyncBnArgs& args) {
-  const uint64_t blocks = (args.channels + 127) / 128;
-  const unsigned grid = unsigned(blocks < uint64_t(ctx.num_sms) * 8 ? blocks : uint64_t(ctx.num_sms) * 8);
+  const uint64_t blocks = (args.channels + kSyncBnThreads - 1) / kSyncBnThreads;
+  const uint64_t cap = uint64_t(ctx.num_sms) * 16;
+  const unsigned grid = unsigned(blocks < cap ? blocks : cap);
   if (grid == 0) return cudaSuccess;
-  return launch_ex(ctx, &k_syncbn_stats, grid, 128, 0, args);
+  return launch_ex(ctx, &k_syncbn_stats, grid, kSyncBnThreads, 0, args);
 }
 
 template cudaError_t launch_copy<CapSmall>(const LaunchCtx&, const SegTable<CapSmall>&);
