@@ -375,3 +375,42 @@ class Reducer:
         if self.handle:
             _ok(load().ar_reducer_destroy(self.handle), "ar_reducer_destroy")
             self.handle = 0
+
+
+class PreparedCall:
+    """One of the flat collectives (``ar_all_reduce``, ``ar_reduce_scatter``,
+    ``ar_all_gather``, ``ar_broadcast``, ``ar_sharded_sgd_step``) with its
+    pointer arrays marshalled once, for a loop that repeats the same call on
+    the same buffers: ``PreparedCall("ar_all_reduce", comm, send, recv,
+    count, dtype, op)(stream)``.  The library still validates every call."""
+
+    _LAYOUT = {
+        "ar_all_reduce": ("comm", "ptrs", "ptrs", "size", "int", "int"),
+        "ar_reduce_scatter": ("comm", "ptrs", "ptrs", "size", "int", "int"),
+        "ar_all_gather": ("comm", "ptrs", "ptrs", "size", "int"),
+        "ar_broadcast": ("comm", "ptrs", "size", "int", "int"),
+        "ar_sharded_sgd_step": ("comm", "ptrs", "ptrs", "ptrs", "ptrs", "size", "int", "int",
+                                "float", "float"),
+    }
+
+    def __init__(self, name: str, *args):
+        kinds = self._LAYOUT[name]
+        if len(args) != len(kinds):
+            raise TypeError(f"{name} takes {len(kinds)} arguments before the stream")
+        self._keep = []
+        conv = []
+        for kind, a in zip(kinds, args):
+            if kind == "ptrs":
+                arr = _ptr_array(a)
+                self._keep.append(arr)
+                conv.append(arr)
+            elif kind == "float":
+                conv.append(float(a))
+            else:
+                conv.append(int(a))
+        self._fn = getattr(load(), name)
+        self._args = tuple(conv)
+        self._name = name
+
+    def __call__(self, stream=None) -> None:
+        _ok(self._fn(*self._args, _stream(stream)), self._name)

@@ -215,7 +215,7 @@ ar_status_t ar_all_reduce(ar_comm_t comm, const void* const* send, void* const* 
     if (!pointer_ok(comm, send[r], bytes) || !pointer_ok(comm, recv[r], bytes))
       return AR_ERR_INVALID_ARG;
 
-  SegTable<CapSmall> t;
+  SegTable<CapTiny> t;
   init_table(t, P, P, 2 * P, P, rop == AR_MEAN);
   const bool tma = choose_tma(comm, P, false, es);
   if (tma) set_tma(t, comm, false, es);

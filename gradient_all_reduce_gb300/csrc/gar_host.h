@@ -32,6 +32,7 @@ namespace gar_host {
 
 using gar::CapLarge;
 using gar::CapSmall;
+using gar::CapTiny;
 using gar::SegTable;
 
 // True when c is a comm returned by ar_init and not yet destroyed.

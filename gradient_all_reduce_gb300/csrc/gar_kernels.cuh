@@ -37,9 +37,11 @@ __host__ __device__ constexpr int unroll_for_sgd(int PT) {
 }
 constexpr int kCopyUnroll = 4;
 
-// Segment table capacities: small launches (<= 16 segments) use a 4 KB
-// parameter block, large ones (<= 256 segments) about 25 KB, inside the
-// 32,764-byte kernel-parameter limit.
+// Segment table capacities: a flat all-reduce (one segment) uses a 400-byte
+// parameter block, small launches (<= 16 segments) about 5 KB, large ones
+// (<= 256 segments) about 25 KB, inside the 32,764-byte kernel-parameter
+// limit; the smaller the block, the cheaper the launch.
+struct CapTiny { static constexpr int kSeg = 1, kPtr = 2 * kMaxRanks; };  // one flat all-reduce
 struct CapSmall { static constexpr int kSeg = 16, kPtr = 512; };
 struct CapLarge { static constexpr int kSeg = 256, kPtr = 2048; };
 

@@ -266,3 +266,38 @@ def test_device_generator_matches_host():
             t = replicas(1, 100_003, dt, kind, 7, std=std)[0]
             assert_bits_equal(to_np(t), host_replicas(1, 100_003, dt, kind, 7, std=std)[0],
                               f"{dt} {kind}")
+
+
+def test_prepared_calls_match_direct_calls(comms):
+    """PreparedCall (arguments marshalled once) gives the direct call's bits,
+    and a CUDA graph of it replays the same computation."""
+    P, n = 8, 100_003
+    comm = comms(P)
+    xs = replicas(P, n, "f32", "uniform", 90)
+    ys = [empty(n, "f32") for _ in range(P)]
+    zs = [empty(n, "f32") for _ in range(P)]
+    gar.ar_all_reduce(comm, xs, ys, n, gar.AR_F32, gar.AR_MEAN)
+    call = gar.PreparedCall("ar_all_reduce", comm, xs, zs, n, gar.AR_F32, gar.AR_MEAN)
+    call()
+    _sync_ok(comm)
+    for r in range(P):
+        assert bits_equal_device(ys[r], zs[r]), r
+    for z in zs:
+        z.zero_()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    call(side)
+    torch.cuda.synchronize()
+    for z in zs:
+        z.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call(torch.cuda.current_stream())
+    graph.replay()
+    torch.cuda.synchronize()
+    for r in range(P):
+        assert bits_equal_device(ys[r], zs[r]), r
+    bc = gar.PreparedCall("ar_broadcast", comm, zs, n, gar.AR_F32, 3)
+    bc()
+    torch.cuda.synchronize()
+    assert bits_equal_device(zs[0], zs[3])
