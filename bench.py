@@ -463,10 +463,24 @@ def time_sweep(device, stream):
                 for kib in (4, 64, 1024):
                     n = (kib << 10) // 4
                     xs = [torch.empty(n, dtype=torch.float32, device=device) for _ in range(P)]
-                    t = timed(lambda: gar.ar_all_reduce(comm, xs, xs, n, gar.AR_F32, gar.AR_MEAN,
-                                                        stream), 50, flush_between=False)
+                    t_api = timed(lambda: gar.ar_all_reduce(comm, xs, xs, n, gar.AR_F32,
+                                                            gar.AR_MEAN, stream),
+                                  200, flush_between=False)
+                    call = gar.PreparedCall("ar_all_reduce", comm, xs, xs, n, gar.AR_F32,
+                                            gar.AR_MEAN)
+                    t_prep = timed(lambda: call(stream), 200, flush_between=False)
+                    side = torch.cuda.Stream(device)
+                    side.wait_stream(stream)
+                    call(side)
+                    torch.cuda.synchronize(device)
+                    graph = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(graph):
+                        call(torch.cuda.current_stream())
+                    t_graph = timed(graph.replay, 200, flush_between=False)
                     out["small_all_reduce_us"].append({"P": P, "KiB_per_replica": kib,
-                                                       "us": t * 1e6})
+                                                       "api_us": t_api * 1e6,
+                                                       "prepared_us": t_prep * 1e6,
+                                                       "graph_us": t_graph * 1e6})
                     del xs
         finally:
             gar.ar_destroy(comm)
