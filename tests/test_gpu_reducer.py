@@ -217,3 +217,43 @@ def test_reducer_wait_bucket_orders_copy_out():
         gar.ar_destroy(comm)
     want = oracle.all_reduce(host_replicas(P, n, "f32", "normal", 70, std=1e-3), op=oracle.SUM)
     assert_bits_equal(to_np(got), want[2][offs[1]:offs[2]], "copied after wait_bucket")
+
+
+def test_reducer_step_captured_in_a_cuda_graph():
+    """A whole reducer step (marks + finalize) captured into a CUDA graph on
+    a capturing stream: the communication streams join the capture through
+    the reducer's events; two replays give two oracle steps' bits."""
+    P = 8
+    numels, offs = _vit_prefix(6_000_000)
+    n = int(offs[-1])
+    flat, w, v, grads, ws, vs = _setup(P, numels, offs)
+    comm = gar.ar_init(P, 0, gar.AR_MEAN)
+    red = gar.Reducer(comm, grads, numels, gar.AR_BF16, 4 << 20, gar.AR_MEAN,
+                      sgd=(0.1, 0.9, ws, vs, 1))
+    order = list(range(len(numels) - 1, -1, -1))
+    host = host_replicas(P, n, "bf16", "normal", 100, std=1e-3)
+    hw = [workloads.normal_f32(200, n, std=0.02)]
+    hv = [np.zeros(n, np.float32)]
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):                 # one eager step (warm-up)
+            red.mark_ready_many(order, side)
+            red.finalize(side)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        oracle.bucket_all_reduce([host], op=oracle.MEAN, sgd=(0.1, 0.9, hw, hv, 1))
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            s = torch.cuda.current_stream()
+            red.mark_ready_many(order, s)
+            red.finalize(s)
+        for step in range(2):
+            graph.replay()
+            torch.cuda.synchronize()
+            oracle.bucket_all_reduce([host], op=oracle.MEAN, sgd=(0.1, 0.9, hw, hv, 1))
+            assert_bits_equal(to_np(w), hw[0], f"replay {step} master")
+            assert_bits_equal(to_np(flat[P - 1]), host[P - 1], f"replay {step} grad")
+    finally:
+        red.destroy()
+        gar.ar_destroy(comm)
