@@ -62,13 +62,14 @@ ar_status_t check_bucket_buffers(const ar_comm_s* comm, const ar_bucket_t* bucke
             [](const Range& a, const Range& b) { return a.lo < b.lo; });
   for (size_t k = 1; k < ranges.size(); ++k)
     if (ranges[k].lo < ranges[k - 1].hi) return AR_ERR_INVALID_ARG;
+  PointerChecker ok(comm);
   for (int t = 0; t < T; ++t) {
     const size_t n = bucket->numel[t];
     if (n == 0) continue;
     for (int r = 0; r < P; ++r)
-      if (!pointer_ok(comm, bucket->dev_ptrs[size_t(t) * P + r], n * es)) return AR_ERR_INVALID_ARG;
+      if (!ok(bucket->dev_ptrs[size_t(t) * P + r], n * es)) return AR_ERR_INVALID_ARG;
     if (sgd != nullptr &&
-        (!pointer_ok(comm, sgd->master[t], n * 4) || !pointer_ok(comm, sgd->momentum_buf[t], n * 4)))
+        (!ok(sgd->master[t], n * 4) || !ok(sgd->momentum_buf[t], n * 4)))
       return AR_ERR_INVALID_ARG;
   }
 
@@ -211,8 +212,9 @@ ar_status_t ar_all_reduce(ar_comm_t comm, const void* const* send, void* const* 
       const bool in_place = q == r && recv[r] == send[r];
       if (!in_place && overlap(recv[r], bytes, send[q], bytes)) return AR_ERR_INVALID_ARG;
     }
+  PointerChecker ok(comm);
   for (int r = 0; r < P; ++r)
-    if (!pointer_ok(comm, send[r], bytes) || !pointer_ok(comm, recv[r], bytes))
+    if (!ok(send[r], bytes) || !ok(recv[r], bytes))
       return AR_ERR_INVALID_ARG;
 
   SegTable<CapTiny> t;
@@ -255,8 +257,9 @@ ar_status_t ar_reduce_scatter(ar_comm_t comm, const void* const* send, void* con
           q == r && addr(recv[r]) == addr(send[r]) + size_t(r) * sbytes;
       if (!in_place && overlap(recv[r], sbytes, send[q], bytes)) return AR_ERR_INVALID_ARG;
     }
+  PointerChecker ok(comm);
   for (int r = 0; r < P; ++r)
-    if (!pointer_ok(comm, send[r], bytes) || !pointer_ok(comm, recv[r], sbytes))
+    if (!ok(send[r], bytes) || !ok(recv[r], sbytes))
       return AR_ERR_INVALID_ARG;
 
   SegTable<CapSmall> t;
@@ -299,8 +302,9 @@ ar_status_t ar_all_gather(ar_comm_t comm, const void* const* send, void* const* 
           q == r && addr(send[r]) == addr(recv[r]) + size_t(r) * sbytes;
       if (!in_place && overlap(recv[r], bytes, send[q], sbytes)) return AR_ERR_INVALID_ARG;
     }
+  PointerChecker ok(comm);
   for (int r = 0; r < P; ++r)
-    if (!pointer_ok(comm, send[r], sbytes) || !pointer_ok(comm, recv[r], bytes))
+    if (!ok(send[r], sbytes) || !ok(recv[r], bytes))
       return AR_ERR_INVALID_ARG;
 
   SegTable<CapSmall> t;
@@ -339,8 +343,9 @@ ar_status_t ar_broadcast(ar_comm_t comm, void* const* buf, size_t count, ar_dtyp
       if (overlap(buf[r], bytes, buf[q], bytes)) return AR_ERR_INVALID_ARG;
   }
   if (P == 1) return AR_OK;
+  PointerChecker ok(comm);
   for (int r = 0; r < P; ++r)
-    if (!pointer_ok(comm, buf[r], bytes)) return AR_ERR_INVALID_ARG;
+    if (!ok(buf[r], bytes)) return AR_ERR_INVALID_ARG;
 
   SegTable<CapSmall> t;
   init_table(t, 1, 0, P, 1, false);
@@ -419,6 +424,7 @@ static ar_status_t check_acc_buffers(const ar_comm_s* comm, const ar_bucket_t* b
   if (acc == nullptr || (b->ntensors > 0 && acc->acc == nullptr)) return AR_ERR_INVALID_ARG;
   const int T = b->ntensors, P = comm->nranks;
   const size_t es = elem_bytes(b->dtype);
+  PointerChecker ok(comm);
   struct Range { uintptr_t lo, hi; };
   std::vector<Range> ranges;
   for (int t = 0; t < T; ++t) {
@@ -428,7 +434,7 @@ static ar_status_t check_acc_buffers(const ar_comm_s* comm, const ar_bucket_t* b
       const void* g = b->dev_ptrs[size_t(t) * P + r];
       const float* a = acc->acc[size_t(t) * P + r];
       if (a == nullptr || !aligned(a, 4)) return AR_ERR_INVALID_ARG;
-      if (!pointer_ok(comm, a, n * 4)) return AR_ERR_INVALID_ARG;
+      if (!ok(a, n * 4)) return AR_ERR_INVALID_ARG;
       ranges.push_back({addr(g), addr(g) + n * es});
       ranges.push_back({addr(a), addr(a) + n * 4});
     }
@@ -569,6 +575,7 @@ ar_status_t ar_sharded_sgd_step(ar_comm_t comm, const void* const* grads, void* 
   if (!guard.ok()) return AR_ERR_CUDA;
   // grads / params: in place (params[r] == grads[r]) or disjoint; shards:
   // fp32, disjoint from everything.
+  PointerChecker ok(comm);
   struct Range { uintptr_t lo, hi; };
   std::vector<Range> ranges;
   for (int r = 0; r < P; ++r) {
@@ -579,8 +586,8 @@ ar_status_t ar_sharded_sgd_step(ar_comm_t comm, const void* const* grads, void* 
     if (g == nullptr || p == nullptr || w == nullptr || v == nullptr) return AR_ERR_INVALID_ARG;
     if (!aligned(g, es) || !aligned(p, es) || !aligned(w, 4) || !aligned(v, 4))
       return AR_ERR_INVALID_ARG;
-    if (!pointer_ok(comm, g, bytes) || !pointer_ok(comm, p, bytes) ||
-        !pointer_ok(comm, w, sbytes) || !pointer_ok(comm, v, sbytes))
+    if (!ok(g, bytes) || !ok(p, bytes) ||
+        !ok(w, sbytes) || !ok(v, sbytes))
       return AR_ERR_INVALID_ARG;
     ranges.push_back({addr(g), addr(g) + bytes});
     if (p != g) ranges.push_back({addr(p), addr(p) + bytes});
@@ -635,12 +642,13 @@ ar_status_t ar_syncbn_stats(ar_comm_t comm, const float* const* sum, const float
   if (!mul_ok(channels, 4, &bytes)) return AR_ERR_INVALID_ARG;
   DeviceGuard guard(comm->device);
   if (!guard.ok()) return AR_ERR_CUDA;
+  PointerChecker ok(comm);
   struct Range { uintptr_t lo, hi; };
   std::vector<Range> outs;
   for (int r = 0; r < P; ++r) {
     const void* ps[4] = {sum[r], sqsum[r], mean[r], invstd[r]};
     for (const void* p : ps)
-      if (p == nullptr || !aligned(p, 4) || !pointer_ok(comm, p, bytes)) return AR_ERR_INVALID_ARG;
+      if (p == nullptr || !aligned(p, 4) || !ok(p, bytes)) return AR_ERR_INVALID_ARG;
     outs.push_back({addr(mean[r]), addr(mean[r]) + bytes});
     outs.push_back({addr(invstd[r]), addr(invstd[r]) + bytes});
   }

@@ -133,3 +133,57 @@ def test_bucket_rejects_overlap(cuda):
                                      sgd=(0.1, 0.9, [w], [w], 1))   # master aliases momentum
     finally:
         gar.ar_destroy(comm)
+
+
+def _allocation(ptr):
+    """(base, size) of the device allocation that holds ptr, from the driver."""
+    import ctypes
+    drv = ctypes.CDLL("libcuda.so.1")
+    base, size = ctypes.c_uint64(), ctypes.c_size_t()
+    rc = drv.cuMemGetAddressRange_v2(ctypes.byref(base), ctypes.byref(size), ctypes.c_uint64(ptr))
+    assert rc == 0, rc
+    return base.value, size.value
+
+
+def test_bounds_checked_inside_an_allocation_already_seen(cuda):
+    """A call validates each device allocation once and then checks later
+    buffers that start inside it against its end alone.  Tensor 0 makes the
+    allocation known; tensor 1 starts inside it: ending exactly at the
+    allocation's end it is accepted (and reduced), one element further it is
+    refused.  Likewise for the SGD master / momentum arrays."""
+    comm = gar.ar_init(1, 0, gar.AR_SUM)
+    try:
+        torch.cuda.empty_cache()        # fresh allocations: no other tensor inside them
+        a = torch.zeros(4 << 20, device=dev())
+        base, size = _allocation(a.data_ptr())
+        k = 4096
+        start = a.data_ptr() + 4 * k
+        m = (base + size - start) // 4               # tensor 1 ends at the allocation's end
+        assert m >= 1 and start + 4 * m == base + size
+        ptrs = [[a.data_ptr()], [start]]
+        gar.ar_bucket_all_reduce(comm, ptrs, [k, m], gar.AR_F32)
+        torch.cuda.synchronize()
+        with pytest.raises(gar.GarError) as e:
+            gar.ar_bucket_all_reduce(comm, ptrs, [k, m + 1], gar.AR_F32)
+        assert e.value.status == gar.AR_ERR_INVALID_ARG
+        with pytest.raises(gar.GarError) as e:                      # the same buffer alone
+            gar.ar_bucket_all_reduce(comm, [[start]], [m + 1], gar.AR_F32)
+        assert e.value.status == gar.AR_ERR_INVALID_ARG
+        # master and momentum as views of one allocation each, after the grads
+        g = torch.zeros(2 * k, device=dev())
+        w = torch.zeros(4 << 20, device=dev())
+        wb, wsize = _allocation(w.data_ptr())
+        v = torch.zeros(2 * k, device=dev())
+        wend = wb + wsize
+        w1 = wend - 4 * k                             # master of tensor 1: the last k floats
+        assert w1 >= w.data_ptr() + 4 * k
+        sgd_ok = (0.1, 0.9, [w.data_ptr(), w1], [v[:k], v[k:]], 0)
+        gar.ar_bucket_all_reduce(comm, [[g[:k]], [g[k:]]], [k, k], gar.AR_F32, sgd=sgd_ok)
+        torch.cuda.synchronize()
+        sgd_bad = (0.1, 0.9, [w.data_ptr(), w1 + 4], [v[:k], v[k:]], 0)   # one float past
+        with pytest.raises(gar.GarError) as e:
+            gar.ar_bucket_all_reduce(comm, [[g[:k]], [g[k:]]], [k, k], gar.AR_F32, sgd=sgd_bad)
+        assert e.value.status == gar.AR_ERR_INVALID_ARG
+        assert gar.ar_get_async_error(comm) == gar.AR_OK
+    finally:
+        gar.ar_destroy(comm)
