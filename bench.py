@@ -63,6 +63,9 @@ def parse():
     ap.add_argument("--overlap", action="store_true",
                     help="measure the all-reduce hidden behind a ViT-B/16 backward pass instead")
     ap.add_argument("--batch", type=int, default=64, help="images per backward pass (--overlap)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="the full size/replica sweep instead: all-reduce (Sum, Mean) and "
+                         "broadcast, 4 KiB .. 1 GiB per replica, P = 2, 4, 8, fp32 and bf16")
     ap.add_argument("--case", choices=["ar", "rs", "ag", "bc", "zero1", "acc", "syncbn"],
                     help="time one collective alone (P=8, 256 MiB per replica; ViT-sized for "
                          "zero1/acc) and print its GB/s; for profiling single kernels")
@@ -393,7 +396,13 @@ def time_e2e(args, device, stream):
 
 
 def flush_l2(buf):
-    buf.add_(1)
+    """Evict L2 before a timed call: write one 256 MiB buffer (twice the L2),
+    then read a second one, which writes the first one's dirty lines back and
+    leaves only clean lines behind.  The timed call then reads its inputs
+    from HBM and pays for no write-back of the flush (the cold, clean state
+    that ncu's cache control also gives)."""
+    buf[0].add_(1)
+    buf[1].sum()
 
 
 def time_sweep(device, stream):
@@ -401,11 +410,12 @@ def time_sweep(device, stream):
     256 MiB and 1 GiB per replica, fp32 and bf16; reduce-scatter,
     all-gather and broadcast at 256 MiB per replica, P = 4 and 8; and the
     latency of small all-reduces (4 KiB .. 1 MiB, P = 8, fp32).  L2 is
-    flushed (a 256 MiB write) between repetitions."""
+    flushed between repetitions (flush_l2: a 256 MiB write, then a 256 MiB
+    read)."""
     import torch
     import gradient_all_reduce_gb300 as gar
     from workloads import gpu as wgpu
-    flush = torch.empty(64 << 20, dtype=torch.float32, device=device)
+    flush = [torch.zeros(64 << 20, dtype=torch.float32, device=device) for _ in range(2)]
     out = {"all_reduce": [], "reduce_scatter": [], "all_gather": [], "broadcast": [],
            "small_all_reduce_us": []}
 
@@ -753,6 +763,125 @@ def run_overlap(args):
         gar.ar_destroy(comm)
 
 
+# ------------------------------------------------------------ full sweep
+
+SWEEP_KIB = [4 << (2 * k) for k in range(10)]          # 4 KiB .. 1 GiB per replica
+
+
+def run_full_sweep(args):
+    """All-reduce GB/s and fraction of the HBM roofline against message size:
+    per replica 4 KiB * 4^k (k = 0..9), P = 2, 4, 8, fp32 and bf16, Sum and
+    Mean, in place; and broadcast from rank 0 at the same sizes.  Each row
+    is the median of event-timed calls on one stream, each preceded by a
+    256 MiB write and a 256 MiB read that leave L2 clean and cold (flush_l2);
+    5 warm-up calls, 20 timed (200 below 1 MiB).  Rows below 1 MiB also
+    give the latency of back-to-back calls through the API and as a
+    replayed CUDA graph (no flush: the launch cost is what they measure).
+    Sum rows repeat on the same buffers (values may overflow to inf; the
+    kernels' time does not depend on values).  One JSON line; rank 0 of a
+    single process only."""
+    import torch
+    import gradient_all_reduce_gb300 as gar
+    from workloads import gpu as wgpu
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device)
+    peak, peak_kind = measured_peak()
+    flush = [torch.zeros(64 << 20, dtype=torch.float32, device=device) for _ in range(2)]
+
+    def median_time(fn, reps, flush_between):
+        ts = []
+        with torch.cuda.stream(stream):
+            for i in range(reps + 5):
+                if flush_between:
+                    flush_l2(flush)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                if i >= 5:
+                    ts.append((e0, e1))
+            torch.cuda.synchronize(device)
+        return statistics.median(a.elapsed_time(b) / 1e3 for a, b in ts)
+
+    def graph_of(fn):
+        side = torch.cuda.Stream(device)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            fn(side)
+        torch.cuda.synchronize(device)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            fn(torch.cuda.current_stream())
+        return graph
+
+    rows = []
+    t_start = time.perf_counter()
+    with ClockSampler(0) as clocks:
+        # The floor of one launch, measured the same ways: a one-CTA torch
+        # kernel on 4 KiB (event-timed after the flush, back to back, and as
+        # a replayed one-node CUDA graph).
+        tiny = torch.zeros(1024, dtype=torch.float32, device=device)
+        g_tiny = graph_of(lambda s: tiny.add_(1))
+        floor = {"what": "torch add_ on 4 KiB (one small kernel), timed like the rows",
+                 "us": 1e6 * median_time(lambda: tiny.add_(1), 200, True),
+                 "api_us": 1e6 * median_time(lambda: tiny.add_(1), 200, False),
+                 "graph_us": 1e6 * median_time(g_tiny.replay, 200, False)}
+        del g_tiny
+        for P in (2, 4, 8):
+            comm = gar.ar_init(P, 0, gar.AR_MEAN)
+            try:
+                for dt, es, tdt, name in ((gar.AR_F32, 4, torch.float32, "f32"),
+                                          (gar.AR_BF16, 2, torch.bfloat16, "bf16")):
+                    nmax = (SWEEP_KIB[-1] << 10) // es
+                    bufs = [torch.empty(nmax, dtype=tdt, device=device) for _ in range(P)]
+                    for kib in SWEEP_KIB:
+                        n = (kib << 10) // es
+                        small = kib < 1024
+                        reps = 200 if small else 20
+                        xs = [b[:n] for b in bufs]
+                        for op, opname in ((gar.AR_SUM, "sum"), (gar.AR_MEAN, "mean"),
+                                           (None, "broadcast")):
+                            for r, x in enumerate(xs):
+                                wgpu.fill(x, "uniform", r)
+                            if op is None:
+                                call = gar.PreparedCall("ar_broadcast", comm, xs, n, dt, 0)
+                                nbytes = P * n * es
+                            else:
+                                call = gar.PreparedCall("ar_all_reduce", comm, xs, xs, n, dt, op)
+                                nbytes = 2 * P * n * es
+                            if op is None:
+                                t = median_time(lambda: gar.ar_broadcast(comm, xs, n, dt, 0, stream),
+                                                reps, True)
+                            else:
+                                t = median_time(lambda: gar.ar_all_reduce(comm, xs, xs, n, dt, op,
+                                                                          stream), reps, True)
+                            row = {"op": opname, "P": P, "dtype": name, "KiB_per_replica": kib,
+                                   "bytes": nbytes, "us": t * 1e6, "GBps": nbytes / t / 1e9,
+                                   "frac": nbytes / t / 1e9 / peak}
+                            if small:
+                                row["api_us"] = 1e6 * median_time(
+                                    lambda: call(stream), reps, False)
+                                g = graph_of(call)
+                                row["graph_us"] = 1e6 * median_time(g.replay, reps, False)
+                                del g
+                            rows.append(row)
+                    del bufs, xs
+                    torch.cuda.empty_cache()
+                if gar.ar_get_async_error(comm) != gar.AR_OK:
+                    raise RuntimeError("device status")
+            finally:
+                gar.ar_destroy(comm)
+    print(json.dumps({
+        "mode": "sweep", "metric": METRIC, "peak_GBps": peak, "peak_kind": peak_kind,
+        "bytes": "all-reduce 2*P*N*s, broadcast P*N*s (every replica read and written once)",
+        "timing": ("median of event-timed calls after a 256 MiB write and a 256 MiB read "
+                   "(L2 cold and clean); 5 warm-up, "
+                   "20 timed (200 below 1 MiB); api_us / graph_us: back-to-back calls, no flush"),
+        "seconds": time.perf_counter() - t_start, "clocks": clocks.summary(),
+        "launch_floor": floor, "rows": rows}), flush=True)
+
+
 # ------------------------------------------------------------------ cases
 
 def run_case(args):
@@ -841,6 +970,9 @@ def main():
         return
     if args.case:
         run_case(args)
+        return
+    if args.sweep:
+        run_full_sweep(args)
         return
     rank, world, local = dist_env()
     import torch

@@ -94,15 +94,20 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// fp32 -> bf16 by IEEE round-to-nearest-even on the 16 dropped bits: adding
-// 0x7FFF plus the lowest kept bit carries into the kept part exactly when
-// the dropped part is above one half, or exactly one half with an odd kept
-// part.  A carry out of the significand increments the exponent (and turns
-// overflow into infinity).  NaN stays NaN (quiet bit forced).
-__device__ __forceinline__ uint32_t bf16_rne(float f) {
-  uint32_t u = __float_as_uint(f);
-  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return (u >> 16) | 0x40u;
-  return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+// fp32 -> bf16, IEEE round to nearest, ties to even, by the hardware
+// conversion (cvt.rn without .ftz: subnormals are kept, a value that rounds
+// past the largest finite bf16 becomes infinity, a NaN stays a NaN).  The
+// packed form takes two values; its first source operand fills the upper
+// half.
+__device__ __forceinline__ uint32_t bf16x2_rne(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+__device__ __forceinline__ uint16_t bf16_rne(float f) {
+  uint16_t h;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(f));
+  return h;
 }
 
 struct F32 {
@@ -137,16 +142,14 @@ struct BF16 {
     f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
   }
   __device__ static __forceinline__ uint4 pack(const float (&f)[8]) {
-    return make_uint4(bf16_rne(f[0]) | (bf16_rne(f[1]) << 16),
-                      bf16_rne(f[2]) | (bf16_rne(f[3]) << 16),
-                      bf16_rne(f[4]) | (bf16_rne(f[5]) << 16),
-                      bf16_rne(f[6]) | (bf16_rne(f[7]) << 16));
+    return make_uint4(bf16x2_rne(f[0], f[1]), bf16x2_rne(f[2], f[3]), bf16x2_rne(f[4], f[5]),
+                      bf16x2_rne(f[6], f[7]));
   }
   __device__ static __forceinline__ float load1(const void* p, uint64_t i) {
     return __uint_as_float(uint32_t(static_cast<const uint16_t*>(p)[i]) << 16);
   }
   __device__ static __forceinline__ void store1(void* p, uint64_t i, float f) {
-    static_cast<uint16_t*>(p)[i] = static_cast<uint16_t>(bf16_rne(f));
+    static_cast<uint16_t*>(p)[i] = bf16_rne(f);
   }
 };
 
