@@ -342,13 +342,14 @@ def time_e2e(args, device, stream):
 
         out_stream = torch.cuda.Stream(device)
         bucket_ids = list(range(len(spans)))
+        # Per-bucket order between consecutive steps, so the host link never
+        # idles at a step boundary: a bucket's next copy-in waits only for
+        # its previous kernel (which read those gradients), and its next
+        # kernel only for its previous copy-out (which read those weights).
+        kernel_done = [torch.cuda.Event() for _ in spans]
+        out_done = [torch.cuda.Event() for _ in spans]
 
         def one():
-            # The copies of this step overwrite the gradients only after the
-            # previous step's kernels and its copy-out have finished.
-            for cs in copy_streams:
-                cs.wait_stream(stream)
-            out_stream.wait_stream(stream)
             k = 0
             for b, (lo, hi, ts) in zip(bucket_ids, spans):
                 used = []
@@ -357,20 +358,23 @@ def time_e2e(args, device, stream):
                     k += 1
                     if cs not in used:
                         used.append(cs)
+                        cs.wait_event(kernel_done[b])
                     with torch.cuda.stream(cs):
                         vs.grads[r][lo:hi].copy_(host_g[r][lo:hi], non_blocking=True)
                 # The bucket's replicas arrive on several copy streams: join
                 # them into one, and mark the bucket's tensors on it.
                 for cs in used[1:]:
                     used[0].wait_stream(cs)
+                used[0].wait_event(out_done[b])
                 red.mark_ready_many(ts, used[0])
                 # As soon as this bucket's kernel is done, its updated
                 # weights go back to the host while later buckets come in.
                 red.wait_bucket(b, out_stream)
+                kernel_done[b].record(out_stream)
                 with torch.cuda.stream(out_stream):
                     host_w[lo:hi].copy_(vs.w[lo:hi], non_blocking=True)
+                out_done[b].record(out_stream)
             red.finalize(stream)
-            stream.wait_stream(out_stream)
 
         with torch.cuda.stream(stream):
             for _ in range(3):
@@ -379,8 +383,11 @@ def time_e2e(args, device, stream):
             t0 = torch.cuda.Event(enable_timing=True)
             t1 = torch.cuda.Event(enable_timing=True)
             t0.record(stream)
+            for cs in copy_streams + [out_stream]:
+                cs.wait_stream(stream)
             for _ in range(steps):
                 one()
+            stream.wait_stream(out_stream)
             t1.record(stream)
             torch.cuda.synchronize(device)
         el = t0.elapsed_time(t1) / 1e3
@@ -388,7 +395,8 @@ def time_e2e(args, device, stream):
                 "h2d_bytes_per_step": 2 * vs.n * P_VIT, "d2h_bytes_per_step": 4 * vs.n,
                 "steps": steps, "ms_per_step": el / steps * 1e3,
                 "path": ("ar_reducer_* with per-bucket H2D on 4 copy streams and per-bucket D2H "
-                         "of the updated weights after ar_reducer_wait_bucket")}
+                         "of the updated weights after ar_reducer_wait_bucket; consecutive steps "
+                         "ordered per bucket, not per step")}
     finally:
         if vs is not None:
             vs.close()
