@@ -774,6 +774,7 @@ def run_overlap(args):
 # ------------------------------------------------------------ full sweep
 
 SWEEP_KIB = [4 << (2 * k) for k in range(10)]          # 4 KiB .. 1 GiB per replica
+L2_BYTES = 129 * 10 ** 6                               # GB300 L2
 
 
 def run_full_sweep(args):
@@ -785,6 +786,10 @@ def run_full_sweep(args):
     5 warm-up calls, 20 timed (200 below 1 MiB).  Rows below 1 MiB also
     give the latency of back-to-back calls through the API and as a
     replayed CUDA graph (no flush: the launch cost is what they measure).
+    Rows whose P replicas hold at least twice the L2 also give the rate of
+    20 calls back to back without a flush, where each call pays for the
+    previous call's writes still dirty in L2 (the steady state; a call
+    after the flush does not pay for its own).
     Sum rows repeat on the same buffers (values may overflow to inf; the
     kernels' time does not depend on values).  One JSON line; rank 0 of a
     single process only."""
@@ -811,6 +816,18 @@ def run_full_sweep(args):
                     ts.append((e0, e1))
             torch.cuda.synchronize(device)
         return statistics.median(a.elapsed_time(b) / 1e3 for a, b in ts)
+
+    def back_to_back(call, reps):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                call(stream)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                call(stream)
+            e1.record(stream)
+            torch.cuda.synchronize(device)
+        return e0.elapsed_time(e1) / 1e3 / reps
 
     def graph_of(fn):
         side = torch.cuda.Stream(device)
@@ -867,6 +884,12 @@ def run_full_sweep(args):
                             row = {"op": opname, "P": P, "dtype": name, "KiB_per_replica": kib,
                                    "bytes": nbytes, "us": t * 1e6, "GBps": nbytes / t / 1e9,
                                    "frac": nbytes / t / 1e9 / peak}
+                            if P * n * es >= 2 * L2_BYTES:
+                                # Steady state of repeated calls: each call also
+                                # writes back the previous one's dirty lines.
+                                tb = back_to_back(call, 20)
+                                row["b2b_GBps"] = nbytes / tb / 1e9
+                                row["b2b_frac"] = nbytes / tb / 1e9 / peak
                             if small:
                                 row["api_us"] = 1e6 * median_time(
                                     lambda: call(stream), reps, False)
