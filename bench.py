@@ -914,6 +914,26 @@ def run_full_sweep(args):
                     raise RuntimeError("device status")
             finally:
                 gar.ar_destroy(comm)
+    # The oracle beside it: its in-place Mean all-reduce on the host, as it
+    # stands (one thread), on 4 MiB per replica of the same uniform inputs,
+    # repeated for at least half a second per cell.
+    import oracle
+    import workloads
+    oracle.build()
+    cpu_rows = []
+    for P in (2, 4, 8):
+        for name, es in (("f32", 4), ("bf16", 2)):
+            n = (4 << 20) // es
+            xs = [workloads.replica_values("uniform", name, r, n) for r in range(P)]
+            reps, spent = 0, 0.0
+            while spent < 0.5 or reps == 0:
+                t0 = time.perf_counter()
+                oracle.all_reduce(xs, recv=xs, op=oracle.MEAN)
+                spent += time.perf_counter() - t0
+                reps += 1
+            cpu_rows.append({"op": "mean", "P": P, "dtype": name, "KiB_per_replica": 4096,
+                             "GBps": 2 * P * n * es * reps / spent / 1e9, "reps": reps,
+                             "cores": 1})
     print(json.dumps({
         "mode": "sweep", "metric": METRIC, "peak_GBps": peak, "peak_kind": peak_kind,
         "bytes": "all-reduce 2*P*N*s, broadcast P*N*s (every replica read and written once)",
@@ -921,7 +941,9 @@ def run_full_sweep(args):
                    "(L2 cold and clean); 5 warm-up, "
                    "20 timed (200 below 1 MiB); api_us / graph_us: back-to-back calls, no flush"),
         "seconds": time.perf_counter() - t_start, "clocks": clocks.summary(),
-        "launch_floor": floor, "rows": rows}), flush=True)
+        "launch_floor": floor, "rows": rows,
+        "cpu_oracle": {"kind": "oracle", "cores": 1, "host_cpus": os.cpu_count(),
+                       "rows": cpu_rows}}), flush=True)
 
 
 # ------------------------------------------------------------------ cases
