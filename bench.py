@@ -48,7 +48,7 @@ WORKLOAD = ("vit_b16_ddp_step: P=8 replicas x 86,567,656 bf16 grads, 8 x 25 MiB 
             "Mean all-reduce fused with SGD momentum (fp32 master), write-back")
 P_VIT = 8
 CAP = 25 << 20
-KERNEL_SOURCES = ["gar_device.cuh", "gar_kernels.cuh"]
+KERNEL_SOURCES = ["gar_device.cuh", "gar_kernels.cuh", "gar_launch.h", "gar_reduce.inc"]
 
 
 def parse():

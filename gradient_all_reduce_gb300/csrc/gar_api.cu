@@ -130,14 +130,12 @@ ar_status_t ar_init(ar_comm_t* comm, int nranks, int cuda_device, ar_op_t defaul
   if (env != nullptr && std::strcmp(env, "tma") == 0) c->kernel_mode = 2;
   env = std::getenv("GAR_PDL");
   c->pdl = !(env != nullptr && std::strcmp(env, "0") == 0);
-  // All-gather and broadcast run on the bulk-store copy kernel unless
-  // GAR_COPY=ldg asks for the register-staged one (measured on GB300 within
-  // 2 % of each other; both DRAM-bound at 5.8-6.1 TB/s for 7 destinations).
+  // All-gather and broadcast run on the register-staged copy kernel (one
+  // CTA per tile) unless GAR_COPY=tma asks for the bulk-store pipeline
+  // (measured on GB300: 0.95-1.04 against 0.86-0.91 of the copy peak at
+  // >= 256 MiB per replica).
   env = std::getenv("GAR_COPY");
-  c->copy_tma = !(env != nullptr && std::strcmp(env, "ldg") == 0);
-  env = std::getenv("GAR_CTAS_PER_SM");
-  c->ctas_per_sm = env != nullptr ? std::atoi(env) : -1;
-  if (c->ctas_per_sm < -1 || c->ctas_per_sm > 32) c->ctas_per_sm = -1;
+  c->copy_tma = env != nullptr && std::strcmp(env, "tma") == 0;
   if (cudaMalloc(&c->d_status, sizeof(uint32_t)) != cudaSuccess) {
     delete c;
     return AR_ERR_CUDA;

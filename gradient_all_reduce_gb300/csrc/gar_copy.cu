@@ -33,7 +33,7 @@ cudaError_t launch_copy(const LaunchCtx& ctx, const SegTable<Cap>& tab) {
     return launch_ex(ctx, k, grid, 32, smem, tab);
   }
   auto* k = &k_copy<Cap>;
-  const unsigned grid = grid_for(tab.ntiles, resident_ctas(reinterpret_cast<const void*>(k)) * ctx.num_sms);
+  const unsigned grid = grid_per_tile(tab.ntiles);
   if (grid == 0) return cudaSuccess;
   return launch_ex(ctx, k, grid, kThreads, 0, tab);
 }

@@ -25,8 +25,7 @@ struct ar_comm_s {
   bool check_pointers;  // validate every pointer against its allocation
   int kernel_mode;      // 0 = default (k_reduce), 1 = k_reduce, 2 = bulk-copy k_reduce_tma
   bool pdl;             // programmatic dependent launch between consecutive kernels
-  int ctas_per_sm;      // GAR_CTAS_PER_SM: k_reduce CTAs per SM (-1 = default, 0 = occupancy)
-  bool copy_tma;        // all-gather / broadcast on the bulk-store k_copy_tma (default)
+  bool copy_tma;        // all-gather / broadcast on the bulk-store k_copy_tma (GAR_COPY=tma)
 };
 
 namespace gar_host {
@@ -250,23 +249,11 @@ inline uint32_t vec_flag(void* const* ptrs, int n, float* const* extra = nullptr
 
 inline ar_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? AR_OK : AR_ERR_CUDA; }
 
-// Grid planning of a k_reduce launch.  GAR_CTAS_PER_SM overrides; by
-// default the fused-SGD kernel plans 3 CTAs per SM when it runs alone
-// (measured on GB300: 0.877 of the copy peak per launch against 0.815 at full
-// occupancy) and full occupancy when the reducer pipelines buckets on two
-// streams (each kernel then fills the GPU and the next one starts as it
-// drains: 6660 against 6428 GB/s per step).
-inline int reduce_cta_cap(const ar_comm_s* c, bool sgd, bool pipelined) {
-  if (c->ctas_per_sm >= 0) return c->ctas_per_sm;
-  return sgd && !pipelined ? 3 : 0;
-}
-
 template <class Cap>
 inline ar_status_t run_reduce(const ar_comm_s* c, ar_dtype_t dt, bool sgd, const SegTable<Cap>& t,
-                              cudaStream_t st, bool pipelined = false) {
+                              cudaStream_t st) {
   if (t.ntiles == 0) return AR_OK;
-  const gar::LaunchCtx ctx{c->device, c->num_sms, st, t.stages > 0, c->pdl,
-                           reduce_cta_cap(c, sgd, pipelined)};
+  const gar::LaunchCtx ctx{c->device, c->num_sms, st, t.stages > 0, c->pdl};
   return from_cuda(dt == AR_F32 ? gar::launch_reduce_f32<Cap>(ctx, sgd, t)
                                 : gar::launch_reduce_bf16<Cap>(ctx, sgd, t));
 }

@@ -72,6 +72,21 @@ struct SegTable {
   void* ptr[Cap::kPtr];           // segment s: ptr[s*stride + 0 .. stride)
 };
 
+// The segment that holds `tile`: the last s >= from with tile0[s] <= tile
+// (tile0 is non-decreasing, tile0[nseg] = ntiles; an empty segment's
+// successor starts at the same tile, so empty segments are never chosen).
+// A CTA may start at any tile, so this is a binary search, not a walk.
+template <class Cap>
+__device__ __forceinline__ uint32_t seg_of(const SegTable<Cap>& a, uint32_t tile, uint32_t from) {
+  uint32_t lo = from, hi = a.nseg;  // tile0[lo] <= tile < tile0[hi]
+  while (hi - lo > 1) {
+    const uint32_t mid = (lo + hi) >> 1;
+    if (a.tile0[mid] <= tile) lo = mid;
+    else hi = mid;
+  }
+  return lo;
+}
+
 // --------------------------------------------------------------- reduce
 
 // SGD on one vector's E elements, w and v already loaded (E / 4 float4
@@ -121,7 +136,7 @@ __global__ void __launch_bounds__(kThreads)
   griddep_wait();
   uint32_t s = 0;
   for (uint32_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
-    while (tile >= a.tile0[s + 1]) ++s;  // tiles are visited in increasing order
+    s = seg_of(a, tile, s);
     const uint64_t n = a.numel[s];
     void* const* seg = a.ptr + uint64_t(s) * a.stride;
     void* const* dst = seg + a.dst_off;
@@ -235,7 +250,7 @@ __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTa
   griddep_wait();
   uint32_t s = 0;
   for (uint32_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
-    while (tile >= a.tile0[s + 1]) ++s;
+    s = seg_of(a, tile, s);
     const uint64_t nbytes = a.numel[s];
     void* const* seg = a.ptr + uint64_t(s) * a.stride;
     const void* src = seg[0];
@@ -309,7 +324,7 @@ __global__ void __launch_bounds__(kThreads) k_accumulate(const __grid_constant__
   const bool first = a.first != 0;
   uint32_t s = 0;
   for (uint32_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
-    while (tile >= a.tile0[s + 1]) ++s;
+    s = seg_of(a, tile, s);
     const uint64_t n = a.numel[s];
     const void* g = a.ptr[uint64_t(s) * a.stride];
     float* acc = static_cast<float*>(a.ptr[uint64_t(s) * a.stride + 1]);
@@ -385,7 +400,7 @@ __global__ void __launch_bounds__(kThreads)
   griddep_wait();
   uint32_t s = 0;
   for (uint32_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
-    while (tile >= a.tile0[s + 1]) ++s;
+    s = seg_of(a, tile, s);
     const uint64_t n = a.numel[s];
     void* const* seg = a.ptr + uint64_t(s) * a.stride;
     const uint64_t lt = tile - a.tile0[s];

@@ -86,11 +86,11 @@ ar_status_t launch_bucket(ar_reducer_s* r, int b) {
     if (cudaStreamWaitEvent(s, r->join, 0) != cudaSuccess) return AR_ERR_CUDA;
   }
   for (const auto& t : bk.small) {
-    ar_status_t st = run_reduce(r->comm, r->dtype, r->sgd, t, s, true);
+    ar_status_t st = run_reduce(r->comm, r->dtype, r->sgd, t, s);
     if (st != AR_OK) return st;
   }
   for (const auto& t : bk.large) {
-    ar_status_t st = run_reduce(r->comm, r->dtype, r->sgd, t, s, true);
+    ar_status_t st = run_reduce(r->comm, r->dtype, r->sgd, t, s);
     if (st != AR_OK) return st;
   }
   if (cudaEventRecord(r->done[k], s) != cudaSuccess) return AR_ERR_CUDA;
