@@ -296,7 +296,9 @@ __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTa
 // the last, no communication): segment = one (tensor, rank) pair, ptr[0] =
 // the gradient (D), ptr[1] = its fp32 accumulator; per element, with
 // s = fl(scale * g):  acc = first ? s : fl(acc + s).
-constexpr int kAccUnroll = 4;
+// Vectors per thread: 2 measured best on GB300 (one 25 MiB bf16 bucket, P = 8:
+// later micro-batches 1.03 of the copy peak against 1.02 with 4 and 1.00 with 8).
+constexpr int kAccUnroll = 2;
 
 template <class D>
 __device__ __forceinline__ void acc_vec(const uint4& gv, float4 (&a4)[D::kElems / 4], float* acc,
