@@ -579,6 +579,9 @@ def time_sweep(device, stream):
                 gar.ar_syncbn_stats(comm, sums, sq, [1000] * P, means, invs, C, 1e-5,
                                     stream if s is None else s)
             t_api = timed(call, 200, flush_between=False)
+            prep = gar.PreparedCall("ar_syncbn_stats", comm, sums, sq, [1000] * P, means, invs,
+                                    C, 1e-5)
+            t_prep = timed(lambda: prep(stream), 200, flush_between=False)
             side = torch.cuda.Stream(device)
             side.wait_stream(stream)
             with torch.cuda.stream(side):
@@ -588,7 +591,8 @@ def time_sweep(device, stream):
             with torch.cuda.graph(graph):
                 call(torch.cuda.current_stream())
             t_graph = timed(graph.replay, 200, flush_between=False)
-            res.append({"P": P, "channels": C, "api_us": t_api * 1e6, "graph_us": t_graph * 1e6})
+            res.append({"P": P, "channels": C, "api_us": t_api * 1e6,
+                        "prepared_us": t_prep * 1e6, "graph_us": t_graph * 1e6})
         out["syncbn_stats_latency"] = res
     finally:
         gar.ar_destroy(comm)

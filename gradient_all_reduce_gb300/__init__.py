@@ -379,10 +379,11 @@ class Reducer:
 
 class PreparedCall:
     """One of the flat collectives (``ar_all_reduce``, ``ar_reduce_scatter``,
-    ``ar_all_gather``, ``ar_broadcast``, ``ar_sharded_sgd_step``) with its
-    pointer arrays marshalled once, for a loop that repeats the same call on
-    the same buffers: ``PreparedCall("ar_all_reduce", comm, send, recv,
-    count, dtype, op)(stream)``.  The library still validates every call."""
+    ``ar_all_gather``, ``ar_broadcast``, ``ar_sharded_sgd_step``,
+    ``ar_syncbn_stats``) with its pointer arrays marshalled once, for a loop
+    that repeats the same call on the same buffers: ``PreparedCall(
+    "ar_all_reduce", comm, send, recv, count, dtype, op)(stream)``.  The
+    library still validates every call."""
 
     _LAYOUT = {
         "ar_all_reduce": ("comm", "ptrs", "ptrs", "size", "int", "int"),
@@ -391,6 +392,7 @@ class PreparedCall:
         "ar_broadcast": ("comm", "ptrs", "size", "int", "int"),
         "ar_sharded_sgd_step": ("comm", "ptrs", "ptrs", "ptrs", "ptrs", "size", "int", "int",
                                 "float", "float"),
+        "ar_syncbn_stats": ("comm", "ptrs", "ptrs", "u64s", "ptrs", "ptrs", "size", "float"),
     }
 
     def __init__(self, name: str, *args):
@@ -402,6 +404,10 @@ class PreparedCall:
         for kind, a in zip(kinds, args):
             if kind == "ptrs":
                 arr = _ptr_array(a)
+                self._keep.append(arr)
+                conv.append(arr)
+            elif kind == "u64s":
+                arr = (ctypes.c_uint64 * max(len(a), 1))(*[int(x) for x in a])
                 self._keep.append(arr)
                 conv.append(arr)
             elif kind == "float":

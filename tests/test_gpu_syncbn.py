@@ -69,3 +69,31 @@ def test_syncbn_end_to_end_whole_batch():
     bn = torch.nn.functional.batch_norm(whole, None, None, training=True, eps=1e-5)
     mine = (whole - means[0].double()[None, :, None, None]) * invs[0].double()[None, :, None, None]
     assert float((mine - bn).abs().max()) <= 1e-4
+
+
+def test_prepared_syncbn_equals_direct_call():
+    """ar_syncbn_stats through PreparedCall (pointer and count arrays
+    marshalled once, called twice) gives the direct call's bits."""
+    P, C = 8, 512
+    rng = np.random.default_rng(77)
+    counts = [int(c) for c in rng.integers(1, 5000, size=P)]
+    sums = [np.float32(rng.normal(0, 1, C) * c) for c in counts]
+    sq = [np.float32(np.abs(rng.normal(1, 0.5, C)) * c + s * s / c) for s, c in zip(sums, counts)]
+    d_s = [torch.from_numpy(x).to(dev()) for x in sums]
+    d_q = [torch.from_numpy(x).to(dev()) for x in sq]
+    direct = [[torch.empty(C, device=dev()) for _ in range(P)] for _ in range(2)]
+    prepared = [[torch.empty(C, device=dev()) for _ in range(P)] for _ in range(2)]
+    comm = gar.ar_init(P, 0, gar.AR_SUM)
+    try:
+        gar.ar_syncbn_stats(comm, d_s, d_q, counts, direct[0], direct[1], C, 1e-5)
+        call = gar.PreparedCall("ar_syncbn_stats", comm, d_s, d_q, counts, prepared[0],
+                                prepared[1], C, 1e-5)
+        call()
+        call()
+        torch.cuda.synchronize()
+        assert gar.ar_get_async_error(comm) == gar.AR_OK
+    finally:
+        gar.ar_destroy(comm)
+    for k in range(2):
+        for r in range(P):
+            assert_bits_equal(to_np(prepared[k][r]), to_np(direct[k][r]), f"output {k} rank {r}")
