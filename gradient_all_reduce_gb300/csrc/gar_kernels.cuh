@@ -295,14 +295,17 @@ __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTa
 // DDP's no_sync gradient accumulation.  k_accumulate (a micro-batch before
 // the last, no communication): segment = one (tensor, rank) pair, ptr[0] =
 // the gradient (D), ptr[1] = its fp32 accumulator; per element, with
-// s = fl(scale * g):  acc = first ? s : fl(acc + s).
-// Vectors per thread: 2 measured best on GB300 (one 25 MiB bf16 bucket, P = 8:
-// later micro-batches 1.03 of the copy peak against 1.02 with 4 and 1.00 with 8).
+// s = fl(scale * g):  acc = first ? s : fl(acc + s).  The first micro-batch
+// (no accumulator to read) is a kernel of its own, FIRST = true: 31 registers
+// instead of 36, so 8 CTAs per SM, and 0.92 of the copy peak on GB300 against
+// 0.85 as a runtime branch of one kernel (one 25 MiB bf16 bucket, P = 8).
+// Vectors per thread: 2 measured best for both (later micro-batches 1.03
+// against 1.02 with 4 and 1.00 with 8; the first 0.92 against 0.78 and 0.84).
 constexpr int kAccUnroll = 2;
 
-template <class D>
+template <class D, bool FIRST>
 __device__ __forceinline__ void acc_vec(const uint4& gv, float4 (&a4)[D::kElems / 4], float* acc,
-                                        uint64_t e0, float scale, bool first) {
+                                        uint64_t e0, float scale) {
   float g[D::kElems];
   D::unpack(gv, g);
 #pragma unroll
@@ -311,19 +314,19 @@ __device__ __forceinline__ void acc_vec(const uint4& gv, float4 (&a4)[D::kElems 
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const float sv = __fmul_rn(scale, g[4 * q + k]);
-      av[k] = first ? sv : __fadd_rn(av[k], sv);
+      av[k] = FIRST ? sv : __fadd_rn(av[k], sv);
     }
     st_f4(acc + e0 + 4 * q, a4[q]);
   }
 }
 
-template <class D, class Cap>
+template <class D, class Cap, bool FIRST>
 __global__ void __launch_bounds__(kThreads) k_accumulate(const __grid_constant__ SegTable<Cap> a) {
   constexpr int E = D::kElems;
-  constexpr uint64_t kTileVec = uint64_t(kAccUnroll) * kThreads;
+  constexpr int U = kAccUnroll;
+  constexpr uint64_t kTileVec = uint64_t(U) * kThreads;
   griddep_launch_dependents();
   griddep_wait();
-  const bool first = a.first != 0;
   uint32_t s = 0;
   for (uint32_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
     s = seg_of(a, tile, s);
@@ -335,20 +338,20 @@ __global__ void __launch_bounds__(kThreads) k_accumulate(const __grid_constant__
       const uint64_t nvec = n / E;
       const uint64_t v0 = lt * kTileVec + threadIdx.x;
       // All gradient and accumulator loads first, then the stores.
-      uint4 x[kAccUnroll];
-      float4 a4[kAccUnroll][E / 4];
+      uint4 x[U];
+      float4 a4[U][E / 4];
 #pragma unroll
-      for (int u = 0; u < kAccUnroll; ++u) {
+      for (int u = 0; u < U; ++u) {
         const uint64_t vi = v0 + uint64_t(u) * kThreads;
         if (vi < nvec) {
           x[u] = ld_stream(static_cast<const uint4*>(g) + vi);
 #pragma unroll
           for (int q = 0; q < E / 4; ++q)
-            a4[u][q] = first ? make_float4(0.f, 0.f, 0.f, 0.f) : ld_f4(acc + vi * E + 4 * q);
+            a4[u][q] = FIRST ? make_float4(0.f, 0.f, 0.f, 0.f) : ld_f4(acc + vi * E + 4 * q);
         }
       }
 #pragma unroll
-      for (int u = 0; u < kAccUnroll; ++u) {
+      for (int u = 0; u < U; ++u) {
         if (v0 + uint64_t(u) * kThreads < nvec) {
           reg_fence(x[u]);
 #pragma unroll
@@ -356,15 +359,15 @@ __global__ void __launch_bounds__(kThreads) k_accumulate(const __grid_constant__
         }
       }
 #pragma unroll
-      for (int u = 0; u < kAccUnroll; ++u) {
+      for (int u = 0; u < U; ++u) {
         const uint64_t vi = v0 + uint64_t(u) * kThreads;
-        if (vi < nvec) acc_vec<D>(x[u], a4[u], acc, vi * E, a.scale, first);
+        if (vi < nvec) acc_vec<D, FIRST>(x[u], a4[u], acc, vi * E, a.scale);
       }
       if (lt + 1 == a.tile0[s + 1] - a.tile0[s]) {
         const uint64_t i = nvec * E + threadIdx.x;
         if (i < n) {
           const float sv = __fmul_rn(a.scale, D::load1(g, i));
-          acc[i] = first ? sv : __fadd_rn(acc[i], sv);
+          acc[i] = FIRST ? sv : __fadd_rn(acc[i], sv);
         }
       }
     } else {
@@ -373,7 +376,7 @@ __global__ void __launch_bounds__(kThreads) k_accumulate(const __grid_constant__
         const uint64_t i = e0 + k;
         if (i >= n) break;
         const float sv = __fmul_rn(a.scale, D::load1(g, i));
-        acc[i] = first ? sv : __fadd_rn(acc[i], sv);
+        acc[i] = FIRST ? sv : __fadd_rn(acc[i], sv);
       }
     }
   }
