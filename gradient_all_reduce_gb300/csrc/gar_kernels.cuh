@@ -28,14 +28,14 @@ __host__ __device__ constexpr int unroll_for(int PT) {
   return PT == 0 ? 1 : (PT <= 4 ? 4 : (PT <= 8 ? 2 : 1));
 }
 // With the fused SGD step each vector also carries its fp32 master weights
-// and momentum (2 x E floats), all loaded up front: fewer vectors per thread.
-#ifndef GAR_SGD_UNROLL_P8
-#define GAR_SGD_UNROLL_P8 1
-#endif
-__host__ __device__ constexpr int unroll_for_sgd(int PT) {
-  return PT == 0 ? 1 : (PT <= 4 ? 2 : (PT <= 8 ? GAR_SGD_UNROLL_P8 : 1));
-}
-constexpr int kCopyUnroll = 4;
+// and momentum (2 x E floats), all loaded up front: 2 vectors per thread for
+// P = 2, 4, 8 (measured on GB300 for P = 8 on the ViT-B/16 buckets: 0.982 of
+// the copy peak back to back against 0.978 with 1).
+__host__ __device__ constexpr int unroll_for_sgd(int PT) { return PT == 0 ? 1 : 2; }
+// Copy vectors per thread: 2 measured best on GB300 (broadcast, P = 8, 64 MiB
+// to 1 GiB per replica: 0.978-0.995 of the copy peak against 0.964-0.991 with
+// 4 and 0.934-0.987 with 8).
+constexpr int kCopyUnroll = 2;
 
 // Segment table capacities: a flat all-reduce (one segment) uses a 400-byte
 // parameter block, small launches (<= 16 segments) about 5 KB, large ones
