@@ -69,6 +69,10 @@ def parse():
     ap.add_argument("--case", choices=["ar", "rs", "ag", "bc", "zero1", "acc", "syncbn"],
                     help="time one collective alone (P=8, 256 MiB per replica; ViT-sized for "
                          "zero1/acc) and print its GB/s; for profiling single kernels")
+    ap.add_argument("--case-ranks", type=int, default=8, choices=[2, 4, 8],
+                    help="P for --case ar/rs/ag/bc")
+    ap.add_argument("--case-dtype", choices=["f32", "bf16"], default="f32",
+                    help="element type for --case ar/rs/ag/bc")
     return ap.parse_args()
 
 
@@ -954,34 +958,38 @@ def run_full_sweep(args):
 
 def run_case(args):
     """One collective alone, K timed calls after W warm-up calls, one JSON
-    line: the workloads of the sweep (P = 8, fp32, 256 MiB per replica) or,
-    for zero1 and acc, of the ViT-B/16 gradient set (bf16)."""
+    line: 256 MiB per replica for ar / rs / ag / bc (P and the element type
+    from --case-ranks and --case-dtype; P = 8, fp32 by default), the
+    ViT-B/16 gradient set (bf16, P = 8) for zero1 and acc."""
     import torch
     import gradient_all_reduce_gb300 as gar
     from workloads import gpu as wgpu
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
     stream = torch.cuda.current_stream()
-    P = 8
+    flat = args.case in ("ar", "rs", "ag", "bc")
+    P = args.case_ranks if flat else 8
     comm = gar.ar_init(P, 0, gar.AR_MEAN)
     try:
-        if args.case in ("ar", "rs", "ag", "bc"):
-            n = (256 << 20) // 4
-            xs = [torch.empty(n, device=device) for _ in range(P)]
+        if flat:
+            es, tdt, dt = ((4, torch.float32, gar.AR_F32) if args.case_dtype == "f32"
+                           else (2, torch.bfloat16, gar.AR_BF16))
+            n = (256 << 20) // es
+            xs = [torch.empty(n, dtype=tdt, device=device) for _ in range(P)]
             for r, x in enumerate(xs):
                 wgpu.fill(x, "uniform", r)
             sh = n // P
-            rs = [torch.empty(sh, device=device) for _ in range(P)]
+            rs = [torch.empty(sh, dtype=tdt, device=device) for _ in range(P)]
             ins = [x[r * sh:(r + 1) * sh] for r, x in enumerate(xs)]
             fn, nbytes = {
-                "ar": (lambda: gar.ar_all_reduce(comm, xs, xs, n, gar.AR_F32, gar.AR_MEAN, stream),
-                       2 * P * n * 4),
-                "rs": (lambda: gar.ar_reduce_scatter(comm, xs, rs, n, gar.AR_F32, gar.AR_SUM, stream),
-                       (P + 1) * n * 4),
-                "ag": (lambda: gar.ar_all_gather(comm, ins, xs, n, gar.AR_F32, stream), P * n * 4),
-                "bc": (lambda: gar.ar_broadcast(comm, xs, n, gar.AR_F32, 0, stream), P * n * 4),
+                "ar": (lambda: gar.ar_all_reduce(comm, xs, xs, n, dt, gar.AR_MEAN, stream),
+                       2 * P * n * es),
+                "rs": (lambda: gar.ar_reduce_scatter(comm, xs, rs, n, dt, gar.AR_SUM, stream),
+                       (P + 1) * n * es),
+                "ag": (lambda: gar.ar_all_gather(comm, ins, xs, n, dt, stream), P * n * es),
+                "bc": (lambda: gar.ar_broadcast(comm, xs, n, dt, 0, stream), P * n * es),
             }[args.case]
-            what = f"P=8 fp32 256 MiB per replica"
+            what = f"P={P} {args.case_dtype} 256 MiB per replica"
         elif args.case == "zero1":
             n = -(-86_567_656 // (P * 8)) * (P * 8)
             g = [torch.empty(n, dtype=torch.bfloat16, device=device) for _ in range(P)]
