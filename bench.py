@@ -228,9 +228,16 @@ class VitStep:
 
 
 def kernel_source_sha() -> str:
+    """sha256[:16] of the bucket kernel's sources with comments and blank
+    space removed: an edit that changes no code keeps the committed ncu
+    figures valid, any change of code does not."""
+    import re
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        h.update((ROOT / "gradient_all_reduce_gb300" / "csrc" / name).read_bytes())
+        text = (ROOT / "gradient_all_reduce_gb300" / "csrc" / name).read_text()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -12,9 +12,10 @@
 // source shard; broadcast: one segment from the root).
 //
 // Work is cut into tiles of kThreads * U 16-byte vectors of one segment.
-// CTAs are persistent: CTA b takes tiles b, b + G, b + 2G, ...; the host
-// picks G so that every CTA gets the same number of tiles (to within one).
-// The segment table travels by value in the kernel's parameter space
+// The host launches one CTA per tile (grid_per_tile), so the block
+// scheduler hands the tiles out in order; the loops still stride by the
+// grid, which covers a table with more tiles than a grid may hold.  The
+// segment table travels by value in the kernel's parameter space
 // (__grid_constant__), so a launch needs no device-side table and no copy.
 #pragma once
 
