@@ -126,6 +126,47 @@ def test_vit_b16_bucketed_sgd_full_size_sampled(path):
         gar.ar_destroy(comm)
 
 
+def test_vit_b16_step_as_benchmarked():
+    """The ViT-B/16 step exactly as bench.py times it: its own VitStep
+    object (the same buffers, seeds and prepared calls), two steps through
+    the reducer (marks in reverse order, buckets on two streams), then one
+    step of the same 8 bucket calls back to back on one stream.  Sampled
+    outputs equal three oracle steps bit for bit; every replica holds the
+    same gradient."""
+    import bench
+    P = bench.P_VIT
+    comm = gar.ar_init(P, 0, gar.AR_MEAN)
+    vs = None
+    try:
+        vs = bench.VitStep(comm, dev())
+        n = vs.n
+        assert n == workloads.VIT_B16_PARAMS and len(vs.calls) == 8
+        idx = sample_indices(n, 200_000, 5, extra=[int(o) for o in vs.offs[1:-1]] +
+                             [int(o) - 1 for o in vs.offs[1:]])
+        cols = host_replicas(P, 0, "bf16", "normal", workloads.VIT_GRAD_SEED,
+                             std=workloads.VIT_GRAD_STD, idx=idx)
+        hw = workloads.normal_f32(workloads.VIT_MASTER_SEED, 0, std=workloads.VIT_MASTER_STD,
+                                  idx=idx)
+        hv = np.zeros(idx.size, np.float32)
+        stream = torch.cuda.Stream(dev())
+        for step, run in enumerate((vs.step, vs.step, vs.step_serial)):
+            with torch.cuda.stream(stream):
+                run(stream)
+            torch.cuda.synchronize()
+            assert gar.ar_get_async_error(comm) == gar.AR_OK
+            oracle.bucket_all_reduce([cols], op=oracle.MEAN, sgd=(0.1, 0.9, [hw], [hv], 1))
+            assert_bits_equal(gather(vs.w, idx), hw, f"step {step} master")
+            assert_bits_equal(gather(vs.v, idx), hv, f"step {step} momentum")
+            for r in (0, 5, P - 1):
+                assert_bits_equal(gather(vs.grads[r], idx), cols[r], f"step {step} grad {r}")
+            for r in range(1, P):
+                assert bits_equal_device(vs.grads[r], vs.grads[0]), r
+    finally:
+        if vs is not None:
+            vs.close()
+        gar.ar_destroy(comm)
+
+
 def test_vit_small_cap_full_check(path):
     """The same step with 4 MiB buckets (many more, smaller launches) on the
     first 12,000,000 ViT elements, checked against the oracle on every
