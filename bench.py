@@ -340,76 +340,91 @@ def time_vit(args, device, stream, world):
         gar.ar_destroy(comm)
 
 
-def time_e2e(args, device, stream):
-    """The same step from pinned host buffers, through the public API: each
+class E2EStep:
+    """The ViT step from pinned host buffers, through the public API: each
     bucket's gradient replicas are copied in (one copy per replica, spread
     over four copy streams) and its tensors marked ready on the copy
     streams, so bucket b's kernel runs while bucket b+1 is still crossing
     the host link; each bucket's updated fp32 master weights are copied out
-    as soon as its kernel is done.  Bytes per step: the P bf16 gradient
-    replicas in, the weights out."""
+    to ``host_w`` as soon as its kernel is done.  Bytes per step: the P
+    bf16 gradient replicas in, the weights out.
+
+    Consecutive steps are ordered per bucket, so the host link never idles
+    at a step boundary: a bucket's next copy-in waits only for its previous
+    kernel (which read those gradients), and its next kernel only for its
+    previous copy-out (which read those weights)."""
+
+    def __init__(self, vs, device):
+        import torch
+        self.vs = vs
+        self.host_g = [g.cpu().pin_memory() for g in vs.grads]
+        self.host_w = torch.empty(vs.n, dtype=torch.float32).pin_memory()
+        self.copy_streams = [torch.cuda.Stream(device) for _ in range(4)]
+        self.out_stream = torch.cuda.Stream(device)
+        o = vs.offs
+        self.spans = [(int(o[min(b)]), int(o[max(b) + 1]), b) for b in vs.buckets]
+        self.kernel_done = [torch.cuda.Event() for _ in self.spans]
+        self.out_done = [torch.cuda.Event() for _ in self.spans]
+
+    def start(self, stream):
+        """Order the copy streams after ``stream`` (the start of a region)."""
+        for cs in self.copy_streams + [self.out_stream]:
+            cs.wait_stream(stream)
+
+    def step(self, stream):
+        import torch
+        vs, red = self.vs, self.vs.reducer
+        k = 0
+        for b, (lo, hi, ts) in enumerate(self.spans):
+            used = []
+            for r in range(P_VIT):
+                cs = self.copy_streams[k % len(self.copy_streams)]
+                k += 1
+                if cs not in used:
+                    used.append(cs)
+                    cs.wait_event(self.kernel_done[b])
+                with torch.cuda.stream(cs):
+                    vs.grads[r][lo:hi].copy_(self.host_g[r][lo:hi], non_blocking=True)
+            # The bucket's replicas arrive on several copy streams: join them
+            # into one, and mark the bucket's tensors on it.
+            for cs in used[1:]:
+                used[0].wait_stream(cs)
+            used[0].wait_event(self.out_done[b])
+            red.mark_ready_many(ts, used[0])
+            red.wait_bucket(b, self.out_stream)
+            self.kernel_done[b].record(self.out_stream)
+            with torch.cuda.stream(self.out_stream):
+                self.host_w[lo:hi].copy_(vs.w[lo:hi], non_blocking=True)
+            self.out_done[b].record(self.out_stream)
+        red.finalize(stream)
+
+    def finish(self, stream):
+        """Order ``stream`` after every copy-out issued so far."""
+        stream.wait_stream(self.out_stream)
+
+
+def time_e2e(args, device, stream):
+    """The ViT step end to end from pinned host buffers (E2EStep), K steps
+    under one event pair after 3 warm-up steps."""
     import torch
     import gradient_all_reduce_gb300 as gar
     comm = gar.ar_init(P_VIT, device.index, gar.AR_MEAN)
     vs = None
     try:
         vs = VitStep(comm, device)
-        host_g = [g.cpu().pin_memory() for g in vs.grads]
-        host_w = torch.empty(vs.n, dtype=torch.float32).pin_memory()
-        copy_streams = [torch.cuda.Stream(device) for _ in range(4)]
-        o = vs.offs
-        spans = [(int(o[min(b)]), int(o[max(b) + 1]), b) for b in vs.buckets]
+        e2e = E2EStep(vs, device)
         steps = max(3, min(args.steps, 50))
-        red = vs.reducer
-
-        out_stream = torch.cuda.Stream(device)
-        bucket_ids = list(range(len(spans)))
-        # Per-bucket order between consecutive steps, so the host link never
-        # idles at a step boundary: a bucket's next copy-in waits only for
-        # its previous kernel (which read those gradients), and its next
-        # kernel only for its previous copy-out (which read those weights).
-        kernel_done = [torch.cuda.Event() for _ in spans]
-        out_done = [torch.cuda.Event() for _ in spans]
-
-        def one():
-            k = 0
-            for b, (lo, hi, ts) in zip(bucket_ids, spans):
-                used = []
-                for r in range(P_VIT):
-                    cs = copy_streams[k % len(copy_streams)]
-                    k += 1
-                    if cs not in used:
-                        used.append(cs)
-                        cs.wait_event(kernel_done[b])
-                    with torch.cuda.stream(cs):
-                        vs.grads[r][lo:hi].copy_(host_g[r][lo:hi], non_blocking=True)
-                # The bucket's replicas arrive on several copy streams: join
-                # them into one, and mark the bucket's tensors on it.
-                for cs in used[1:]:
-                    used[0].wait_stream(cs)
-                used[0].wait_event(out_done[b])
-                red.mark_ready_many(ts, used[0])
-                # As soon as this bucket's kernel is done, its updated
-                # weights go back to the host while later buckets come in.
-                red.wait_bucket(b, out_stream)
-                kernel_done[b].record(out_stream)
-                with torch.cuda.stream(out_stream):
-                    host_w[lo:hi].copy_(vs.w[lo:hi], non_blocking=True)
-                out_done[b].record(out_stream)
-            red.finalize(stream)
-
         with torch.cuda.stream(stream):
             for _ in range(3):
-                one()
+                e2e.step(stream)
             torch.cuda.synchronize(device)
             t0 = torch.cuda.Event(enable_timing=True)
             t1 = torch.cuda.Event(enable_timing=True)
             t0.record(stream)
-            for cs in copy_streams + [out_stream]:
-                cs.wait_stream(stream)
+            e2e.start(stream)
             for _ in range(steps):
-                one()
-            stream.wait_stream(out_stream)
+                e2e.step(stream)
+            e2e.finish(stream)
             t1.record(stream)
             torch.cuda.synchronize(device)
         el = t0.elapsed_time(t1) / 1e3

@@ -167,6 +167,52 @@ def test_vit_b16_step_as_benchmarked():
         gar.ar_destroy(comm)
 
 
+def test_vit_b16_e2e_pipelined_steps():
+    """The end-to-end step bench.py times (E2EStep): gradients copied in
+    from pinned host memory bucket by bucket, the reducer, the updated
+    weights copied out, consecutive steps ordered per bucket only.  After
+    four steps issued back to back, the weights copied to the host and the
+    gradient replicas equal four oracle steps (each on the original
+    gradients, which every step copies in afresh), sampled bit for bit: no
+    copy-in overtook a kernel that still read its bucket, and no kernel
+    overtook a copy-out."""
+    import bench
+    P = bench.P_VIT
+    comm = gar.ar_init(P, 0, gar.AR_MEAN)
+    vs = None
+    try:
+        vs = bench.VitStep(comm, dev())
+        e2e = bench.E2EStep(vs, dev())
+        n = vs.n
+        idx = sample_indices(n, 200_000, 6, extra=[int(o) for o in vs.offs[1:-1]] +
+                             [int(o) - 1 for o in vs.offs[1:]])
+        cols0 = host_replicas(P, 0, "bf16", "normal", workloads.VIT_GRAD_SEED,
+                              std=workloads.VIT_GRAD_STD, idx=idx)
+        hw = workloads.normal_f32(workloads.VIT_MASTER_SEED, 0, std=workloads.VIT_MASTER_STD,
+                                  idx=idx)
+        hv = np.zeros(idx.size, np.float32)
+        stream = torch.cuda.Stream(dev())
+        with torch.cuda.stream(stream):
+            e2e.start(stream)
+            for _ in range(4):
+                e2e.step(stream)
+            e2e.finish(stream)
+        torch.cuda.synchronize()
+        assert gar.ar_get_async_error(comm) == gar.AR_OK
+        for _ in range(4):
+            cols = [c.copy() for c in cols0]
+            oracle.bucket_all_reduce([cols], op=oracle.MEAN, sgd=(0.1, 0.9, [hw], [hv], 1))
+        it = torch.from_numpy(idx.astype(np.int64))
+        assert_bits_equal(e2e.host_w[it].numpy(), hw, "weights copied out")
+        assert_bits_equal(gather(vs.v, idx), hv, "momentum")
+        for r in (0, 4, P - 1):
+            assert_bits_equal(gather(vs.grads[r], idx), cols[r], f"grad {r}")
+    finally:
+        if vs is not None:
+            vs.close()
+        gar.ar_destroy(comm)
+
+
 def test_vit_small_cap_full_check(path):
     """The same step with 4 MiB buckets (many more, smaller launches) on the
     first 12,000,000 ViT elements, checked against the oracle on every
