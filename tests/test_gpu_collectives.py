@@ -301,3 +301,75 @@ def test_prepared_calls_match_direct_calls(comms):
     bc()
     torch.cuda.synchronize()
     assert bits_equal_device(zs[0], zs[3])
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_chained_collectives_without_syncs(comms, dt):
+    """24 collectives of every kind on the same buffers, issued back to back
+    on one stream with no synchronisation in between (each kernel may start
+    while the previous one drains, under programmatic dependent launch):
+    all-reduce Sum and Mean in and out of place, reduce-scatter and
+    all-gather in place, broadcast from a random root, and the bucketed
+    Mean + SGD step.  The result equals the oracle running the same
+    sequence, bit for bit.  Shards of 65,541 elements leave most of them off
+    16-byte boundaries, so both access paths take part."""
+    P, s = 4, 65_541
+    n = P * s
+    h = n // 2
+    comm = comms(P)
+    xs = replicas(P, n, dt, "uniform", 90)
+    ys = [empty(n, dt) for _ in range(P)]
+    w = torch.zeros(n, dtype=torch.float32, device=dev())
+    v = torch.zeros(n, dtype=torch.float32, device=dev())
+    hx = host_replicas(P, n, dt, "uniform", 90)
+    hy = [None] * P
+    hw = np.zeros(n, np.float32)
+    hv = np.zeros(n, np.float32)
+    rng = np.random.default_rng(91)
+    kinds = ["ar_sum", "ar_mean", "ar_to_y", "ar_from_y", "rs", "ag", "bc", "bucket_sgd"]
+    seq = [kinds[int(k)] for k in rng.integers(0, len(kinds), 24)]
+    seq[:3] = ["ar_to_y", "rs", "ag"]          # ys is written before any op reads it
+    t = DT[dt]
+    for k, op in enumerate(seq):
+        if op == "ar_sum":
+            gar.ar_all_reduce(comm, xs, xs, n, t, gar.AR_SUM)
+            hx = oracle.all_reduce(hx, op=oracle.SUM)
+        elif op == "ar_mean":
+            gar.ar_all_reduce(comm, xs, xs, n, t, gar.AR_MEAN)
+            hx = oracle.all_reduce(hx, op=oracle.MEAN)
+        elif op == "ar_to_y":
+            gar.ar_all_reduce(comm, xs, ys, n, t, gar.AR_MEAN)
+            hy = oracle.all_reduce(hx, op=oracle.MEAN)
+        elif op == "ar_from_y":
+            gar.ar_all_reduce(comm, ys, xs, n, t, gar.AR_SUM)
+            hx = oracle.all_reduce(hy, op=oracle.SUM)
+        elif op == "rs":
+            gar.ar_reduce_scatter(comm, xs, [x[r * s:(r + 1) * s] for r, x in enumerate(xs)], n, t,
+                                  gar.AR_MEAN)
+            shards = oracle.reduce_scatter(hx, op=oracle.MEAN)
+            for r in range(P):
+                hx[r][r * s:(r + 1) * s] = shards[r]
+        elif op == "ag":
+            gar.ar_all_gather(comm, [x[r * s:(r + 1) * s] for r, x in enumerate(xs)], xs, n, t)
+            hx = oracle.all_gather([hx[r][r * s:(r + 1) * s].copy() for r in range(P)])
+        elif op == "bc":
+            root = int(rng.integers(0, P))
+            gar.ar_broadcast(comm, xs, n, t, root)
+            oracle.broadcast(hx, root=root)
+        else:
+            gar.ar_bucket_all_reduce(comm, [[x[:h] for x in xs], [x[h:] for x in xs]], [h, n - h],
+                                     t, gar.AR_MEAN,
+                                     sgd=(0.1, 0.9, [w[:h], w[h:]], [v[:h], v[h:]], 1))
+            tens = [[hx[r][:h].copy() for r in range(P)], [hx[r][h:].copy() for r in range(P)]]
+            ws, vs = [hw[:h].copy(), hw[h:].copy()], [hv[:h].copy(), hv[h:].copy()]
+            oracle.bucket_all_reduce(tens, op=oracle.MEAN, sgd=(0.1, 0.9, ws, vs, 1))
+            hx = [np.concatenate([tens[0][r], tens[1][r]]) for r in range(P)]
+            hw, hv = np.concatenate(ws), np.concatenate(vs)
+    _sync_ok(comm)
+    for r in range(P):
+        got, want = to_np(xs[r]), hx[r]
+        wf = want.astype(np.float32) if dt == "f32" else (want.astype(np.uint32) << 16).view(np.float32)
+        assert not np.isnan(wf).any()
+        assert_bits_equal(got, want, f"{dt} replica {r} after {seq}")
+    assert_bits_equal(to_np(w), hw, "master")
+    assert_bits_equal(to_np(v), hv, "momentum")
