@@ -3,9 +3,11 @@
 One step is the data-parallel gradient synchronisation and optimizer step
 of ViT-B/16: P = 8 replicas of the model's 86,567,656 bf16 gradients
 (152 tensors in module order), packed into 25 MiB buckets in reverse
-order (8 buckets), each bucket all-reduced with Mean by one kernel launch
-fused with SGD (momentum 0.9, lr 0.1) on fp32 master weights, the reduced
-gradient written back to every replica.  Throughput is algorithmic bytes
+order (8 buckets), all-reduced with Mean fused with SGD (momentum 0.9, lr
+0.1) on fp32 master weights, the reduced gradient written back to every
+replica.  The step runs through the reducer, which launches buckets as
+they complete; here every gradient is marked ready in one call, so the 8
+buckets go out as one combined launch.  Throughput is algorithmic bytes
 per second: per step every replica is read and written once (2*P*N*2
 bytes) and the fp32 weights and momentum are read and written once (16*N
 bytes), 4.155 GB in all.
@@ -13,8 +15,9 @@ bytes), 4.155 GB in all.
 Output: one JSON line (rank 0).  ``value`` times the device-resident step
 with CUDA events; ``e2e`` times the same step through the public API from
 pinned host buffers (gradients in, updated weights out); ``roofline``
-relates the bucket kernel's own event-timed duration to the measured HBM
-copy bandwidth; ``sweep`` gives the flat all-reduce (and RS/AG/BC) GB/s
+relates the step kernel's event-timed average launch duration (the one
+launch the reducer issues for all 8 buckets) to the measured HBM copy
+bandwidth; ``sweep`` gives the flat all-reduce (and RS/AG/BC) GB/s
 against message size for P = 2, 4, 8; ``cpu_baseline`` times the CPU
 oracle on a bounded sample of the same step.
 
@@ -203,6 +206,16 @@ class VitStep:
                                                  gar.AR_BF16, gar.AR_MEAN, sgd))
             self.bucket_bytes.append(vit_bytes(sum(self.numels[t] for t in b)))
         self.step_bytes = vit_bytes(n)
+        # The whole step as one bucket call over all tensors in the reducer's
+        # launch order (bucket by bucket, each in reverse registration order):
+        # the combined launch the reducer issues when all buckets complete
+        # in one call, issued directly on the caller's stream.
+        order = [t for b in self.buckets for t in b]
+        self.combined = gar.PreparedBucket(
+            comm, [[g[o[t]:o[t + 1]] for g in self.grads] for t in order],
+            [self.numels[t] for t in order], gar.AR_BF16, gar.AR_MEAN,
+            (0.1, 0.9, [self.w[o[t]:o[t + 1]] for t in order],
+             [self.v[o[t]:o[t + 1]] for t in order], 1))
         self.reducer = gar.Reducer(
             comm, [[g[o[t]:o[t + 1]] for g in self.grads] for t in range(len(self.numels))],
             self.numels, gar.AR_BF16, CAP, gar.AR_MEAN,
@@ -222,6 +235,10 @@ class VitStep:
         """The same step as eight ar_bucket_all_reduce calls on one stream."""
         for c in self.calls:
             c(stream)
+
+    def step_combined(self, stream):
+        """The same step as one ar_bucket_all_reduce call over every tensor."""
+        self.combined(stream)
 
     def close(self):
         self.reducer.destroy()
@@ -249,13 +266,14 @@ def measured_peak():
 
 
 def committed_traffic():
-    """DRAM bytes per launch of the bucket kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
+    """DRAM bytes per launch of the roofline kernel (the combined launch of
+    the ViT step) from the committed ncu summary, if it was taken on the
+    current kernel source."""
     p = ROOT / "profiles" / "traffic.json"
     if not p.exists():
         return None
     d = json.loads(p.read_text())
-    if d.get("kernel_source_sha") != kernel_source_sha():
+    if d.get("kernel_source_sha") != kernel_source_sha() or "dram_bytes_per_launch" not in d:
         return None
     return d
 
@@ -264,13 +282,28 @@ def committed_traffic():
 
 def time_vit(args, device, stream, world):
     """K timed steps of the ViT workload through the reducer (the headline
-    value); then K timed steps of the same bucket launches issued one after
-    another on one stream (the kernel's average launch duration, for the
-    roofline), and once more with an event pair around each launch."""
+    value).  Then, for the roofline, K steps of the kernel the reducer
+    launches there (one combined launch of all 8 buckets) issued back to
+    back on the timing stream; and, for comparison, K steps of the 8 bucket
+    calls one after another, without and with an event pair around each."""
     import torch
     import gradient_all_reduce_gb300 as gar
     comm = gar.ar_init(P_VIT, device.index, gar.AR_MEAN)
     vs = None
+
+    def region(fn):
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                fn(stream)
+            torch.cuda.synchronize(device)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(K):
+                fn(stream)
+            e1.record(stream)
+            torch.cuda.synchronize(device)
+        return e0.elapsed_time(e1) / 1e3
+
     try:
         vs = VitStep(comm, device)
         K = args.steps
@@ -281,6 +314,7 @@ def time_vit(args, device, stream, world):
         start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
         torch.cuda.synchronize(device)
+        launches0 = vs.reducer.launches()
         with ClockSampler(device.index) as clocks, torch.cuda.stream(stream):
             start.record(stream)
             for _ in range(K):
@@ -288,6 +322,7 @@ def time_vit(args, device, stream, world):
             stop.record(stream)
             torch.cuda.synchronize(device)
         elapsed = start.elapsed_time(stop) / 1e3
+        launches = vs.reducer.launches() - launches0
         # Host time to issue one step, on a burst short enough that the
         # launch queue never fills (a full queue makes the host wait).
         with torch.cuda.stream(stream):
@@ -297,25 +332,17 @@ def time_vit(args, device, stream, world):
             host_s = (time.perf_counter() - h0) * K / 8
             torch.cuda.synchronize(device)
 
-        # The kernel roofline: the same 8 bucket launches one after another on
-        # one stream, K steps under one event pair.  Only this kernel runs
-        # there and consecutive launches do not overlap (its grids launch
-        # without PDL), so the region's time over its launches is the
-        # kernel's average launch duration, gaps between launches included.
+        # The kernel roofline: the combined launch, K times back to back on
+        # the timing stream.  Only this kernel runs there, and a launch's
+        # CTAs wait for the previous launch to complete before they touch
+        # memory, so the region's time over K is the kernel's average launch
+        # duration, gaps between launches included.
+        combined_s = region(vs.step_combined)
+        # The 8 bucket calls one after another (per-bucket launches), and the
+        # same with an event pair around each launch (each record is a
+        # serialisation point of its own).
         nb = len(vs.calls)
-        with torch.cuda.stream(stream):
-            for _ in range(args.warmup):
-                vs.step_serial(stream)
-            torch.cuda.synchronize(device)
-            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            s0.record(stream)
-            for _ in range(K):
-                vs.step_serial(stream)
-            s1.record(stream)
-            torch.cuda.synchronize(device)
-        serial_s = s0.elapsed_time(s1) / 1e3
-        # The same launches with an event pair around each one (each record
-        # is a serialisation point of its own): per-launch durations.
+        serial_s = region(vs.step_serial)
         ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(nb)] for _ in range(K)]
         with torch.cuda.stream(stream):
@@ -330,10 +357,11 @@ def time_vit(args, device, stream, world):
         if status != gar.AR_OK:
             raise RuntimeError(f"device status {gar.ar_status_string(status)}")
         return {"elapsed": elapsed, "launch_s": launch_s, "serial_s": serial_s,
-                "launches": K * nb,
+                "combined_s": combined_s, "launches": launches, "serial_launches": K * nb,
                 "step_bytes": vs.step_bytes, "launch_bytes": sum(vs.bucket_bytes) * K,
                 "clocks": clocks.summary(), "n": vs.n, "host_us_per_step": host_s / K * 1e6,
-                "serial_ms_per_step": serial_s / K * 1e3}
+                "serial_ms_per_step": serial_s / K * 1e3,
+                "combined_ms_per_step": combined_s / K * 1e3}
     finally:
         if vs is not None:
             vs.close()
@@ -1089,7 +1117,8 @@ def main():
     total_bytes = res["step_bytes"] * args.steps * world
     value = total_bytes / elapsed / 1e9
     peak, peak_kind = measured_peak()
-    achieved = res["launch_bytes"] / res["serial_s"] / 1e9
+    achieved = res["step_bytes"] * args.steps / res["combined_s"] / 1e9
+    per_bucket = res["launch_bytes"] / res["serial_s"] / 1e9
     achieved_events = res["launch_bytes"] / res["launch_s"] / 1e9
     traffic = committed_traffic()
     line = {
@@ -1103,22 +1132,32 @@ def main():
                    "l2": "inputs larger than L2 (4.155 GB moved per step, no flush)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "kernel": "k_reduce<BF16, P=8, SGD> (one launch per bucket)",
-                     "note": ("the same 8 bucket launches issued one after another on one "
-                              "stream, K steps under one CUDA-event pair (second timed region): "
-                              "region time / launches = average launch duration; the headline "
-                              "value overlaps consecutive buckets on the reducer's two streams"),
+                     "kernel": ("k_reduce<BF16, P=8, SGD, CapLarge>: one launch over the 8 "
+                                "buckets' 152 tensors (4.155 GB)"),
+                     "note": ("the kernel the reducer launches in the headline region, issued "
+                              "K times back to back on the timing stream under one CUDA-event "
+                              "pair (second timed region): region time / K = average launch "
+                              "duration"),
+                     "achieved_per_bucket_launch": per_bucket,
+                     "frac_per_bucket_launch": per_bucket / peak,
+                     "per_bucket_note": ("the 8 bucket calls one after another on one stream "
+                                         "(8 launches per step)"),
                      "achieved_per_launch_events": achieved_events,
                      "frac_per_launch_events": achieved_events / peak,
-                     "traffic": traffic["dram_bytes_per_step"] / 8 if traffic else None},
+                     "traffic": traffic["dram_bytes_per_launch"] if traffic else None},
         "gpu_launches": res["launches"],
+        "gpu_launches_note": ("kernel launches in the headline region, counted by the reducer "
+                              "(ar_reducer_launches): the 8 buckets of a step complete in one "
+                              "mark_ready_many call and go out as one combined launch; the "
+                              "roofline region issues the 8 bucket calls one by one"),
         "host_us_per_step": res["host_us_per_step"],
         "serialized_ms_per_step": res["serial_ms_per_step"],
+        "combined_ms_per_step": res["combined_ms_per_step"],
         "clocks": res["clocks"],
     }
     if traffic:
-        line["roofline"]["traffic_note"] = ("DRAM bytes per launch, mean over the 8 bucket "
-                                            "launches of one step, from " + traffic["source"])
+        line["roofline"]["traffic_note"] = ("DRAM bytes read + written by one combined launch, "
+                                            "from " + traffic["source"])
     if rank == 0 and not args.no_e2e:
         line["e2e"] = time_e2e(args, device, stream)
     if rank == 0 and not args.no_sweep:

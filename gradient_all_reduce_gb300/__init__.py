@@ -88,6 +88,7 @@ def _load() -> ctypes.CDLL:
         "ar_reducer_set_sgd": [P, ctypes.c_float, ctypes.c_float],
         "ar_reducer_wait_bucket": [P, ctypes.c_int, P],
         "ar_reducer_info": [P, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)],
+        "ar_reducer_launches": [P, ctypes.POINTER(ctypes.c_uint64)],
         "ar_reducer_destroy": [P],
         "ar_all_reduce_noalloc": [ctypes.c_int, PP, PP, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
                                   P],
@@ -370,6 +371,12 @@ class Reducer:
         out = (ctypes.c_int * max(self.ntensors, 1))()
         _ok(load().ar_reducer_info(self.handle, ctypes.byref(k), out), "ar_reducer_info")
         return list(out)[:self.ntensors]
+
+    def launches(self) -> int:
+        """Kernel launches issued by this reducer so far."""
+        k = ctypes.c_uint64()
+        _ok(load().ar_reducer_launches(self.handle, ctypes.byref(k)), "ar_reducer_launches")
+        return int(k.value)
 
     def destroy(self) -> None:
         if self.handle:

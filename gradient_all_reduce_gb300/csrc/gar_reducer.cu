@@ -18,6 +18,10 @@
 //                taken as ready on the caller's stream), then make the
 //                caller's stream wait for every launched bucket; the marks
 //                reset for the next step.
+// Buckets that one call completes together (mark_ready_many, finalize) go
+// out as one launch over their combined segment table when it fits one
+// parameter block: the same arithmetic per element, fewer launches and no
+// ramp-up and drain between them.
 #include <mutex>
 #include <new>
 #include <unordered_set>
@@ -51,6 +55,8 @@ struct ar_reducer_s {
   bool used[2] = {false, false};
   int next = 0;
   cudaEvent_t join = nullptr;
+  SegTable<CapLarge> group;                    // combined table of buckets launched together
+  uint64_t launches = 0;                       // kernel launches issued so far
 };
 
 namespace {
@@ -88,10 +94,12 @@ ar_status_t launch_bucket(ar_reducer_s* r, int b) {
   for (const auto& t : bk.small) {
     ar_status_t st = run_reduce(r->comm, r->dtype, r->sgd, t, s);
     if (st != AR_OK) return st;
+    if (t.ntiles > 0) ++r->launches;
   }
   for (const auto& t : bk.large) {
     ar_status_t st = run_reduce(r->comm, r->dtype, r->sgd, t, s);
     if (st != AR_OK) return st;
+    if (t.ntiles > 0) ++r->launches;
   }
   if (cudaEventRecord(r->done[k], s) != cudaSuccess) return AR_ERR_CUDA;
   if (cudaEventRecord(bk.done, s) != cudaSuccess) return AR_ERR_CUDA;
@@ -104,6 +112,123 @@ void note_stream(ar_reducer_s::Bucket& bk, cudaStream_t s) {
   for (cudaStream_t x : bk.mark_streams)
     if (x == s) return;
   bk.mark_streams.push_back(s);
+}
+
+// The bucket's only launch table, if it has exactly one.
+template <class F>
+bool with_single_table(const ar_reducer_s::Bucket& bk, F&& f) {
+  if (bk.small.size() + bk.large.size() != 1) return false;
+  if (!bk.small.empty()) return f(bk.small.front());
+  return f(bk.large.front());
+}
+
+// Appends src's segments to the combined table g (whose header matches,
+// every table of a reducer being built with the same parameters); false,
+// leaving g unchanged, if they do not fit.
+template <class Cap>
+bool append_segments(SegTable<CapLarge>& g, const SegTable<Cap>& src) {
+  if (g.nseg + src.nseg > uint32_t(CapLarge::kSeg) ||
+      uint64_t(g.nseg + src.nseg) * uint64_t(g.stride) > uint64_t(CapLarge::kPtr) ||
+      uint64_t(g.ntiles) + src.ntiles > 0xFFFFFFF0ull)
+    return false;
+  for (uint32_t k = 0; k < src.nseg; ++k) {
+    const uint32_t d = g.nseg;
+    for (int q = 0; q < g.stride; ++q) g.ptr[size_t(d) * g.stride + q] = src.ptr[size_t(k) * src.stride + q];
+    g.numel[d] = src.numel[k];
+    g.flags[d] = src.flags[k];
+    g.master[d] = src.master[k];
+    g.mom[d] = src.mom[k];
+    g.ntiles += src.tile0[k + 1] - src.tile0[k];
+    g.tile0[d + 1] = g.ntiles;
+    g.nseg = d + 1;
+  }
+  return true;
+}
+
+// The header of a combined table: src's launch parameters, no segments.
+template <class Cap>
+void start_group(SegTable<CapLarge>& g, const SegTable<Cap>& src) {
+  g.nseg = 0;
+  g.ntiles = 0;
+  g.np = src.np;
+  g.ndst = src.ndst;
+  g.stride = src.stride;
+  g.dst_off = src.dst_off;
+  g.mean = src.mean;
+  g.write_back = src.write_back;
+  g.store_w = src.store_w;
+  g.lr = src.lr;
+  g.mu = src.mu;
+  g.scale = src.scale;
+  g.first = src.first;
+  g.stages = src.stages;
+  g.stage_bytes = src.stage_bytes;
+  g.status = src.status;
+  g.tile0[0] = 0;
+}
+
+// One launch of the combined table of buckets bs, on the next stream,
+// after the work of every stream that marked one of their tensors.
+ar_status_t launch_group(ar_reducer_s* r, const std::vector<int>& bs) {
+  const int k = r->next;
+  r->next ^= 1;
+  cudaStream_t s = r->streams[k];
+  std::vector<cudaStream_t> waited;
+  for (int b : bs)
+    for (cudaStream_t ms : r->buckets[b].mark_streams) {
+      bool seen = false;
+      for (cudaStream_t x : waited) seen = seen || x == ms;
+      if (seen) continue;
+      waited.push_back(ms);
+      if (cudaEventRecord(r->join, ms) != cudaSuccess) return AR_ERR_CUDA;
+      if (cudaStreamWaitEvent(s, r->join, 0) != cudaSuccess) return AR_ERR_CUDA;
+    }
+  ar_status_t st = run_reduce(r->comm, r->dtype, r->sgd, r->group, s);
+  if (st != AR_OK) return st;
+  if (r->group.ntiles > 0) ++r->launches;
+  if (cudaEventRecord(r->done[k], s) != cudaSuccess) return AR_ERR_CUDA;
+  for (int b : bs) {
+    if (cudaEventRecord(r->buckets[b].done, s) != cudaSuccess) return AR_ERR_CUDA;
+    r->buckets[b].launched = true;
+  }
+  r->used[k] = true;
+  return AR_OK;
+}
+
+// Launch the buckets that one call completed, in completion order:
+// consecutive buckets with a single launch table each share one launch of
+// their combined table while it fits; any other bucket launches alone.
+ar_status_t launch_ready(ar_reducer_s* r, const std::vector<int>& ready) {
+  if (ready.size() == 1) return launch_bucket(r, ready.front());
+  std::vector<int> group;
+  auto flush = [&]() -> ar_status_t {
+    ar_status_t st = AR_OK;
+    if (group.size() == 1) st = launch_bucket(r, group.front());
+    else if (!group.empty()) st = launch_group(r, group);
+    group.clear();
+    return st;
+  };
+  for (int b : ready) {
+    const auto& bk = r->buckets[b];
+    const bool single = bk.small.size() + bk.large.size() == 1;
+    if (!single) {
+      ar_status_t st = flush();
+      if (st == AR_OK) st = launch_bucket(r, b);
+      if (st != AR_OK) return st;
+      continue;
+    }
+    if (group.empty()) with_single_table(bk, [&](const auto& t) { start_group(r->group, t); return true; });
+    bool fits = with_single_table(bk, [&](const auto& t) { return append_segments(r->group, t); });
+    if (!fits) {
+      ar_status_t st = flush();
+      if (st != AR_OK) return st;
+      with_single_table(bk, [&](const auto& t) { start_group(r->group, t); return true; });
+      fits = with_single_table(bk, [&](const auto& t) { return append_segments(r->group, t); });
+      if (!fits) return AR_ERR_INVALID_ARG;  // a single table always fits
+    }
+    group.push_back(b);
+  }
+  return flush();
 }
 
 }  // namespace
@@ -234,15 +359,27 @@ ar_status_t ar_reducer_mark_ready_many(ar_reducer_t r, const int* tensors, int n
                                        ar_stream_t stream) {
   if (!reducer_live(r) || !is_live(r->comm)) return AR_ERR_STATE;
   if (n < 0 || (n > 0 && tensors == nullptr)) return AR_ERR_INVALID_ARG;
-  for (int i = 0; i < n; ++i) {
+  for (int i = 0; i < n; ++i)
     if (tensors[i] < 0 || tensors[i] >= r->ntensors) return AR_ERR_INVALID_ARG;
-    if (r->marked[tensors[i]]) return AR_ERR_STATE;
-  }
+  DeviceGuard guard(r->comm->device);
+  if (!guard.ok()) return AR_ERR_CUDA;
+  // Mark all or none: a tensor marked before, or listed twice, undoes this
+  // call's marks and refuses it.
   for (int i = 0; i < n; ++i) {
-    ar_status_t st = ar_reducer_mark_ready(r, tensors[i], stream);
-    if (st != AR_OK) return st;
+    if (r->marked[tensors[i]]) {
+      for (int j = 0; j < i; ++j) r->marked[tensors[j]] = 0;
+      return AR_ERR_STATE;
+    }
+    r->marked[tensors[i]] = 1;
   }
-  return AR_OK;
+  std::vector<int> ready;
+  for (int i = 0; i < n; ++i) {
+    const int b = r->bucket_of[tensors[i]];
+    ar_reducer_s::Bucket& bk = r->buckets[b];
+    note_stream(bk, static_cast<cudaStream_t>(stream));
+    if (--bk.pending == 0) ready.push_back(b);
+  }
+  return ready.empty() ? AR_OK : launch_ready(r, ready);
 }
 
 ar_status_t ar_reducer_finalize(ar_reducer_t r, ar_stream_t stream) {
@@ -250,14 +387,15 @@ ar_status_t ar_reducer_finalize(ar_reducer_t r, ar_stream_t stream) {
   DeviceGuard guard(r->comm->device);
   if (!guard.ok()) return AR_ERR_CUDA;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  ar_status_t st = AR_OK;
-  for (size_t b = 0; b < r->buckets.size() && st == AR_OK; ++b) {
+  std::vector<int> rest;
+  for (size_t b = 0; b < r->buckets.size(); ++b) {
     auto& bk = r->buckets[b];
     if (!bk.launched && !bk.tensors.empty()) {
       note_stream(bk, s);
-      st = launch_bucket(r, int(b));
+      rest.push_back(int(b));
     }
   }
+  ar_status_t st = rest.empty() ? AR_OK : launch_ready(r, rest);
   for (int k = 0; k < 2 && st == AR_OK; ++k)
     if (r->used[k] && cudaStreamWaitEvent(s, r->done[k], 0) != cudaSuccess) st = AR_ERR_CUDA;
   for (auto& bk : r->buckets) {
@@ -304,6 +442,13 @@ ar_status_t ar_reducer_info(ar_reducer_t r, int* nbuckets, int* bucket_of) {
   *nbuckets = int(r->buckets.size());
   if (bucket_of != nullptr)
     for (int t = 0; t < r->ntensors; ++t) bucket_of[t] = r->bucket_of[t];
+  return AR_OK;
+}
+
+ar_status_t ar_reducer_launches(ar_reducer_t r, uint64_t* launches) {
+  if (!reducer_live(r)) return AR_ERR_STATE;
+  if (launches == nullptr) return AR_ERR_INVALID_ARG;
+  *launches = r->launches;
   return AR_OK;
 }
 

@@ -315,17 +315,23 @@ ar_status_t ar_reducer_create(ar_reducer_t *reducer, ar_comm_t comm, const ar_bu
  */
 ar_status_t ar_reducer_mark_ready(ar_reducer_t reducer, int tensor, ar_stream_t stream);
 
-/* ar_reducer_mark_ready for tensors[0], tensors[1], ... in that order (one
- * call for a group of gradients that become final together).  Checks every
- * index first: nothing is marked when one is out of range or already
- * marked (a repeated index within the list is refused when reached). */
+/* ar_reducer_mark_ready for tensors[0], tensors[1], ... (one call for a
+ * group of gradients that become final together).  All or nothing: when an
+ * index is out of range (AR_ERR_INVALID_ARG), already marked or listed
+ * twice (AR_ERR_STATE), no tensor is marked.  The buckets the call
+ * completes are launched at its end, in completion order; consecutive ones
+ * whose combined segment table fits one launch (<= 256 tensors, <= 2048
+ * replica pointers) share a single kernel launch, with the same results
+ * and every bucket's completion (ar_reducer_wait_bucket) recorded after
+ * it. */
 ar_status_t ar_reducer_mark_ready_many(ar_reducer_t reducer, const int *tensors, int n,
                                        ar_stream_t stream);
 
 /*
  * End of the step: launches every bucket not launched yet (its unmarked
- * tensors are taken as ready on `stream`), makes `stream` wait for all the
- * step's buckets (no host blocking), and clears the marks for the next step.
+ * tensors are taken as ready on `stream`; combined launches as in
+ * ar_reducer_mark_ready_many), makes `stream` wait for all the step's
+ * buckets (no host blocking), and clears the marks for the next step.
  */
 ar_status_t ar_reducer_finalize(ar_reducer_t reducer, ar_stream_t stream);
 
@@ -344,6 +350,12 @@ ar_status_t ar_reducer_set_sgd(ar_reducer_t reducer, float lr, float momentum);
 
 /* Number of buckets and, if bucket_of is not NULL, each tensor's bucket. */
 ar_status_t ar_reducer_info(ar_reducer_t reducer, int *nbuckets, int *bucket_of);
+
+/* *launches = kernel launches the reducer has issued since it was created
+ * (one per launch table of a bucket launched alone, one per combined
+ * launch; buckets whose tensors are all empty launch nothing).  Host-side
+ * count: no device synchronisation.  AR_ERR_INVALID_ARG for a null output. */
+ar_status_t ar_reducer_launches(ar_reducer_t reducer, uint64_t *launches);
 
 /* Waits for the reducer's streams, then frees it.  AR_ERR_STATE if not live. */
 ar_status_t ar_reducer_destroy(ar_reducer_t reducer);

@@ -257,3 +257,83 @@ def test_reducer_step_captured_in_a_cuda_graph():
     finally:
         red.destroy()
         gar.ar_destroy(comm)
+
+
+def test_reducer_mark_ready_many_refuses_a_repeated_index():
+    """A tensor listed twice refuses the whole call and marks nothing."""
+    P = 2
+    numels = [300, 500]
+    offs = np.concatenate([[0], np.cumsum(numels)])
+    n = int(offs[-1])
+    flat, w, v, grads, ws, vs = _setup(P, numels, offs, dt="f32", seed=61)
+    comm = gar.ar_init(P, 0, gar.AR_SUM)
+    red = gar.Reducer(comm, grads, numels, gar.AR_F32, 25 << 20, gar.AR_SUM)
+    try:
+        with pytest.raises(gar.GarError) as e:
+            red.mark_ready_many([1, 0, 1])
+        assert e.value.status == gar.AR_ERR_STATE
+        red.mark_ready_many([0, 1])                 # nothing was marked: both still free
+        red.finalize()
+        torch.cuda.synchronize()
+    finally:
+        red.destroy()
+        gar.ar_destroy(comm)
+    want = oracle.all_reduce(host_replicas(P, n, "f32", "normal", 61, std=1e-3), op=oracle.SUM)
+    assert_bits_equal(to_np(flat[1]), want[1], "after a refused call")
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_reducer_combined_launches_split_at_table_capacity(path):
+    """600 tensors of 1,000 to 1,599 fp32 elements, P = 8, 100 KB buckets
+    (24 buckets of about 25 tensors), all marked in one call: the completed
+    buckets go out as combined launches, which must split where the table
+    holds 256 tensors / 2048 replica pointers.  Two Mean + SGD steps equal
+    the oracle's bucket steps, and the last bucket's completion event
+    orders a side stream after that bucket's results."""
+    P = 8
+    rng = np.random.default_rng(62)
+    numels = [int(x) for x in rng.integers(1000, 1600, 600)]
+    offs = np.concatenate([[0], np.cumsum(numels)])
+    n = int(offs[-1])
+    flat, w, v, grads, ws, vs = _setup(P, numels, offs, dt="f32", seed=62)
+    comm = init(P, gar.AR_MEAN, path)
+    red = gar.Reducer(comm, grads, numels, gar.AR_F32, 100_000, gar.AR_MEAN,
+                      sgd=(0.1, 0.9, ws, vs, 1))
+    side = torch.cuda.Stream()
+    host = host_replicas(P, n, "f32", "normal", 62, std=1e-3)
+    hw = workloads.normal_f32(200, n, std=0.02)
+    hv = np.zeros(n, np.float32)
+    try:
+        bucket_of = red.bucket_of()
+        nb = len(set(bucket_of))
+        assert nb >= 20
+        order = list(range(len(numels) - 1, -1, -1))
+        for step in range(2):
+            red.mark_ready_many(order)
+            last = bucket_of[0]                     # the bucket of the first tensor completes last
+            red.wait_bucket(last, side)
+            with torch.cuda.stream(side):
+                got_w_side = w.clone()
+            red.finalize()
+            torch.cuda.synchronize()
+            assert gar.ar_get_async_error(comm) == gar.AR_OK
+            tens = [[host[r][offs[t]:offs[t + 1]].copy() for r in range(P)] for t in range(len(numels))]
+            tw = [hw[offs[t]:offs[t + 1]].copy() for t in range(len(numels))]
+            tv = [hv[offs[t]:offs[t + 1]].copy() for t in range(len(numels))]
+            for b in range(nb):
+                ts = [t for t in range(len(numels)) if bucket_of[t] == b]
+                oracle.bucket_all_reduce([tens[t] for t in ts], op=oracle.MEAN,
+                                         sgd=(0.1, 0.9, [tw[t] for t in ts], [tv[t] for t in ts], 1))
+            hw, hv = np.concatenate(tw), np.concatenate(tv)
+            host = [np.concatenate([tens[t][r] for t in range(len(numels))]) for r in range(P)]
+            assert_bits_equal(to_np(w), hw, f"step {step} master")
+            assert_bits_equal(to_np(v), hv, f"step {step} momentum")
+            mine = np.concatenate([np.arange(offs[t], offs[t + 1]) for t in range(len(numels))
+                                   if bucket_of[t] == last])
+            assert_bits_equal(to_np(got_w_side)[mine], hw[mine],
+                              f"step {step} bucket {last} seen after wait_bucket")
+            for r in (0, P - 1):
+                assert_bits_equal(to_np(flat[r]), host[r], f"step {step} grad {r}")
+    finally:
+        red.destroy()
+        gar.ar_destroy(comm)
