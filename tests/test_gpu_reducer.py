@@ -307,9 +307,20 @@ def test_reducer_combined_launches_split_at_table_capacity(path):
         bucket_of = red.bucket_of()
         nb = len(set(bucket_of))
         assert nb >= 20
+        # Expected launches per step: buckets in completion order (0, 1, ...)
+        # grouped while a group holds <= 256 tensors and <= 2048 pointers.
+        sizes = [bucket_of.count(b) for b in range(nb)]
+        groups, segs = 1, 0
+        for k in sizes:
+            if segs + k > 256 or (segs + k) * P > 2048:
+                groups, segs = groups + 1, 0
+            segs += k
+        assert groups >= 3
         order = list(range(len(numels) - 1, -1, -1))
         for step in range(2):
+            before = red.launches()
             red.mark_ready_many(order)
+            assert red.launches() - before == groups
             last = bucket_of[0]                     # the bucket of the first tensor completes last
             red.wait_bucket(last, side)
             with torch.cuda.stream(side):
@@ -337,3 +348,39 @@ def test_reducer_combined_launches_split_at_table_capacity(path):
     finally:
         red.destroy()
         gar.ar_destroy(comm)
+
+
+def test_reducer_launch_count():
+    """Marked one at a time, every bucket launches alone (one launch each);
+    marked in one call, the buckets it completes share one launch; the
+    counter (ar_reducer_launches) reports exactly that, and both steps give
+    the oracle's bits."""
+    P = 4
+    numels = [40_000] * 12
+    offs = np.concatenate([[0], np.cumsum(numels)])
+    n = int(offs[-1])
+    flat, w, v, grads, ws, vs = _setup(P, numels, offs, dt="f32", seed=63)
+    comm = gar.ar_init(P, 0, gar.AR_SUM)
+    red = gar.Reducer(comm, grads, numels, gar.AR_F32, 4 * 40_000 * 3, gar.AR_SUM)
+    try:
+        nb = len(set(red.bucket_of()))
+        assert nb == 4
+        assert red.launches() == 0
+        for t in range(len(numels) - 1, -1, -1):
+            red.mark_ready(t)
+        red.finalize()
+        assert red.launches() == nb
+        red.mark_ready_many(list(range(len(numels) - 1, -1, -1)))
+        red.finalize()
+        assert red.launches() == nb + 1
+        red.finalize()                              # nothing marked: the buckets launch in finalize
+        assert red.launches() == nb + 2
+        torch.cuda.synchronize()
+        assert gar.ar_get_async_error(comm) == gar.AR_OK
+    finally:
+        red.destroy()
+        gar.ar_destroy(comm)
+    host = host_replicas(P, n, "f32", "normal", 63, std=1e-3)
+    for _ in range(3):
+        host = oracle.all_reduce(host, op=oracle.SUM)
+    assert_bits_equal(to_np(flat[2]), host[2], "three Sum steps")
