@@ -1148,8 +1148,7 @@ def main():
         "gpu_launches": res["launches"],
         "gpu_launches_note": ("kernel launches in the headline region, counted by the reducer "
                               "(ar_reducer_launches): the 8 buckets of a step complete in one "
-                              "mark_ready_many call and go out as one combined launch; the "
-                              "roofline region issues the 8 bucket calls one by one"),
+                              "mark_ready_many call and go out as one combined launch"),
         "host_us_per_step": res["host_us_per_step"],
         "serialized_ms_per_step": res["serial_ms_per_step"],
         "combined_ms_per_step": res["combined_ms_per_step"],
