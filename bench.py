@@ -430,6 +430,24 @@ class E2EStep:
         """Order ``stream`` after every copy-out issued so far."""
         stream.wait_stream(self.out_stream)
 
+    def copies_only(self, stream):
+        """The step's host transfers alone, on the same streams and in the
+        same pieces: every bucket's replicas in, its weights out, no kernel.
+        Their time is the host link's bound on the end-to-end step."""
+        import torch
+        vs = self.vs
+        k = 0
+        for lo, hi, _ in self.spans:
+            for r in range(P_VIT):
+                cs = self.copy_streams[k % len(self.copy_streams)]
+                k += 1
+                with torch.cuda.stream(cs):
+                    vs.grads[r][lo:hi].copy_(self.host_g[r][lo:hi], non_blocking=True)
+            with torch.cuda.stream(self.out_stream):
+                self.host_w[lo:hi].copy_(vs.w[lo:hi], non_blocking=True)
+        for cs in self.copy_streams + [self.out_stream]:
+            stream.wait_stream(cs)
+
 
 def time_e2e(args, device, stream):
     """The ViT step end to end from pinned host buffers (E2EStep), K steps
@@ -456,9 +474,26 @@ def time_e2e(args, device, stream):
             t1.record(stream)
             torch.cuda.synchronize(device)
         el = t0.elapsed_time(t1) / 1e3
-        return {"value": vs.step_bytes * steps / el / 1e9, "unit": "GB/s",
+        # The host link alone, moving the same bytes the same way: the
+        # ceiling of this measurement on this machine.
+        link_steps = max(3, steps // 5)
+        with torch.cuda.stream(stream):
+            e2e.copies_only(stream)
+            torch.cuda.synchronize(device)
+            t0.record(stream)
+            e2e.start(stream)
+            for _ in range(link_steps):
+                e2e.copies_only(stream)
+            t1.record(stream)
+            torch.cuda.synchronize(device)
+        link = t0.elapsed_time(t1) / 1e3 / link_steps
+        value = vs.step_bytes * steps / el / 1e9
+        return {"value": value, "unit": "GB/s",
                 "h2d_bytes_per_step": 2 * vs.n * P_VIT, "d2h_bytes_per_step": 4 * vs.n,
                 "steps": steps, "ms_per_step": el / steps * 1e3,
+                "link_only_ms_per_step": link * 1e3,
+                "link_bound_GBps": vs.step_bytes / link / 1e9,
+                "frac_of_link_bound": value / (vs.step_bytes / link / 1e9),
                 "path": ("ar_reducer_* with per-bucket H2D on 4 copy streams and per-bucket D2H "
                          "of the updated weights after ar_reducer_wait_bucket; consecutive steps "
                          "ordered per bucket, not per step")}
