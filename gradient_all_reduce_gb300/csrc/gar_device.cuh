@@ -154,25 +154,28 @@ struct BF16 {
 };
 
 // ---------------------------------------------------------- reduction
-// PT > 0: P is the compile-time constant PT.  PT == 0: P is the runtime
-// value np (1 <= np <= kMaxRanks); loops run to kMaxRanks under a guard so
-// the operands stay in registers.
+// PT > 0: P is the compile-time constant PT.  PT < 0: P is the runtime
+// value np, at most -PT; PT == 0: at most kMaxRanks.  Bounded loops run to
+// the maximum under a guard so the operands stay in registers.
 template <int PT>
 struct Ranks {
-  static constexpr int kMax = PT > 0 ? PT : kMaxRanks;
+  static constexpr int kMax = PT > 0 ? PT : (PT < 0 ? -PT : kMaxRanks);
   __device__ static __forceinline__ bool has(int r, int np) { return PT > 0 ? r < PT : r < np; }
   __device__ static __forceinline__ int count(int np) { return PT > 0 ? PT : np; }
 };
 
 // Mean: one correctly rounded fp32 division by P.  For P a power of two
 // the product with the exact reciprocal is the same correctly rounded
-// quotient, so the compile-time powers of two multiply instead.
+// quotient, so powers of two multiply instead (decided at compile time for
+// a fixed P, per call for a runtime P).
 template <int PT>
 __device__ __forceinline__ float mean_of(float sum, int np) {
   if constexpr (PT > 0 && (PT & (PT - 1)) == 0) {
     return __fmul_rn(sum, 1.0f / float(PT));
+  } else if constexpr (PT > 0) {
+    return __fdiv_rn(sum, float(PT));
   } else {
-    return __fdiv_rn(sum, float(Ranks<PT>::count(np)));
+    return (np & (np - 1)) == 0 ? __fmul_rn(sum, __frcp_rn(float(np))) : __fdiv_rn(sum, float(np));
   }
 }
 

@@ -85,7 +85,7 @@ cudaError_t launch_wait_selftest(cudaStream_t stream, uint32_t* status, uint64_t
 // P ranks, the given element size, and with or without the SGD step.
 inline uint64_t reduce_tile(int P, int elem_bytes, bool tma = false, bool sgd = false) {
   if (tma) return tma_tile_elems(16 / elem_bytes);
-  const int PT = (P == 2 || P == 4 || P == 8) ? P : 0;
+  const int PT = rank_class(P);
   const int U = sgd ? unroll_for_sgd(PT) : unroll_for(PT);
   return uint64_t(U) * kThreads * (16 / elem_bytes);
 }
