@@ -38,7 +38,7 @@ def _host(P, sizes, dt, seed0):
 SHAPES = [(1,), (7,), (768,), (1000,), (2304, 768), (3,), (65_536 + 13,)]
 
 
-@pytest.mark.parametrize("P", [2, 3, 4, 8])
+@pytest.mark.parametrize("P", [2, 3, 4, 6, 8, 12])
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("op", ["sum", "mean"])
 def test_bucket_equals_oracle(cuda, path, P, dt, op):
@@ -57,13 +57,14 @@ def test_bucket_equals_oracle(cuda, path, P, dt, op):
             assert_bits_equal(to_np(ts[t][r]), host[t][r], f"tensor {t} rank {r}")
 
 
+@pytest.mark.parametrize("P", [3, 6, 8, 12])
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("write_back", [0, 1])
 @pytest.mark.parametrize("aligned", [True, False])
-def test_bucket_sgd_equals_oracle(cuda, path, dt, write_back, aligned):
+def test_bucket_sgd_equals_oracle(cuda, path, P, dt, write_back, aligned):
     """Two steps of the fused Mean + SGD(momentum 0.9, lr 0.1) on fp32
-    master weights ~N(0, 0.02) and zero momentum."""
-    P = 8
+    master weights ~N(0, 0.02) and zero momentum, for P = 8 and for one P
+    of each bounded kernel (at most 4, 8, 16 ranks)."""
     sizes = [int(np.prod(s)) for s in SHAPES]
     off = 0 if aligned else 1
     ts = _bucket(P, sizes, dt, 2, offset=off)

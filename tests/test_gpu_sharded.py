@@ -32,7 +32,7 @@ def _shards(P, s, off=0):
     return ws, vs, hw, hv
 
 
-@pytest.mark.parametrize("P", [2, 3, 4, 8])
+@pytest.mark.parametrize("P", [2, 3, 4, 6, 8, 16])
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("shard", [1, 5, 4096, 33_331])
 @pytest.mark.parametrize("in_place", [False, True])
