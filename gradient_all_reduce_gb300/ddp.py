@@ -9,10 +9,13 @@ parallelism and all-reduce"; Lecture 8, rd.me/cs336/lec8, Part 2 s.1).
 ``ReplicaDDP`` wires a torch module to the library's reducer
 (``ar_reducer_*``): each parameter's ``.grad`` is a view into rank 0's flat
 gradient buffer (ranks 1..P-1 get flat buffers of their own), and an
-autograd post-accumulate hook marks the parameter's gradient ready on the
-current stream, so the reducer launches each bucket during the backward
-pass.  ``finish()`` ends the step.  All arithmetic runs in the library's
-kernels; this module only wires buffers and hooks.
+autograd post-accumulate hook counts the parameter's gradient as final;
+when a bucket's last gradient is final, its tensors are marked ready in one
+call on the current stream, so the reducer launches the bucket during the
+backward pass.  (One library call per bucket instead of one per parameter:
+the hooks run on the host inside the backward pass.)  ``finish()`` ends the
+step.  All arithmetic runs in the library's kernels; this module only wires
+buffers and hooks.
 """
 from __future__ import annotations
 
@@ -61,6 +64,12 @@ class ReplicaDDP:
                         [self.momentum[offs[t]:offs[t + 1]] for t in range(len(self.params))], 1)
         self.reducer = gar.Reducer(comm, grads, self.numels, _AR_DTYPE[dtype], cap_bytes, op,
                                    sgd=sgd_args)
+        self._bucket_of = self.reducer.bucket_of()
+        nb = max(self._bucket_of) + 1
+        self._bucket_tensors = [[] for _ in range(nb)]
+        for t in range(len(self.params) - 1, -1, -1):      # the order gradients become final
+            self._bucket_tensors[self._bucket_of[t]].append(t)
+        self._pending = [len(ts) for ts in self._bucket_tensors]
         self.hooks_enabled = True
         self._stream = None          # handle of the stream the current backward runs on
         self._handles = []
@@ -68,11 +77,15 @@ class ReplicaDDP:
             self._handles.append(p.register_post_accumulate_grad_hook(self._hook(t)))
 
     def _hook(self, t: int):
+        b = self._bucket_of[t]
+
         def hook(_param):
             if self.hooks_enabled:
                 if self._stream is None:   # looked up once per step
                     self._stream = torch.cuda.current_stream().cuda_stream
-                self.reducer.mark_ready(t, self._stream)
+                self._pending[b] -= 1
+                if self._pending[b] == 0:
+                    self.reducer.mark_ready_many(self._bucket_tensors[b], self._stream)
         return hook
 
     def replica_grad(self, rank: int, t: int) -> torch.Tensor:
@@ -93,6 +106,7 @@ class ReplicaDDP:
         """End of the step: every bucket launched, the stream ordered after them."""
         self.reducer.finalize(torch.cuda.current_stream() if stream is None else stream)
         self._stream = None
+        self._pending = [len(ts) for ts in self._bucket_tensors]
 
     def close(self) -> None:
         for h in self._handles:
