@@ -9,7 +9,7 @@ import torch
 import gradient_all_reduce_gb300 as gar
 import oracle
 import workloads
-from gpucase import assert_bits_equal
+from gpucase import assert_bits_equal, bits_equal_device
 from golden import table
 from gradient_all_reduce_gb300.ddp import ReplicaDDP
 from oracle import mlp
@@ -114,3 +114,51 @@ def test_replica_ddp_equals_full_batch_gradient():
         gar.ar_destroy(comm)
     err = mlp.linf_rel(got, full)
     assert err <= float(table("ddp_equivalence.txt")["accept"]), err
+
+
+def test_replica_ddp_unused_parameter_and_two_steps():
+    """A parameter that gets no gradient never completes its bucket in the
+    hooks; finish() launches that bucket all the same.  Both ranks see the
+    same shard, so the Mean equals one rank's gradient bit for bit (and the
+    unused parameter's stays zero); two steps in a row check that the
+    per-bucket counts reset."""
+    torch.manual_seed(5)
+
+    class Net(torch.nn.Module):
+        def __init__(self):
+            super().__init__()
+            self.a = torch.nn.Linear(64, 64, bias=False)
+            self.unused = torch.nn.Linear(64, 64, bias=False)
+            self.b = torch.nn.Linear(64, 8)
+
+        def forward(self, x):
+            return self.b(torch.relu(self.a(x)))
+
+    model = Net().cuda()
+    ref = Net().cuda()
+    ref.load_state_dict(model.state_dict())
+    P = 2
+    comm = gar.ar_init(P, 0, gar.AR_MEAN)
+    ddp = ReplicaDDP(comm, model, P, cap_bytes=1)       # one bucket per parameter
+    try:
+        assert len(set(ddp.reducer.bucket_of())) == len(ddp.params)
+        x = torch.randn(32, 64, device="cuda")
+        for step in range(2):
+            ddp.zero_()
+            for r in (1, 0):
+                ddp.point_grads_at(r)
+                ddp.hooks_enabled = r == 0
+                model(x).square().mean().backward()
+            ddp.finish()
+            torch.cuda.synchronize()
+            assert gar.ar_get_async_error(comm) == gar.AR_OK
+            ref.zero_grad(set_to_none=False)
+            ref(x).square().mean().backward()
+            for (name, pr), t in zip(ref.named_parameters(), range(len(ddp.params))):
+                got = ddp.replica_grad(0, t)
+                want = pr.grad if pr.grad is not None else torch.zeros_like(pr)
+                assert bits_equal_device(got, want), (step, name)
+                assert bits_equal_device(ddp.replica_grad(1, t), want), (step, name)
+    finally:
+        ddp.close()
+        gar.ar_destroy(comm)
