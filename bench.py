@@ -389,6 +389,10 @@ class E2EStep:
         self.host_w = torch.empty(vs.n, dtype=torch.float32).pin_memory()
         self.copy_streams = [torch.cuda.Stream(device) for _ in range(4)]
         self.out_stream = torch.cuda.Stream(device)
+        # Kernel completions are recorded on a stream of their own, so a
+        # bucket's next copy-in does not queue behind another bucket's
+        # copy-out.
+        self.event_stream = torch.cuda.Stream(device)
         o = vs.offs
         self.spans = [(int(o[min(b)]), int(o[max(b) + 1]), b) for b in vs.buckets]
         self.kernel_done = [torch.cuda.Event() for _ in self.spans]
@@ -396,7 +400,7 @@ class E2EStep:
 
     def start(self, stream):
         """Order the copy streams after ``stream`` (the start of a region)."""
-        for cs in self.copy_streams + [self.out_stream]:
+        for cs in self.copy_streams + [self.out_stream, self.event_stream]:
             cs.wait_stream(stream)
 
     def step(self, stream):
@@ -419,8 +423,9 @@ class E2EStep:
                 used[0].wait_stream(cs)
             used[0].wait_event(self.out_done[b])
             red.mark_ready_many(ts, used[0])
+            red.wait_bucket(b, self.event_stream)
+            self.kernel_done[b].record(self.event_stream)
             red.wait_bucket(b, self.out_stream)
-            self.kernel_done[b].record(self.out_stream)
             with torch.cuda.stream(self.out_stream):
                 self.host_w[lo:hi].copy_(vs.w[lo:hi], non_blocking=True)
             self.out_done[b].record(self.out_stream)
@@ -429,6 +434,7 @@ class E2EStep:
     def finish(self, stream):
         """Order ``stream`` after every copy-out issued so far."""
         stream.wait_stream(self.out_stream)
+        stream.wait_stream(self.event_stream)
 
     def copies_only(self, stream):
         """The step's host transfers alone, on the same streams and in the
