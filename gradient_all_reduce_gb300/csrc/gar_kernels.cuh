@@ -24,10 +24,12 @@
 namespace gar {
 
 // The kernel specialisation that serves P ranks: P itself for 2, 4 and 8;
-// otherwise a bounded kernel sized for at most 4, 8 or 16 ranks (PT = -4,
-// -8, 0) with P read at run time.  Host (tile sizes) and launch agree on it.
+// otherwise a bounded kernel sized for at most 4, 8, 12 or 16 ranks
+// (PT = -4, -8, -12, 0) with P read at run time.  Host (tile sizes) and
+// launch agree on it.
 __host__ __device__ constexpr int rank_class(int P) {
-  return (P == 2 || P == 4 || P == 8) ? P : (P <= 4 ? -4 : (P <= 8 ? -8 : 0));
+  return (P == 2 || P == 4 || P == 8) ? P
+                                      : (P <= 4 ? -4 : (P <= 8 ? -8 : (P <= 12 ? -12 : 0)));
 }
 
 // Vectors per thread per tile: enough 16-byte loads in flight per thread
@@ -38,9 +40,12 @@ __host__ __device__ constexpr int unroll_for(int PT) {
 }
 // With the fused SGD step each vector also carries its fp32 master weights
 // and momentum (2 x E floats), all loaded up front: 2 vectors per thread for
-// P = 2, 4, 8 (measured on GB300 for P = 8 on the ViT-B/16 buckets: 0.982 of
-// the copy peak back to back against 0.978 with 1).
-__host__ __device__ constexpr int unroll_for_sgd(int PT) { return PT == 0 ? 1 : 2; }  // PT < 0 too
+// up to 8 ranks (measured on GB300 for P = 8 on the ViT-B/16 buckets: 0.982
+// of the copy peak back to back against 0.978 with 1), 1 beyond, where 2
+// would take one CTA per SM (168 registers at 12 ranks).
+__host__ __device__ constexpr int unroll_for_sgd(int PT) {
+  return (PT == 0 || PT < -8) ? 1 : 2;  // 2 for up to 8 ranks, exact or bounded
+}
 // Copy vectors per thread: 2 measured best on GB300 (broadcast, P = 8, 64 MiB
 // to 1 GiB per replica: 0.978-0.995 of the copy peak against 0.964-0.991 with
 // 4 and 0.934-0.987 with 8).

@@ -52,7 +52,7 @@ def test_tiny_config_mean_in_place(comms):
         assert_bits_equal(to_np(xs[r]), want[r], f"replica {r}")
 
 
-@pytest.mark.parametrize("P", [1, 2, 3, 4, 5, 8, 16])
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 5, 8, 12, 16])
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("op", ["sum", "mean"])
 @pytest.mark.parametrize("n", SIZES)
@@ -134,7 +134,7 @@ def test_special_values(comms):
             assert_bits_equal(got[~nan], want[0][~nan], f"{dt} {op}")
 
 
-@pytest.mark.parametrize("P", [1, 2, 3, 4, 8, 16])
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 8, 10, 16])
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("shard", [0, 1, 5, 4096, 33_331])
 def test_reduce_scatter(comms, P, dt, shard):
