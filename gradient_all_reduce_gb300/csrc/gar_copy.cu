@@ -1,4 +1,5 @@
 // k_copy instantiations and launch (all-gather, broadcast).
+#include <algorithm>
 #include <mutex>
 #include <unordered_map>
 
@@ -32,10 +33,16 @@ cudaError_t launch_copy(const LaunchCtx& ctx, const SegTable<Cap>& tab) {
     if (grid == 0) return cudaSuccess;
     return launch_ex(ctx, k, grid, 32, smem, tab);
   }
-  auto* k = &k_copy<Cap>;
-  const unsigned grid = grid_per_tile(tab.ntiles);
+  // The largest destination count of the segments travels in ndst (the
+  // bulk-store kernel reads each segment's own count instead).
+  SegTable<Cap> t = tab;
+  t.ndst = 0;
+  for (uint32_t s = 0; s < t.nseg; ++s) t.ndst = std::max(t.ndst, int(t.flags[s] >> 8));
+  const uint64_t items =
+      (uint64_t(t.ntiles) + kCopyWindow - 1) / kCopyWindow * kCopyWindow * uint64_t(t.ndst);
+  const unsigned grid = items < 0x7FFFFFFFull ? unsigned(items) : 0x7FFFFFFFu;
   if (grid == 0) return cudaSuccess;
-  return launch_ex(ctx, k, grid, kThreads, 0, tab);
+  return launch_ex(ctx, &k_copy<Cap>, grid, kThreads, 0, t);
 }
 
 __global__ void k_wait_selftest(uint32_t* status, uint64_t limit_ns) {

@@ -257,20 +257,41 @@ __global__ void __launch_bounds__(kThreads)
 // numel[s] is in bytes (always even: elements are 2 or 4 bytes); segment s
 // has flags[s] >> 8 destinations (an in-place all-gather skips the shard
 // that is already in place).
+//
+// One CTA copies one tile of a segment to one destination.  The work items
+// are ordered destination by destination within windows of kCopyWindow
+// tiles: item b is tile (b / (W D)) W + b % W for destination (b / W) % D,
+// with D = a.ndst, the largest destination count of the table's segments.
+// The CTAs in flight then write one or two destinations at a time, and the
+// window's source tiles, read from HBM for the first destination, are read
+// again from L2.  Measured on GB300 for broadcast and all-gather at P = 8,
+// 64 MiB - 1 GiB per replica: 1.05-1.08 of the copy peak against 0.98-1.00
+// when each CTA wrote its tile to every destination (windows of 512-2048
+// tiles measured; 1024 best).  A CTA whose segment has fewer destinations,
+// or whose tile is past the end, does nothing.
+constexpr uint64_t kCopyWindow = 1024;
+
 template <class Cap>
 __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTable<Cap> a) {
   constexpr uint64_t kTileVec = uint64_t(kCopyUnroll) * kThreads;
   griddep_launch_dependents();
   griddep_wait();
-  uint32_t s = 0;
-  for (uint32_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
-    s = seg_of(a, tile, s);
+  const uint32_t D = uint32_t(a.ndst);
+  const uint64_t items = (uint64_t(a.ntiles) + kCopyWindow - 1) / kCopyWindow * kCopyWindow * D;
+  for (uint64_t b = blockIdx.x; b < items; b += gridDim.x) {
+    // (window, destination) pair and tile: a shift and one 32-bit division
+    // (pairs number below 2^32: tiles / kCopyWindow * D).
+    const uint32_t q = uint32_t(b / kCopyWindow);
+    const uint32_t win = q / D, d = q - win * D;
+    const uint64_t tile = uint64_t(win) * kCopyWindow + b % kCopyWindow;
+    if (tile >= a.ntiles) continue;
+    const uint32_t s = seg_of(a, uint32_t(tile), 0);
+    if (d >= (a.flags[s] >> 8)) continue;
     const uint64_t nbytes = a.numel[s];
     void* const* seg = a.ptr + uint64_t(s) * a.stride;
     const void* src = seg[0];
-    void* const* dst = seg + a.dst_off;
+    void* out = seg[a.dst_off + d];
     const uint64_t lt = tile - a.tile0[s];
-    const int nd = int(a.flags[s] >> 8);
     if (a.flags[s] & kSegVec) {
       const uint64_t nvec = nbytes / 16;
       const uint64_t v0 = lt * kTileVec + threadIdx.x;
@@ -283,23 +304,18 @@ __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTa
 #pragma unroll
       for (int u = 0; u < kCopyUnroll; ++u) {
         const uint64_t vi = v0 + uint64_t(u) * kThreads;
-        if (vi < nvec)
-          for (int d = 0; d < nd; ++d) st_stream(static_cast<uint4*>(dst[d]) + vi, x[u]);
+        if (vi < nvec) st_stream(static_cast<uint4*>(out) + vi, x[u]);
       }
       if (lt + 1 == a.tile0[s + 1] - a.tile0[s]) {
         const uint64_t h = (nvec * 16) / 2 + threadIdx.x;  // 2-byte units of the tail
-        if (h < nbytes / 2) {
-          const uint16_t x1 = static_cast<const uint16_t*>(src)[h];
-          for (int d = 0; d < nd; ++d) static_cast<uint16_t*>(dst[d])[h] = x1;
-        }
+        if (h < nbytes / 2) static_cast<uint16_t*>(out)[h] = static_cast<const uint16_t*>(src)[h];
       }
     } else {
       const uint64_t h0 = lt * kTileVec * 8;  // 2-byte units per tile
       for (uint64_t k = threadIdx.x; k < kTileVec * 8; k += kThreads) {
         const uint64_t h = h0 + k;
         if (h >= nbytes / 2) break;
-        const uint16_t x1 = static_cast<const uint16_t*>(src)[h];
-        for (int d = 0; d < nd; ++d) static_cast<uint16_t*>(dst[d])[h] = x1;
+        static_cast<uint16_t*>(out)[h] = static_cast<const uint16_t*>(src)[h];
       }
     }
   }
