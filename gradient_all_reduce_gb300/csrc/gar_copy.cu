@@ -33,13 +33,17 @@ cudaError_t launch_copy(const LaunchCtx& ctx, const SegTable<Cap>& tab) {
     if (grid == 0) return cudaSuccess;
     return launch_ex(ctx, k, grid, 32, smem, tab);
   }
-  // The largest destination count of the segments travels in ndst (the
-  // bulk-store kernel reads each segment's own count instead).
+  // A large copy from one source (a broadcast) runs destination by
+  // destination in windows: the destination count travels in ndst (the
+  // bulk-store kernel reads each segment's own count instead).  Everything
+  // else keeps ndst = 0: one CTA per tile, every destination.
   SegTable<Cap> t = tab;
   t.ndst = 0;
-  for (uint32_t s = 0; s < t.nseg; ++s) t.ndst = std::max(t.ndst, int(t.flags[s] >> 8));
-  const uint64_t items =
-      (uint64_t(t.ntiles) + kCopyWindow - 1) / kCopyWindow * kCopyWindow * uint64_t(t.ndst);
+  uint64_t items = t.ntiles;
+  if (t.nseg == 1 && t.ntiles >= kCopyWindowMin) {
+    for (uint32_t s = 0; s < t.nseg; ++s) t.ndst = std::max(t.ndst, int(t.flags[s] >> 8));
+    items = (uint64_t(t.ntiles) + kCopyWindow - 1) / kCopyWindow * kCopyWindow * uint64_t(t.ndst);
+  }
   const unsigned grid = items < 0x7FFFFFFFull ? unsigned(items) : 0x7FFFFFFFu;
   if (grid == 0) return cudaSuccess;
   return launch_ex(ctx, &k_copy<Cap>, grid, kThreads, 0, t);

@@ -258,24 +258,89 @@ __global__ void __launch_bounds__(kThreads)
 // has flags[s] >> 8 destinations (an in-place all-gather skips the shard
 // that is already in place).
 //
-// One CTA copies one tile of a segment to one destination.  The work items
-// are ordered destination by destination within windows of kCopyWindow
-// tiles: item b is tile (b / (W D)) W + b % W for destination (b / W) % D,
-// with D = a.ndst, the largest destination count of the table's segments.
-// The CTAs in flight then write one or two destinations at a time, and the
-// window's source tiles, read from HBM for the first destination, are read
-// again from L2.  Measured on GB300 for broadcast and all-gather at P = 8,
-// 64 MiB - 1 GiB per replica: 1.05-1.08 of the copy peak against 0.98-1.00
-// when each CTA wrote its tile to every destination (windows of 512-2048
-// tiles measured; 1024 best).  A CTA whose segment has fewer destinations,
-// or whose tile is past the end, does nothing.
+// Windowed copies (a.ndst = D > 0; the host picks them for a broadcast of
+// at least kCopyWindowMin tiles): one CTA copies one tile of a segment to
+// one destination, and the work items run destination by destination within
+// windows of kCopyWindow tiles -- item b is tile (b / (W D)) W + b % W for
+// destination (b / W) % D.  The CTAs in flight then write one or two
+// destinations at a time, while the window's source tiles, read from HBM
+// for the first destination, are read again from L2: the source is loaded
+// with an L2 evict-last policy so that the L2's replacement keeps it
+// (without the hint the reuse depended on what had run before), and the CTA
+// of a tile's last destination returns the tile's lines to normal priority.
+// Measured on GB300, broadcast at P = 8, 64 MiB - 1 GiB per replica:
+// 1.04-1.08 of the copy peak against 0.96-0.99 when each CTA wrote its tile
+// to every destination (windows of 512-2048 tiles measured; 1024 best).
+// For an all-gather (one source segment per rank) the same order measured
+// 0.88-0.91 with the hint and 0.92-1.07 without it depending on what had
+// run before, so an all-gather keeps the order below.
+//
+// Other copies (a.ndst = 0): each CTA copies one tile to every destination
+// of its segment (all-gather 0.96-0.99; small broadcasts, below
+// kCopyWindowMin tiles, 0.92 against 0.87 for single calls from a cold
+// L2 at 16 MiB per replica, as fewer CTAs carry the same bytes).
 constexpr uint64_t kCopyWindow = 1024;
+constexpr uint64_t kCopyWindowMin = 4 * kCopyWindow;
+
+// 16-byte load that asks L2 to keep the line (policy from createpolicy).
+__device__ __forceinline__ uint4 ld_keep(const uint4* p, uint64_t policy) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p), "l"(policy));
+  return r;
+}
 
 template <class Cap>
 __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTable<Cap> a) {
   constexpr uint64_t kTileVec = uint64_t(kCopyUnroll) * kThreads;
   griddep_launch_dependents();
   griddep_wait();
+  if (a.ndst == 0) {  // small copies: one tile to every destination per CTA
+    for (uint32_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
+      const uint32_t s = seg_of(a, tile, 0);
+      const uint64_t nbytes = a.numel[s];
+      void* const* seg = a.ptr + uint64_t(s) * a.stride;
+      const void* src = seg[0];
+      void* const* dst = seg + a.dst_off;
+      const uint64_t lt = tile - a.tile0[s];
+      const int nd = int(a.flags[s] >> 8);
+      if (a.flags[s] & kSegVec) {
+        const uint64_t nvec = nbytes / 16;
+        const uint64_t v0 = lt * kTileVec + threadIdx.x;
+        uint4 x[kCopyUnroll];
+#pragma unroll
+        for (int u = 0; u < kCopyUnroll; ++u) {
+          const uint64_t vi = v0 + uint64_t(u) * kThreads;
+          if (vi < nvec) x[u] = ld_stream(static_cast<const uint4*>(src) + vi);
+        }
+#pragma unroll
+        for (int u = 0; u < kCopyUnroll; ++u) {
+          const uint64_t vi = v0 + uint64_t(u) * kThreads;
+          if (vi < nvec)
+            for (int d = 0; d < nd; ++d) st_stream(static_cast<uint4*>(dst[d]) + vi, x[u]);
+        }
+        if (lt + 1 == a.tile0[s + 1] - a.tile0[s]) {
+          const uint64_t h = (nvec * 16) / 2 + threadIdx.x;  // 2-byte units of the tail
+          if (h < nbytes / 2) {
+            const uint16_t x1 = static_cast<const uint16_t*>(src)[h];
+            for (int d = 0; d < nd; ++d) static_cast<uint16_t*>(dst[d])[h] = x1;
+          }
+        }
+      } else {
+        const uint64_t h0 = lt * kTileVec * 8;  // 2-byte units per tile
+        for (uint64_t k = threadIdx.x; k < kTileVec * 8; k += kThreads) {
+          const uint64_t h = h0 + k;
+          if (h >= nbytes / 2) break;
+          const uint16_t x1 = static_cast<const uint16_t*>(src)[h];
+          for (int d = 0; d < nd; ++d) static_cast<uint16_t*>(dst[d])[h] = x1;
+        }
+      }
+    }
+    return;
+  }
+  uint64_t keep;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
   const uint32_t D = uint32_t(a.ndst);
   const uint64_t items = (uint64_t(a.ntiles) + kCopyWindow - 1) / kCopyWindow * kCopyWindow * D;
   for (uint64_t b = blockIdx.x; b < items; b += gridDim.x) {
@@ -286,7 +351,8 @@ __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTa
     const uint64_t tile = uint64_t(win) * kCopyWindow + b % kCopyWindow;
     if (tile >= a.ntiles) continue;
     const uint32_t s = seg_of(a, uint32_t(tile), 0);
-    if (d >= (a.flags[s] >> 8)) continue;
+    const uint32_t nd = a.flags[s] >> 8;
+    if (d >= nd) continue;
     const uint64_t nbytes = a.numel[s];
     void* const* seg = a.ptr + uint64_t(s) * a.stride;
     const void* src = seg[0];
@@ -299,12 +365,24 @@ __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTa
 #pragma unroll
       for (int u = 0; u < kCopyUnroll; ++u) {
         const uint64_t vi = v0 + uint64_t(u) * kThreads;
-        if (vi < nvec) x[u] = ld_stream(static_cast<const uint4*>(src) + vi);
+        if (vi < nvec) x[u] = ld_keep(static_cast<const uint4*>(src) + vi, keep);
       }
 #pragma unroll
       for (int u = 0; u < kCopyUnroll; ++u) {
         const uint64_t vi = v0 + uint64_t(u) * kThreads;
         if (vi < nvec) st_stream(static_cast<uint4*>(out) + vi, x[u]);
+      }
+      if (d + 1 == nd) {
+        // The tile's last destination: its source lines go back to normal
+        // eviction priority.  Lines are 128 bytes: each address is the
+        // 128-byte boundary at or below a byte of the tile (so inside the
+        // source's allocation); the instruction changes no data.
+        const uint4* base = static_cast<const uint4*>(src);
+        const uint64_t first = lt * kTileVec, last = min(first + kTileVec, nvec);
+        const uintptr_t lo = reinterpret_cast<uintptr_t>(base + first) & ~uintptr_t(127);
+        const uintptr_t hi = reinterpret_cast<uintptr_t>(base + last);
+        for (uintptr_t p = lo + uintptr_t(threadIdx.x) * 128; p < hi; p += uintptr_t(kThreads) * 128)
+          asm volatile("applypriority.global.L2::evict_normal [%0], 128;" ::"l"(p) : "memory");
       }
       if (lt + 1 == a.tile0[s + 1] - a.tile0[s]) {
         const uint64_t h = (nvec * 16) / 2 + threadIdx.x;  // 2-byte units of the tail
