@@ -69,11 +69,13 @@ def parse():
     ap.add_argument("--sweep", action="store_true",
                     help="the full size/replica sweep instead: all-reduce (Sum, Mean) and "
                          "broadcast, 4 KiB .. 1 GiB per replica, P = 2, 4, 8, fp32 and bf16")
-    ap.add_argument("--case", choices=["ar", "rs", "ag", "bc", "zero1", "acc", "syncbn"],
+    ap.add_argument("--case", choices=["ar", "rs", "ag", "bc", "zero1", "acc", "acclast", "syncbn"],
                     help="time one collective alone (P=8, 256 MiB per replica; ViT-sized for "
-                         "zero1/acc) and print its GB/s; for profiling single kernels")
-    ap.add_argument("--case-ranks", type=int, default=8, choices=[2, 4, 8],
-                    help="P for --case ar/rs/ag/bc")
+                         "zero1; one 25 MiB bf16 bucket for acc, a micro-batch before the last, "
+                         "and acclast, the last one fused with Mean + SGD) and print its GB/s; "
+                         "for profiling single kernels")
+    ap.add_argument("--case-ranks", type=int, default=8, choices=range(2, 17), metavar="P",
+                    help="P (2..16) for --case ar/rs/ag/bc/acc/acclast")
     ap.add_argument("--case-dtype", choices=["f32", "bf16"], default="f32",
                     help="element type for --case ar/rs/ag/bc")
     return ap.parse_args()
@@ -1048,10 +1050,13 @@ def run_full_sweep(args):
 # ------------------------------------------------------------------ cases
 
 def run_case(args):
-    """One collective alone, K timed calls after W warm-up calls, one JSON
-    line: 256 MiB per replica for ar / rs / ag / bc (P and the element type
-    from --case-ranks and --case-dtype; P = 8, fp32 by default), the
-    ViT-B/16 gradient set (bf16, P = 8) for zero1 and acc."""
+    """One collective alone and one JSON line: K calls back to back after W
+    warm-up calls (us, GBps, frac), then the median of 20 calls each timed
+    alone from a cold, clean L2 (us_cold, GBps_cold, frac_cold).  256 MiB
+    per replica for ar / rs / ag / bc (P and the element type from
+    --case-ranks and --case-dtype; P = 8, fp32 by default); one 25 MiB bf16
+    bucket for acc and acclast (P from --case-ranks); the ViT-B/16 gradient
+    set (bf16, P = 8) for zero1."""
     import torch
     import gradient_all_reduce_gb300 as gar
     from workloads import gpu as wgpu
@@ -1059,13 +1064,13 @@ def run_case(args):
     torch.cuda.set_device(device)
     stream = torch.cuda.current_stream()
     flat = args.case in ("ar", "rs", "ag", "bc")
-    P = args.case_ranks if flat else 8
+    P = args.case_ranks if flat or args.case in ("acc", "acclast") else 8
     comm = gar.ar_init(P, 0, gar.AR_MEAN)
     try:
         if flat:
             es, tdt, dt = ((4, torch.float32, gar.AR_F32) if args.case_dtype == "f32"
                            else (2, torch.bfloat16, gar.AR_BF16))
-            n = (256 << 20) // es
+            n = (256 << 20) // es // (8 * P) * (8 * P)  # whole 16-byte vectors per shard
             xs = [torch.empty(n, dtype=tdt, device=device) for _ in range(P)]
             for r, x in enumerate(xs):
                 wgpu.fill(x, "uniform", r)
@@ -1100,7 +1105,19 @@ def run_case(args):
             acc = [[torch.zeros(n, device=device) for _ in range(P)]]
             fn = lambda: gar.ar_bucket_accumulate(comm, [g], [n], gar.AR_BF16, acc, 0.25, False,
                                                   stream)
-            nbytes, what = 10 * P * n, "one 25 MiB bf16 bucket, P=8, a micro-batch before the last"
+            nbytes, what = 10 * P * n, f"one 25 MiB bf16 bucket, P={P}, a micro-batch before the last"
+        elif args.case == "acclast":
+            n = (25 << 20) // 2
+            g = [torch.empty(n, dtype=torch.bfloat16, device=device) for _ in range(P)]
+            for r, x in enumerate(g):
+                wgpu.fill(x, "normal", 100 + r, std=1e-3)
+            acc = [[torch.zeros(n, device=device) for _ in range(P)]]
+            w, v = torch.zeros(n, device=device), torch.zeros(n, device=device)
+            fn = lambda: gar.ar_bucket_all_reduce_accumulated(
+                comm, [g], [n], gar.AR_BF16, acc, 0.25, False, gar.AR_MEAN,
+                sgd=(0.1, 0.9, [w], [v], 1), stream=stream)
+            nbytes = 8 * P * n + 16 * n
+            what = f"one 25 MiB bf16 bucket, P={P}, the last micro-batch with Mean + SGD"
         else:
             C = 2048
             sums = [torch.rand(C, device=device) for _ in range(P)]
@@ -1119,8 +1136,23 @@ def run_case(args):
         e1.record(stream)
         torch.cuda.synchronize()
         t = e0.elapsed_time(e1) / 1e3 / args.steps
+        # The same call alone from a cold, clean L2: median of event pairs.
+        flush = [torch.empty(64 << 20, device=device) for _ in range(2)]
+        pairs = []
+        for _ in range(20):
+            flush_l2(flush)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            pairs.append((a, b))
+        torch.cuda.synchronize()
+        cold = statistics.median(a.elapsed_time(b) for a, b in pairs) / 1e3
+        peak, _ = measured_peak()
         print(json.dumps({"case": args.case, "workload": what, "us": t * 1e6,
-                          "GBps": nbytes / t / 1e9}), flush=True)
+                          "GBps": nbytes / t / 1e9, "frac": nbytes / t / 1e9 / peak,
+                          "us_cold": cold * 1e6, "GBps_cold": nbytes / cold / 1e9,
+                          "frac_cold": nbytes / cold / 1e9 / peak}), flush=True)
     finally:
         gar.ar_destroy(comm)
 

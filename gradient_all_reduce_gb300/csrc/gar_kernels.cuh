@@ -120,22 +120,6 @@ __device__ __forceinline__ void sgd_vec(const float (&g)[D::kElems], float4 (&w4
   }
 }
 
-// The same when w and v still have to be loaded (one vector at a time).
-template <class D, bool SGD>
-__device__ __forceinline__ void epilogue_vec(float (&g)[D::kElems], float* w, float* v,
-                                             uint64_t e0, float lr, float mu) {
-  static_assert(D::kElems % 4 == 0, "vector holds whole float4 groups");
-  if constexpr (SGD) {
-    float4 w4[D::kElems / 4], v4[D::kElems / 4];
-#pragma unroll
-    for (int q = 0; q < D::kElems / 4; ++q) {
-      w4[q] = ld_f4(w + e0 + 4 * q);
-      v4[q] = ld_f4(v + e0 + 4 * q);
-    }
-    sgd_vec<D>(g, w4, v4, w, v, e0, lr, mu);
-  }
-}
-
 template <class D, int PT, bool SGD, class Cap>
 __global__ void __launch_bounds__(kThreads)
     k_reduce(const __grid_constant__ SegTable<Cap> a) {
@@ -496,10 +480,95 @@ __global__ void __launch_bounds__(kThreads) k_accumulate(const __grid_constant__
 // fl(acc_r + s_r) with s_r = fl(scale * g_r); the totals are reduced in rank
 // order exactly as k_reduce reduces gradients, then the optional SGD step
 // and the stores follow as in k_reduce.  The accumulators are only read.
+//
+// A thread takes one vector at a time and issues every load of it (the
+// gradients, the accumulators, and w and v with SGD) before any arithmetic.
+// Loading w and v only after the reduction cost a second round trip to HBM
+// per vector.  The kernels for a runtime P (the bounded rank classes) hold
+// registers for up to 4, 8, 12 or 16 ranks, which leaves room for two
+// 256-thread CTAs per SM at most; they run 128-thread CTAs that take the
+// tile's vectors in two turns, so that an SM holds more CTAs whose phases
+// overlap.  Measured on GB300, one 25 MiB bf16 bucket per replica, Mean +
+// SGD, from a cold L2, as fractions of the copy peak:
+//   P                        2     3     4     5     6     8     11    16
+//   w, v after the reduction 0.62  0.62  0.69  -     0.77  1.01  0.86  0.94
+//   w, v up front            1.01  0.92  1.03  -     0.80  1.05  0.94  0.98
+//   + 128-thread CTAs        1.01  0.97  1.03  0.94  0.96  1.04  0.95  1.00
+// With 128-thread CTAs only from the 12-rank class up, P = 5 and 6 measured
+// 0.76 and 0.80; only from the 8-rank class up, P = 3 measured 0.92.
+__host__ __device__ constexpr int acc_threads(int PT) { return PT <= 0 ? kThreads / 2 : kThreads; }
+
 template <int PT>
 __device__ __forceinline__ float total_of(float g, float acc, float scale, bool first) {
   const float sv = __fmul_rn(scale, g);
   return first ? sv : __fadd_rn(acc, sv);
+}
+
+template <class D, int PT, bool SGD>
+__device__ __forceinline__ void reduce_accumulated_vec(void* const* seg, int np, uint64_t vi,
+                                                       float* w, float* v, float scale, float lr,
+                                                       float mu, bool mean, bool first, bool do_store) {
+  constexpr int E = D::kElems;
+  constexpr int MAXP = Ranks<PT>::kMax;
+  constexpr int WV = SGD ? E / 4 : 1;
+  uint4 in[MAXP];
+  float4 ac[MAXP][E / 4];
+  float4 w4[WV], v4[WV];
+#pragma unroll
+  for (int r = 0; r < MAXP; ++r)
+    if (Ranks<PT>::has(r, np)) {
+      in[r] = ld_stream(static_cast<const uint4*>(seg[r]) + vi);
+      if (!first) {
+#pragma unroll
+        for (int q = 0; q < E / 4; ++q)
+          ac[r][q] = ld_f4(static_cast<const float*>(seg[np + r]) + vi * E + 4 * q);
+      }
+    }
+  if constexpr (SGD) {
+#pragma unroll
+    for (int q = 0; q < WV; ++q) {
+      w4[q] = ld_f4(w + vi * E + 4 * q);
+      v4[q] = ld_f4(v + vi * E + 4 * q);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < MAXP; ++r)
+    if (Ranks<PT>::has(r, np)) {
+      reg_fence(in[r]);
+      if (!first) {
+#pragma unroll
+        for (int q = 0; q < E / 4; ++q) reg_fence(ac[r][q]);
+      }
+    }
+  if constexpr (SGD) {
+#pragma unroll
+    for (int q = 0; q < WV; ++q) {
+      reg_fence(w4[q]);
+      reg_fence(v4[q]);
+    }
+  }
+  float g[E];
+#pragma unroll
+  for (int r = 0; r < MAXP; ++r) {
+    if (Ranks<PT>::has(r, np)) {
+      float x[E];
+      D::unpack(in[r], x);
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const float t = total_of<PT>(x[e], first ? 0.f : (&ac[r][e / 4].x)[e % 4], scale, first);
+        g[e] = r == 0 ? t : __fadd_rn(g[e], t);
+      }
+    }
+  }
+  if (mean) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) g[e] = mean_of<PT, E == 8>(g[e], np);
+  }
+  if constexpr (SGD) sgd_vec<D>(g, w4, v4, w, v, vi * E, lr, mu);
+  if (do_store) {
+    const uint4 out = D::pack(g);
+    for (int d = 0; d < np; ++d) st_stream(static_cast<uint4*>(seg[d]) + vi, out);
+  }
 }
 
 template <class D, int PT, bool SGD, class Cap>
@@ -507,6 +576,7 @@ __global__ void __launch_bounds__(kThreads)
     k_reduce_accumulated(const __grid_constant__ SegTable<Cap> a) {
   constexpr int E = D::kElems;
   constexpr int MAXP = Ranks<PT>::kMax;
+  constexpr int T = acc_threads(PT);
   const int np = a.np;
   const bool mean = a.mean != 0, first = a.first != 0;
   griddep_launch_dependents();
@@ -522,42 +592,12 @@ __global__ void __launch_bounds__(kThreads)
     float* v = SGD ? a.mom[s] : nullptr;
     if (a.flags[s] & kSegVec) {
       const uint64_t nvec = n / E;
-      const uint64_t vi = lt * kThreads + threadIdx.x;
-      if (vi < nvec) {
-        uint4 in[MAXP];
-        float4 ac[MAXP][E / 4];
 #pragma unroll
-        for (int r = 0; r < MAXP; ++r)
-          if (Ranks<PT>::has(r, np)) {
-            in[r] = ld_stream(static_cast<const uint4*>(seg[r]) + vi);
-            if (!first) {
-#pragma unroll
-              for (int q = 0; q < E / 4; ++q)
-                ac[r][q] = ld_f4(static_cast<const float*>(seg[np + r]) + vi * E + 4 * q);
-            }
-          }
-        float g[E];
-#pragma unroll
-        for (int r = 0; r < MAXP; ++r) {
-          if (Ranks<PT>::has(r, np)) {
-            float x[E];
-            D::unpack(in[r], x);
-#pragma unroll
-            for (int e = 0; e < E; ++e) {
-              const float t = total_of<PT>(x[e], first ? 0.f : (&ac[r][e / 4].x)[e % 4], a.scale, first);
-              g[e] = r == 0 ? t : __fadd_rn(g[e], t);
-            }
-          }
-        }
-        if (mean) {
-#pragma unroll
-          for (int e = 0; e < E; ++e) g[e] = mean_of<PT>(g[e], np);
-        }
-        epilogue_vec<D, SGD>(g, w, v, vi * E, a.lr, a.mu);
-        if (do_store) {
-          const uint4 out = D::pack(g);
-          for (int d = 0; d < np; ++d) st_stream(static_cast<uint4*>(seg[d]) + vi, out);
-        }
+      for (int turn = 0; turn < kThreads / T; ++turn) {
+        const uint64_t vi = lt * kThreads + uint64_t(turn) * T + threadIdx.x;
+        if (vi < nvec)
+          reduce_accumulated_vec<D, PT, SGD>(seg, np, vi, w, v, a.scale, a.lr, a.mu, mean, first,
+                                             do_store);
       }
       if (lt + 1 == a.tile0[s + 1] - a.tile0[s]) {
         const uint64_t i = nvec * E + threadIdx.x;
@@ -570,7 +610,7 @@ __global__ void __launch_bounds__(kThreads)
                                            a.scale, first);
               g = r == 0 ? t : __fadd_rn(g, t);
             }
-          if (mean) g = mean_of<PT>(g, np);
+          if (mean) g = mean_of<PT, E == 8>(g, np);
           if constexpr (SGD) sgd_step(g, a.lr, a.mu, w[i], v[i]);
           if (do_store)
             for (int d = 0; d < np; ++d) D::store1(seg[d], i, g);
@@ -578,7 +618,7 @@ __global__ void __launch_bounds__(kThreads)
       }
     } else {
       const uint64_t e0 = lt * uint64_t(kThreads) * E;
-      for (uint64_t k = threadIdx.x; k < uint64_t(kThreads) * E; k += kThreads) {
+      for (uint64_t k = threadIdx.x; k < uint64_t(kThreads) * E; k += T) {
         const uint64_t i = e0 + k;
         if (i >= n) break;
         float g = 0.f;
@@ -589,7 +629,7 @@ __global__ void __launch_bounds__(kThreads)
                                          a.scale, first);
             g = r == 0 ? t : __fadd_rn(g, t);
           }
-        if (mean) g = mean_of<PT>(g, np);
+        if (mean) g = mean_of<PT, E == 8>(g, np);
         if constexpr (SGD) sgd_step(g, a.lr, a.mu, w[i], v[i]);
         if (do_store)
           for (int d = 0; d < np; ++d) D::store1(seg[d], i, g);

@@ -37,7 +37,7 @@ def _micro_host(P, sizes, dt, m):
              for r in range(P)] for t, n in enumerate(sizes)]
 
 
-@pytest.mark.parametrize("P", [2, 3, 6, 8, 11])
+@pytest.mark.parametrize("P", [2, 3, 4, 6, 8, 11, 16])
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("sgd_wb", [None, 0, 1])
 @pytest.mark.parametrize("aligned", [True, False])
