@@ -69,15 +69,21 @@ def parse():
     ap.add_argument("--sweep", action="store_true",
                     help="the full size/replica sweep instead: all-reduce (Sum, Mean) and "
                          "broadcast, 4 KiB .. 1 GiB per replica, P = 2, 4, 8, fp32 and bf16")
-    ap.add_argument("--case", choices=["ar", "rs", "ag", "bc", "zero1", "acc", "acclast", "syncbn"],
+    ap.add_argument("--case", choices=["ar", "rs", "ag", "bc", "zero1", "accfirst", "acc", "acclast",
+                                       "syncbn"],
                     help="time one collective alone (P=8, 256 MiB per replica; ViT-sized for "
-                         "zero1; one 25 MiB bf16 bucket for acc, a micro-batch before the last, "
-                         "and acclast, the last one fused with Mean + SGD) and print its GB/s; "
-                         "for profiling single kernels")
+                         "zero1; one 25 MiB bf16 bucket for accfirst, the first micro-batch, acc, "
+                         "a later one before the last, and acclast, the last one fused with "
+                         "Mean + SGD) and print its GB/s; for profiling single kernels")
     ap.add_argument("--case-ranks", type=int, default=8, choices=range(2, 17), metavar="P",
-                    help="P (2..16) for --case ar/rs/ag/bc/acc/acclast")
+                    help="P (2..16) for --case ar/rs/ag/bc/accfirst/acc/acclast")
     ap.add_argument("--case-dtype", choices=["f32", "bf16"], default="f32",
                     help="element type for --case ar/rs/ag/bc")
+    ap.add_argument("--case-mib", type=int, default=256,
+                    help="MiB per replica for --case ar/rs/ag/bc (4096: the 2**30-element fp32 "
+                         "replicas of the large-bucket workload)")
+    ap.add_argument("--case-op", choices=["sum", "mean"],
+                    help="reduction of --case ar/rs (default: Mean for ar, Sum for rs)")
     return ap.parse_args()
 
 
@@ -1055,7 +1061,7 @@ def run_case(args):
     alone from a cold, clean L2 (us_cold, GBps_cold, frac_cold).  256 MiB
     per replica for ar / rs / ag / bc (P and the element type from
     --case-ranks and --case-dtype; P = 8, fp32 by default); one 25 MiB bf16
-    bucket for acc and acclast (P from --case-ranks); the ViT-B/16 gradient
+    bucket for accfirst, acc and acclast (P from --case-ranks); the ViT-B/16 gradient
     set (bf16, P = 8) for zero1."""
     import torch
     import gradient_all_reduce_gb300 as gar
@@ -1064,13 +1070,15 @@ def run_case(args):
     torch.cuda.set_device(device)
     stream = torch.cuda.current_stream()
     flat = args.case in ("ar", "rs", "ag", "bc")
-    P = args.case_ranks if flat or args.case in ("acc", "acclast") else 8
+    P = args.case_ranks if flat or args.case.startswith("acc") else 8
     comm = gar.ar_init(P, 0, gar.AR_MEAN)
     try:
         if flat:
             es, tdt, dt = ((4, torch.float32, gar.AR_F32) if args.case_dtype == "f32"
                            else (2, torch.bfloat16, gar.AR_BF16))
-            n = (256 << 20) // es // (8 * P) * (8 * P)  # whole 16-byte vectors per shard
+            n = (args.case_mib << 20) // es // (8 * P) * (8 * P)  # whole 16-byte vectors per shard
+            op_name = args.case_op or ("mean" if args.case == "ar" else "sum")
+            op = gar.AR_SUM if op_name == "sum" else gar.AR_MEAN
             xs = [torch.empty(n, dtype=tdt, device=device) for _ in range(P)]
             for r, x in enumerate(xs):
                 wgpu.fill(x, "uniform", r)
@@ -1078,14 +1086,15 @@ def run_case(args):
             rs = [torch.empty(sh, dtype=tdt, device=device) for _ in range(P)]
             ins = [x[r * sh:(r + 1) * sh] for r, x in enumerate(xs)]
             fn, nbytes = {
-                "ar": (lambda: gar.ar_all_reduce(comm, xs, xs, n, dt, gar.AR_MEAN, stream),
-                       2 * P * n * es),
-                "rs": (lambda: gar.ar_reduce_scatter(comm, xs, rs, n, dt, gar.AR_SUM, stream),
+                "ar": (lambda: gar.ar_all_reduce(comm, xs, xs, n, dt, op, stream), 2 * P * n * es),
+                "rs": (lambda: gar.ar_reduce_scatter(comm, xs, rs, n, dt, op, stream),
                        (P + 1) * n * es),
                 "ag": (lambda: gar.ar_all_gather(comm, ins, xs, n, dt, stream), P * n * es),
                 "bc": (lambda: gar.ar_broadcast(comm, xs, n, dt, 0, stream), P * n * es),
             }[args.case]
-            what = f"P={P} {args.case_dtype} 256 MiB per replica"
+            what = f"P={P} {args.case_dtype} {args.case_mib} MiB per replica"
+            if args.case in ("ar", "rs"):
+                what += f", {op_name}"
         elif args.case == "zero1":
             n = -(-86_567_656 // (P * 8)) * (P * 8)
             g = [torch.empty(n, dtype=torch.bfloat16, device=device) for _ in range(P)]
@@ -1097,15 +1106,18 @@ def run_case(args):
             fn = lambda: gar.ar_sharded_sgd_step(comm, g, params, ws, vs, n, gar.AR_BF16, 0.1, 0.9,
                                                  gar.AR_MEAN, stream)
             nbytes, what = 4 * P * n + 16 * n, "ViT-B/16 flat unit, P=8 bf16"
-        elif args.case == "acc":
+        elif args.case in ("accfirst", "acc"):
+            first = args.case == "accfirst"
             n = (25 << 20) // 2
             g = [torch.empty(n, dtype=torch.bfloat16, device=device) for _ in range(P)]
             for r, x in enumerate(g):
                 wgpu.fill(x, "normal", 100 + r, std=1e-3)
             acc = [[torch.zeros(n, device=device) for _ in range(P)]]
-            fn = lambda: gar.ar_bucket_accumulate(comm, [g], [n], gar.AR_BF16, acc, 0.25, False,
+            fn = lambda: gar.ar_bucket_accumulate(comm, [g], [n], gar.AR_BF16, acc, 0.25, first,
                                                   stream)
-            nbytes, what = 10 * P * n, f"one 25 MiB bf16 bucket, P={P}, a micro-batch before the last"
+            nbytes = (6 if first else 10) * P * n
+            what = (f"one 25 MiB bf16 bucket, P={P}, "
+                    + ("the first micro-batch" if first else "a micro-batch before the last"))
         elif args.case == "acclast":
             n = (25 << 20) // 2
             g = [torch.empty(n, dtype=torch.bfloat16, device=device) for _ in range(P)]
