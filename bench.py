@@ -1055,6 +1055,68 @@ def run_full_sweep(args):
 
 # ------------------------------------------------------------------ cases
 
+def case_cpu_baseline(case, P, dtype_name, op_name, min_seconds=1.0):
+    """The oracle beside a --case line: the oracle as it stands (one
+    thread) on a bounded sample of the case's workload, 2**20 elements per
+    replica (the 2048 channels for syncbn), the same seeded inputs, repeated
+    for at least min_seconds; GB/s by the case's algorithmic-bytes formula."""
+    import numpy as np
+    import oracle
+    import workloads
+    oracle.build()
+    op = oracle.SUM if op_name == "sum" else oracle.MEAN
+    n = (1 << 20) // (8 * P) * (8 * P)
+    if case in ("ar", "rs", "ag", "bc"):
+        es = 4 if dtype_name == "f32" else 2
+        xs = [workloads.replica_values("uniform", dtype_name, r, n) for r in range(P)]
+        sh = n // P
+        if case == "ar":
+            fn, nbytes = (lambda: oracle.all_reduce(xs, recv=xs, op=op)), 2 * P * n * es
+        elif case == "rs":
+            out = [np.empty(sh, xs[0].dtype) for _ in range(P)]
+            fn, nbytes = (lambda: oracle.reduce_scatter(xs, recv=out, op=op)), (P + 1) * n * es
+        elif case == "ag":
+            shards = [x[r * sh:(r + 1) * sh].copy() for r, x in enumerate(xs)]
+            fn, nbytes = (lambda: oracle.all_gather(shards, recv=xs)), P * n * es
+        else:
+            fn, nbytes = (lambda: oracle.broadcast(xs, 0)), P * n * es
+        sample = f"{n} {dtype_name} elements per replica"
+    elif case == "zero1":
+        g = [workloads.replica_values("normal", "bf16", 100 + r, n, std=1e-3) for r in range(P)]
+        params = [np.zeros(n, np.uint16) for _ in range(P)]
+        ws = [np.zeros(n // P, np.float32) for _ in range(P)]
+        vs = [np.zeros(n // P, np.float32) for _ in range(P)]
+        fn = lambda: oracle.sharded_sgd_step(g, params, ws, vs, 0.1, 0.9, oracle.MEAN)
+        nbytes, sample = 4 * P * n + 16 * n, f"a flat unit of {n} bf16 elements"
+    elif case in ("accfirst", "acc", "acclast"):
+        g = [[workloads.replica_values("normal", "bf16", 100 + r, n, std=1e-3) for r in range(P)]]
+        acc = [[np.zeros(n, np.float32) for _ in range(P)]]
+        if case == "acclast":
+            w, v = np.zeros(n, np.float32), np.zeros(n, np.float32)
+            fn = lambda: oracle.bucket_all_reduce_accumulated(g, acc, 0.25, False, oracle.MEAN,
+                                                              sgd=(0.1, 0.9, [w], [v], 1))
+            nbytes = 8 * P * n + 16 * n
+        else:
+            first = case == "accfirst"
+            fn = lambda: oracle.bucket_accumulate(g, acc, 0.25, first)
+            nbytes = (6 if first else 10) * P * n
+        sample = f"one bucket of {n} bf16 elements per replica"
+    else:
+        C = 2048
+        sums = [workloads.uniform_f32(r, C) for r in range(P)]
+        sq = [workloads.uniform_f32(100 + r, C) + np.float32(1) for r in range(P)]
+        fn = lambda: oracle.syncbn_stats(sums, sq, [1000] * P, 1e-5)
+        nbytes, sample = 4 * P * C * 4, f"{C} channels"
+    reps, spent = 0, 0.0
+    while spent < min_seconds or reps == 0:
+        t0 = time.perf_counter()
+        fn()
+        spent += time.perf_counter() - t0
+        reps += 1
+    return {"value": nbytes * reps / spent / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{sample}, P={P}, {reps} calls in {spent:.2f} s, one thread"}
+
+
 def run_case(args):
     """One collective alone and one JSON line: K calls back to back after W
     warm-up calls (us, GBps, frac), then the median of 20 calls each timed
@@ -1161,10 +1223,14 @@ def run_case(args):
         torch.cuda.synchronize()
         cold = statistics.median(a.elapsed_time(b) for a, b in pairs) / 1e3
         peak, _ = measured_peak()
-        print(json.dumps({"case": args.case, "workload": what, "us": t * 1e6,
-                          "GBps": nbytes / t / 1e9, "frac": nbytes / t / 1e9 / peak,
-                          "us_cold": cold * 1e6, "GBps_cold": nbytes / cold / 1e9,
-                          "frac_cold": nbytes / cold / 1e9 / peak}), flush=True)
+        line = {"case": args.case, "workload": what, "us": t * 1e6, "GBps": nbytes / t / 1e9,
+                "frac": nbytes / t / 1e9 / peak, "us_cold": cold * 1e6,
+                "GBps_cold": nbytes / cold / 1e9, "frac_cold": nbytes / cold / 1e9 / peak}
+        if not args.no_cpu:
+            line["cpu_baseline"] = case_cpu_baseline(
+                args.case, P, args.case_dtype if flat else "bf16",
+                args.case_op or ("mean" if args.case == "ar" else "sum"))
+        print(json.dumps(line), flush=True)
     finally:
         gar.ar_destroy(comm)
 

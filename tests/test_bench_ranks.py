@@ -53,3 +53,15 @@ def test_reference_arm_runs_on_rank0_only():
                         "--steps", "1", "--warmup", "0"], env=env, capture_output=True, text=True,
                        timeout=120)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+@pytest.mark.parametrize("case", ["ar", "rs", "ag", "bc", "zero1", "accfirst", "acc", "acclast",
+                                  "syncbn"])
+def test_case_cpu_baseline_runs_every_case(case):
+    """The oracle beside each --case line runs on the host for every case,
+    at a P that is not a power of two, and reports a positive rate."""
+    sys.path.insert(0, ROOT)
+    import bench
+    got = bench.case_cpu_baseline(case, 6, "bf16", "mean", min_seconds=0.0)
+    assert got["kind"] == "oracle" and got["cores"] == 1 and got["unit"] == "GB/s"
+    assert got["value"] > 0 and "P=6" in got["sample"]
