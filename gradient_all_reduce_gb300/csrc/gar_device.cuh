@@ -55,6 +55,13 @@ __device__ __forceinline__ void st_stream(void* p, const uint4& v) {
 #endif
 }
 
+// 8-byte form of ld_stream (four bf16 elements).
+__device__ __forceinline__ uint2 ld_stream8(const void* p) {
+  uint2 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+  return r;
+}
+
 // fp32 master-weight / momentum arrays are read and written by the same
 // thread (read-modify-write), so they use the coherent path.
 __device__ __forceinline__ float4 ld_f4(const float* p) {
@@ -77,6 +84,7 @@ __device__ __forceinline__ void st_f4(float* p, const float4& v) {
 __device__ __forceinline__ void reg_fence(uint4& v) {
   asm volatile("" : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w));
 }
+__device__ __forceinline__ void reg_fence(uint2& v) { asm volatile("" : "+r"(v.x), "+r"(v.y)); }
 __device__ __forceinline__ void reg_fence(float4& v) {
   asm volatile("" : "+f"(v.x), "+f"(v.y), "+f"(v.z), "+f"(v.w));
 }
@@ -123,6 +131,12 @@ struct F32 {
     return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
                       __float_as_uint(f[3]));
   }
+  // A quad is 4 consecutive elements (16 bytes): quad q holds elements 4q .. 4q + 3.
+  using Quad = uint4;
+  __device__ static __forceinline__ Quad ld_quad(const void* p, uint64_t q) {
+    return ld_stream(static_cast<const uint4*>(p) + q);
+  }
+  __device__ static __forceinline__ void unpack_quad(const Quad& v, float (&f)[4]) { unpack(v, f); }
   __device__ static __forceinline__ float load1(const void* p, uint64_t i) {
     return static_cast<const float*>(p)[i];
   }
@@ -144,6 +158,15 @@ struct BF16 {
   __device__ static __forceinline__ uint4 pack(const float (&f)[8]) {
     return make_uint4(bf16x2_rne(f[0], f[1]), bf16x2_rne(f[2], f[3]), bf16x2_rne(f[4], f[5]),
                       bf16x2_rne(f[6], f[7]));
+  }
+  // A quad is 4 consecutive elements (8 bytes): quad q holds elements 4q .. 4q + 3.
+  using Quad = uint2;
+  __device__ static __forceinline__ Quad ld_quad(const void* p, uint64_t q) {
+    return ld_stream8(static_cast<const uint2*>(p) + q);
+  }
+  __device__ static __forceinline__ void unpack_quad(const Quad& v, float (&f)[4]) {
+    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+    f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
   }
   __device__ static __forceinline__ float load1(const void* p, uint64_t i) {
     return __uint_as_float(uint32_t(static_cast<const uint16_t*>(p)[i]) << 16);

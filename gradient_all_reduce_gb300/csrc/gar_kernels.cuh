@@ -388,35 +388,28 @@ __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTa
 // the last, no communication): segment = one (tensor, rank) pair, ptr[0] =
 // the gradient (D), ptr[1] = its fp32 accumulator; per element, with
 // s = fl(scale * g):  acc = first ? s : fl(acc + s).  The first micro-batch
-// (no accumulator to read) is a kernel of its own, FIRST = true: 31 registers
-// instead of 36, so 8 CTAs per SM, and 0.92 of the copy peak on GB300 against
-// 0.85 as a runtime branch of one kernel (one 25 MiB bf16 bucket, P = 8).
-// Vectors per thread: 2 measured best for both (later micro-batches 1.03
-// against 1.02 with 4 and 1.00 with 8; the first 0.92 against 0.78 and 0.84).
+// (no accumulator to read) is a kernel of its own, FIRST = true: fewer
+// registers, 8 CTAs per SM, and 0.92 of the copy peak on GB300 against 0.85
+// as a runtime branch of one kernel (one 25 MiB bf16 bucket, P = 8).
+//
+// A thread works on quads (4 consecutive elements) kThreads apart, so every
+// warp-wide access covers one contiguous span: 8 or 16 bytes of gradient
+// and 16 bytes of accumulator per lane.  With a bf16 vector of 8 elements
+// per thread instead, each fp32 access wrote or read half of every 32-byte
+// sector it touched (16 bytes at a 32-byte stride), and the L1-to-L2 write
+// path ran at 72-82 % of its peak under ncu.  Measured on GB300 (one 25 MiB
+// bf16 bucket, of the copy peak, back to back / from a cold L2): the first
+// micro-batch at P = 8 rose from 0.94 / 0.92 to 1.00 / 1.02, at P = 2 from
+// 0.82 / 0.76 to 0.90 / 0.95; later micro-batches at P = 8 from 1.03 / 1.04
+// to 1.03 / 1.06.  Vectors per thread: 2 measured best for both kernels in
+// the vector form (later micro-batches 1.03 against 1.02 with 4 and 1.00
+// with 8; the first 0.92 against 0.78 and 0.84).
 constexpr int kAccUnroll = 2;
-
-template <class D, bool FIRST>
-__device__ __forceinline__ void acc_vec(const uint4& gv, float4 (&a4)[D::kElems / 4], float* acc,
-                                        uint64_t e0, float scale) {
-  float g[D::kElems];
-  D::unpack(gv, g);
-#pragma unroll
-  for (int q = 0; q < D::kElems / 4; ++q) {
-    float* av = &a4[q].x;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float sv = __fmul_rn(scale, g[4 * q + k]);
-      av[k] = FIRST ? sv : __fadd_rn(av[k], sv);
-    }
-    st_f4(acc + e0 + 4 * q, a4[q]);
-  }
-}
 
 template <class D, class Cap, bool FIRST>
 __global__ void __launch_bounds__(kThreads) k_accumulate(const __grid_constant__ SegTable<Cap> a) {
-  constexpr int E = D::kElems;
-  constexpr int U = kAccUnroll;
-  constexpr uint64_t kTileVec = uint64_t(U) * kThreads;
+  constexpr int J = kAccUnroll * D::kElems / 4;  // quads per thread per tile
+  constexpr uint64_t kTileQuads = uint64_t(J) * kThreads;
   griddep_launch_dependents();
   griddep_wait();
   uint32_t s = 0;
@@ -427,44 +420,50 @@ __global__ void __launch_bounds__(kThreads) k_accumulate(const __grid_constant__
     float* acc = static_cast<float*>(a.ptr[uint64_t(s) * a.stride + 1]);
     const uint64_t lt = tile - a.tile0[s];
     if (a.flags[s] & kSegVec) {
-      const uint64_t nvec = n / E;
-      const uint64_t v0 = lt * kTileVec + threadIdx.x;
-      // All gradient and accumulator loads first, then the stores.
-      uint4 x[U];
-      float4 a4[U][E / 4];
+      const uint64_t nq = n / 4;
+      const uint64_t q0 = lt * kTileQuads + threadIdx.x;
+      typename D::Quad x[J];
+      float4 a4[J];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const uint64_t vi = v0 + uint64_t(u) * kThreads;
-        if (vi < nvec) {
-          x[u] = ld_stream(static_cast<const uint4*>(g) + vi);
-#pragma unroll
-          for (int q = 0; q < E / 4; ++q)
-            a4[u][q] = FIRST ? make_float4(0.f, 0.f, 0.f, 0.f) : ld_f4(acc + vi * E + 4 * q);
+      for (int j = 0; j < J; ++j) {
+        const uint64_t qi = q0 + uint64_t(j) * kThreads;
+        if (qi < nq) {
+          x[j] = D::ld_quad(g, qi);
+          a4[j] = FIRST ? make_float4(0.f, 0.f, 0.f, 0.f) : ld_f4(acc + 4 * qi);
         }
       }
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (v0 + uint64_t(u) * kThreads < nvec) {
-          reg_fence(x[u]);
-#pragma unroll
-          for (int q = 0; q < E / 4; ++q) reg_fence(a4[u][q]);
+      for (int j = 0; j < J; ++j) {
+        if (q0 + uint64_t(j) * kThreads < nq) {
+          reg_fence(x[j]);
+          reg_fence(a4[j]);
         }
       }
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const uint64_t vi = v0 + uint64_t(u) * kThreads;
-        if (vi < nvec) acc_vec<D, FIRST>(x[u], a4[u], acc, vi * E, a.scale);
+      for (int j = 0; j < J; ++j) {
+        const uint64_t qi = q0 + uint64_t(j) * kThreads;
+        if (qi < nq) {
+          float f[4];
+          D::unpack_quad(x[j], f);
+          float* av = &a4[j].x;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float sv = __fmul_rn(a.scale, f[k]);
+            av[k] = FIRST ? sv : __fadd_rn(av[k], sv);
+          }
+          st_f4(acc + 4 * qi, a4[j]);
+        }
       }
       if (lt + 1 == a.tile0[s + 1] - a.tile0[s]) {
-        const uint64_t i = nvec * E + threadIdx.x;
+        const uint64_t i = nq * 4 + threadIdx.x;
         if (i < n) {
           const float sv = __fmul_rn(a.scale, D::load1(g, i));
           acc[i] = FIRST ? sv : __fadd_rn(acc[i], sv);
         }
       }
     } else {
-      const uint64_t e0 = lt * kTileVec * E;
-      for (uint64_t k = threadIdx.x; k < kTileVec * E; k += kThreads) {
+      const uint64_t e0 = lt * kTileQuads * 4;
+      for (uint64_t k = threadIdx.x; k < kTileQuads * 4; k += kThreads) {
         const uint64_t i = e0 + k;
         if (i >= n) break;
         const float sv = __fmul_rn(a.scale, D::load1(g, i));
@@ -495,7 +494,11 @@ __global__ void __launch_bounds__(kThreads) k_accumulate(const __grid_constant__
 //   w, v up front            1.01  0.92  1.03  -     0.80  1.05  0.94  0.98
 //   + 128-thread CTAs        1.01  0.97  1.03  0.94  0.96  1.04  0.95  1.00
 // With 128-thread CTAs only from the 12-rank class up, P = 5 and 6 measured
-// 0.76 and 0.80; only from the 8-rank class up, P = 3 measured 0.92.
+// 0.76 and 0.80; only from the 8-rank class up, P = 3 measured 0.92.  The
+// quad layout of k_accumulate (fp32 accesses contiguous across a warp) was
+// tried here too: from a cold L2 it gained at P = 2 and 4 (1.01 -> 1.05,
+// 1.03 -> 1.05) but back to back nothing, and the runtime-P kernels lost
+// 0.02-0.04 to the 10-16 registers it added, so the vector layout stays.
 __host__ __device__ constexpr int acc_threads(int PT) { return PT <= 0 ? kThreads / 2 : kThreads; }
 
 template <int PT>
