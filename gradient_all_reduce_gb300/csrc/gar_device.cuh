@@ -204,6 +204,21 @@ __device__ __forceinline__ float div_small(float x, float d, float r) {
   return __fmaf_rn(e, r, y);
 }
 
+// x / d for a quotient that is only ever stored as bf16 (round to nearest
+// even of the correctly rounded fp32 quotient q).  With r = RN(1/d) and
+// y = RN(x r), y = (x/d)(1 + e1)(1 + e2) with |e1|, |e2| <= 2^-24, so y lies
+// within three units in the last place of q (as bit patterns).  Two fp32
+// values that close round to the same bf16 unless a rounding boundary lies
+// between them, and the boundaries sit next to a low half of 0x8000 (the
+// tie).  So y serves unless its low half lies in 0x7FFC .. 0x8003, where
+// div_small gives q itself.  Zeros and infinities pass through y unchanged
+// and a NaN stays a NaN.  Checked on the GPU for every fp32 x and d = 3..15:
+// the bf16 rounding equals that of __fdiv_rn.
+__device__ __forceinline__ float div_small_bf16(float x, float d, float r) {
+  const float y = __fmul_rn(x, r);
+  return ((__float_as_uint(y) - 0x7FFCu) & 0xFFFFu) < 8u ? div_small(x, d, r) : y;
+}
+
 // Mean: one correctly rounded fp32 division by P.  For P a power of two
 // the product with the exact reciprocal is the same correctly rounded
 // quotient, so powers of two multiply instead (decided at compile time for
@@ -211,7 +226,9 @@ __device__ __forceinline__ float div_small(float x, float d, float r) {
 // Markstein's correction when FAST (the bf16 kernels: 8 divisions per
 // vector, and the same CTAs per SM), by the IEEE division otherwise (in the
 // fp32 kernels the correction's registers would cost one CTA per SM).
-template <int PT, bool FAST = false>
+// BF16_OUT: the mean is only stored as bf16, so a quotient with the same
+// bf16 rounding serves (div_small_bf16).
+template <int PT, bool FAST = false, bool BF16_OUT = false>
 __device__ __forceinline__ float mean_of(float sum, int np) {
   if constexpr (PT > 0 && (PT & (PT - 1)) == 0) {
     return __fmul_rn(sum, 1.0f / float(PT));
@@ -219,7 +236,9 @@ __device__ __forceinline__ float mean_of(float sum, int np) {
     return __fdiv_rn(sum, float(PT));
   } else {
     const float d = float(np), r = __frcp_rn(d);
-    if constexpr (FAST) {
+    if constexpr (FAST && BF16_OUT) {
+      return (np & (np - 1)) == 0 ? __fmul_rn(sum, r) : div_small_bf16(sum, d, r);
+    } else if constexpr (FAST) {
       return (np & (np - 1)) == 0 ? __fmul_rn(sum, r) : div_small(sum, d, r);
     } else {
       return (np & (np - 1)) == 0 ? __fmul_rn(sum, r) : __fdiv_rn(sum, d);
@@ -228,8 +247,9 @@ __device__ __forceinline__ float mean_of(float sum, int np) {
 }
 
 // acc[e] = in[0][e] + in[1][e] + ... + in[P-1][e], left to right in fp32,
-// seeded with rank 0's value; then divided by P when mean is set.
-template <class D, int PT>
+// seeded with rank 0's value; then divided by P when mean is set.  STORE_ONLY:
+// the caller only stores the result in the replicas' element type.
+template <class D, int PT, bool STORE_ONLY = false>
 __device__ __forceinline__ void reduce_vec(const uint4 (&in)[Ranks<PT>::kMax], int np, bool mean,
                                            float (&acc)[D::kElems]) {
   D::unpack(in[0], acc);
@@ -244,7 +264,8 @@ __device__ __forceinline__ void reduce_vec(const uint4 (&in)[Ranks<PT>::kMax], i
   }
   if (mean) {
 #pragma unroll
-    for (int e = 0; e < D::kElems; ++e) acc[e] = mean_of<PT, D::kElems == 8>(acc[e], np);
+    for (int e = 0; e < D::kElems; ++e)
+      acc[e] = mean_of<PT, D::kElems == 8, STORE_ONLY && D::kElems == 8>(acc[e], np);
   }
 }
 

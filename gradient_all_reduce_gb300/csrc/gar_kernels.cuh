@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(kThreads)
         const uint64_t vi = v0 + uint64_t(u) * kThreads;
         if (vi < nvec) {
           float g[E];
-          reduce_vec<D, PT>(in[u], np, mean, g);
+          reduce_vec<D, PT, !SGD>(in[u], np, mean, g);
           if constexpr (SGD) {
             sgd_vec<D>(g, w4[u], v4[u], w, v, vi * E, a.lr, a.mu);
             if (a.store_w) {  // the sharded step: every rank gets the new weights
