@@ -132,8 +132,8 @@ ar_status_t ar_init(ar_comm_t* comm, int nranks, int cuda_device, ar_op_t defaul
   c->pdl = !(env != nullptr && std::strcmp(env, "0") == 0);
   // All-gather and broadcast run on the register-staged copy kernel (one
   // CTA per tile) unless GAR_COPY=tma asks for the bulk-store pipeline
-  // (measured on GB300: 0.95-1.04 against 0.86-0.91 of the copy peak at
-  // >= 256 MiB per replica).
+  // (measured on GB300, broadcast back to back at 64 MiB - 1 GiB per
+  // replica: 1.01-1.08 of the copy peak against 0.85-1.02).
   env = std::getenv("GAR_COPY");
   c->copy_tma = env != nullptr && std::strcmp(env, "tma") == 0;
   if (cudaMalloc(&c->d_status, sizeof(uint32_t)) != cudaSuccess) {

@@ -95,9 +95,9 @@ inline uint64_t reduce_tile(int P, int elem_bytes, bool tma = false, bool sgd = 
 // always cover one compact window of every buffer, and no CTA is left with
 // a tail of its own.  Measured on GB300 against a persistent grid of the
 // same kernels (grid-stride over equal tile counts): flat all-reduce at
-// >= 256 MiB per replica 0.92-0.95 -> 1.03-1.04 of the copy peak, broadcast
-// 0.84-0.93 -> 0.95-1.04, the ViT-B/16 bucket step 0.92 -> 0.95 launched
-// one bucket after another.
+// >= 256 MiB per replica 0.92-0.95 -> 1.03-1.05 of the copy peak, broadcast
+// 0.84-0.93 -> 0.95-1.04, the ViT-B/16 bucket step 0.92 -> 0.98 launched
+// one bucket after another and 0.98 -> 1.02 through the reducer.
 inline unsigned grid_per_tile(uint32_t ntiles) { return ntiles < 0x7FFFFFFFu ? ntiles : 0x7FFFFFFFu; }
 
 // Persistent grid of the bulk-copy pipelines (each CTA keeps a ring of
