@@ -257,7 +257,9 @@ __global__ void __launch_bounds__(kThreads)
 // to every destination (windows of 512-2048 tiles measured; 1024 best).
 // For an all-gather (one source segment per rank) the same order measured
 // 0.88-0.91 with the hint and 0.92-1.07 without it depending on what had
-// run before, so an all-gather keeps the order below.
+// run before; with the priority reset too, 0.90 at P = 8 (256 MiB and
+// 1 GiB per replica) against 0.98-1.00 in the classic order, and no better
+// at P = 4.  So an all-gather keeps the order below.
 //
 // Other copies (a.ndst = 0): each CTA copies one tile to every destination
 // of its segment (all-gather 0.96-0.99; small broadcasts, below
