@@ -16,7 +16,7 @@ from fractions import Fraction
 import numpy as np
 
 import oracle
-from oracle import BF16, F32, MEAN, SUM  # noqa: F401
+from oracle import MEAN, SUM
 
 SIZES = (0, 1, 2, 3, 5, 8, 17, 33)
 

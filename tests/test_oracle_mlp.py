@@ -7,7 +7,6 @@ factor P of an undivided accumulation ("Distributed Training",
 computervisiononline.com, "How to Apply It", part 1 output).
 """
 import numpy as np
-import pytest
 
 import oracle
 import workloads
