@@ -74,6 +74,39 @@ def test_reducer_two_steps_match_oracle(path):
         gar.ar_destroy(comm)
 
 
+@pytest.mark.parametrize("P", [3, 6, 12])
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_reducer_runtime_p_combined_launch_matches_oracle(P, dt):
+    """A rank count that is not a power of two (the kernels sized for up to
+    4, 8 or 12 ranks, and the Mean's division): 4M elements of the ViT-B/16
+    set, 2 MiB buckets, Mean + SGD, every tensor marked in one
+    mark_ready_many call (so the buckets go out as combined launches), two
+    steps."""
+    numels, offs = _vit_prefix(4_000_000)
+    n = int(offs[-1])
+    flat, w, v, grads, ws, vs = _setup(P, numels, offs, dt)
+    comm = gar.ar_init(P, 0, gar.AR_MEAN)
+    red = gar.Reducer(comm, grads, numels, gar.AR_BF16 if dt == "bf16" else gar.AR_F32, 2 << 20,
+                      gar.AR_MEAN, sgd=(0.1, 0.9, ws, vs, 1))
+    try:
+        host = host_replicas(P, n, dt, "normal", 100, std=1e-3)
+        hw = [workloads.normal_f32(200, n, std=0.02)]
+        hv = [np.zeros(n, np.float32)]
+        for step in range(2):
+            red.mark_ready_many(list(range(len(numels) - 1, -1, -1)))
+            red.finalize()
+            torch.cuda.synchronize()
+            oracle.bucket_all_reduce([host], op=oracle.MEAN, sgd=(0.1, 0.9, hw, hv, 1))
+            assert_bits_equal(to_np(w), hw[0], f"step {step} master")
+            assert_bits_equal(to_np(v), hv[0], f"step {step} momentum")
+            for r in (0, P - 1):
+                assert_bits_equal(to_np(flat[r]), host[r], f"step {step} grad {r}")
+        assert gar.ar_get_async_error(comm) == gar.AR_OK
+    finally:
+        red.destroy()
+        gar.ar_destroy(comm)
+
+
 def test_reducer_orders_after_producer_streams():
     """Each gradient is written by a copy on one of three side streams and
     marked ready on that stream, in a shuffled order; the all-reduce must
