@@ -33,10 +33,18 @@ __host__ __device__ constexpr int rank_class(int P) {
 }
 
 // Vectors per thread per tile: enough 16-byte loads in flight per thread
-// (P * U * 16 bytes) to cover HBM latency, bounded by registers.  A
-// bounded kernel takes the unroll of its maximum.
+// (P * U * 16 bytes) to cover HBM latency, bounded by registers.  The
+// bounded kernels (a runtime P) take half the unroll of their maximum: they
+// hold registers for ranks they may not use, and a Mean over P that is not
+// a power of two divides, so more CTAs per SM hide more of that arithmetic.
+// Measured on GB300 at 128 MiB per replica, back to back, of the copy
+// peak: the 4-rank kernel at P = 3 with U = 4 / 3 / 2 (126 / 80 / 64
+// registers for bf16): bf16 Mean 0.91 / 0.99 / 1.01, fp32 1.00 / 1.01 /
+// 1.01; the 8-rank kernel at P = 5, 6, 7 with U = 2 / 1: bf16 Mean 0.94 /
+// 0.96, 0.99 / 1.00, 1.01 / 1.02 (fp32 up by 0.00-0.01).
 __host__ __device__ constexpr int unroll_for(int PT) {
-  return PT < 0 ? unroll_for(-PT) : (PT == 0 ? 1 : (PT <= 4 ? 4 : (PT <= 8 ? 2 : 1)));
+  return PT == -4 ? 2 : PT == -8 ? 1 : PT < 0 ? unroll_for(-PT)
+         : (PT == 0 ? 1 : (PT <= 4 ? 4 : (PT <= 8 ? 2 : 1)));
 }
 // With the fused SGD step each vector also carries its fp32 master weights
 // and momentum (2 x E floats), all loaded up front: 2 vectors per thread for
