@@ -69,14 +69,15 @@ def parse():
     ap.add_argument("--sweep", action="store_true",
                     help="the full size/replica sweep instead: all-reduce (Sum, Mean) and "
                          "broadcast, 4 KiB .. 1 GiB per replica, P = 2, 4, 8, fp32 and bf16")
-    ap.add_argument("--case", choices=["ar", "rs", "ag", "bc", "zero1", "accfirst", "acc", "acclast",
-                                       "syncbn"],
+    ap.add_argument("--case", choices=["ar", "rs", "ag", "bc", "zero1", "sgd", "accfirst", "acc",
+                                       "acclast", "syncbn"],
                     help="time one collective alone (P=8, 256 MiB per replica; ViT-sized for "
-                         "zero1; one 25 MiB bf16 bucket for accfirst, the first micro-batch, acc, "
-                         "a later one before the last, and acclast, the last one fused with "
-                         "Mean + SGD) and print its GB/s; for profiling single kernels")
+                         "zero1; one 25 MiB bf16 bucket for sgd, the bucket step with Mean + SGD, "
+                         "accfirst, the first micro-batch, acc, a later one before the last, and "
+                         "acclast, the last one fused with Mean + SGD) and print its GB/s; for "
+                         "profiling single kernels")
     ap.add_argument("--case-ranks", type=int, default=8, choices=range(2, 17), metavar="P",
-                    help="P (2..16) for --case ar/rs/ag/bc/accfirst/acc/acclast")
+                    help="P (2..16) for --case ar/rs/ag/bc/sgd/accfirst/acc/acclast")
     ap.add_argument("--case-dtype", choices=["f32", "bf16"], default="f32",
                     help="element type for --case ar/rs/ag/bc")
     ap.add_argument("--case-mib", type=int, default=256,
@@ -1102,6 +1103,11 @@ def case_cpu_baseline(case, P, dtype_name, op_name, min_seconds=1.0):
         vs = [np.zeros(n // P, np.float32) for _ in range(P)]
         fn = lambda: oracle.sharded_sgd_step(g, params, ws, vs, 0.1, 0.9, oracle.MEAN)
         nbytes, sample = 4 * P * n + 16 * n, f"a flat unit of {n} bf16 elements"
+    elif case == "sgd":
+        g = [[workloads.replica_values("normal", "bf16", 100 + r, n, std=1e-3) for r in range(P)]]
+        w, v = np.zeros(n, np.float32), np.zeros(n, np.float32)
+        fn = lambda: oracle.bucket_all_reduce(g, op=oracle.MEAN, sgd=(0.1, 0.9, [w], [v], 1))
+        nbytes, sample = 4 * P * n + 16 * n, f"one bucket of {n} bf16 elements per replica"
     elif case in ("accfirst", "acc", "acclast"):
         g = [[workloads.replica_values("normal", "bf16", 100 + r, n, std=1e-3) for r in range(P)]]
         acc = [[np.zeros(n, np.float32) for _ in range(P)]]
@@ -1137,7 +1143,7 @@ def run_case(args):
     alone from a cold, clean L2 (us_cold, GBps_cold, frac_cold).  256 MiB
     per replica for ar / rs / ag / bc (P and the element type from
     --case-ranks and --case-dtype; P = 8, fp32 by default); one 25 MiB bf16
-    bucket for accfirst, acc and acclast (P from --case-ranks); the ViT-B/16 gradient
+    bucket for sgd, accfirst, acc and acclast (P from --case-ranks); the ViT-B/16 gradient
     set (bf16, P = 8) for zero1."""
     import torch
     import gradient_all_reduce_gb300 as gar
@@ -1146,7 +1152,7 @@ def run_case(args):
     torch.cuda.set_device(device)
     stream = torch.cuda.current_stream()
     flat = args.case in ("ar", "rs", "ag", "bc")
-    P = args.case_ranks if flat or args.case.startswith("acc") else 8
+    P = args.case_ranks if flat or args.case.startswith("acc") or args.case == "sgd" else 8
     comm = gar.ar_init(P, 0, gar.AR_MEAN)
     try:
         if flat:
@@ -1182,6 +1188,16 @@ def run_case(args):
             fn = lambda: gar.ar_sharded_sgd_step(comm, g, params, ws, vs, n, gar.AR_BF16, 0.1, 0.9,
                                                  gar.AR_MEAN, stream)
             nbytes, what = 4 * P * n + 16 * n, "ViT-B/16 flat unit, P=8 bf16"
+        elif args.case == "sgd":
+            n = (25 << 20) // 2
+            g = [torch.empty(n, dtype=torch.bfloat16, device=device) for _ in range(P)]
+            for r, x in enumerate(g):
+                wgpu.fill(x, "normal", 100 + r, std=1e-3)
+            w, v = torch.zeros(n, device=device), torch.zeros(n, device=device)
+            fn = lambda: gar.ar_bucket_all_reduce(comm, [g], [n], gar.AR_BF16, gar.AR_MEAN,
+                                                  sgd=(0.1, 0.9, [w], [v], 1), stream=stream)
+            nbytes = 4 * P * n + 16 * n
+            what = f"one 25 MiB bf16 bucket, P={P}, Mean + SGD with write-back"
         elif args.case in ("accfirst", "acc"):
             first = args.case == "accfirst"
             n = (25 << 20) // 2

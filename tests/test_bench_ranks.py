@@ -55,8 +55,8 @@ def test_reference_arm_runs_on_rank0_only():
     assert r.returncode == 0 and r.stdout.strip() == ""
 
 
-@pytest.mark.parametrize("case", ["ar", "rs", "ag", "bc", "zero1", "accfirst", "acc", "acclast",
-                                  "syncbn"])
+@pytest.mark.parametrize("case", ["ar", "rs", "ag", "bc", "zero1", "sgd", "accfirst", "acc",
+                                  "acclast", "syncbn"])
 def test_case_cpu_baseline_runs_every_case(case):
     """The oracle beside each --case line runs on the host for every case,
     at a P that is not a power of two, and reports a positive rate."""
