@@ -51,7 +51,11 @@ WORKLOAD = ("vit_b16_ddp_step: P=8 replicas x 86,567,656 bf16 grads, 8 x 25 MiB 
             "Mean all-reduce fused with SGD momentum (fp32 master), write-back")
 P_VIT = 8
 CAP = 25 << 20
-KERNEL_SOURCES = ["gar_device.cuh", "gar_kernels.cuh", "gar_launch.h", "gar_reduce.inc"]
+# Sources of the roofline kernel and of the host code that builds its launch
+# (segment table, combined launch): a committed DRAM figure holds only while
+# these hash to the value recorded when it was captured.
+KERNEL_SOURCES = ["gar_device.cuh", "gar_kernels.cuh", "gar_launch.h", "gar_reduce.inc",
+                  "gar_reducer.cu", "gar_api.cu", "gar_host.h"]
 
 
 def parse():
@@ -60,6 +64,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["gar", "reference"], default="gar")
+    ap.add_argument("--ref-budget", type=float, default=60.0, metavar="S",
+                    help="--impl reference: seconds of oracle work the timed and warm-up steps "
+                         "may take together; a step covers as much of the workload as fits")
     ap.add_argument("--no-sweep", action="store_true", help="skip the size/replica sweep")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
@@ -69,13 +76,13 @@ def parse():
     ap.add_argument("--sweep", action="store_true",
                     help="the full size/replica sweep instead: all-reduce (Sum, Mean) and "
                          "broadcast, 4 KiB .. 1 GiB per replica, P = 2, 4, 8, fp32 and bf16")
-    ap.add_argument("--case", choices=["ar", "rs", "ag", "bc", "zero1", "sgd", "accfirst", "acc",
-                                       "acclast", "syncbn"],
+    ap.add_argument("--case", choices=["ar", "rs", "ag", "bc", "tiny", "zero1", "sgd", "accfirst",
+                                       "acc", "acclast", "syncbn"],
                     help="time one collective alone (P=8, 256 MiB per replica; ViT-sized for "
                          "zero1; one 25 MiB bf16 bucket for sgd, the bucket step with Mean + SGD, "
                          "accfirst, the first micro-batch, acc, a later one before the last, and "
-                         "acclast, the last one fused with Mean + SGD) and print its GB/s; for "
-                         "profiling single kernels")
+                         "acclast, the last one fused with Mean + SGD; tiny is ar at P=4, 4 MiB "
+                         "fp32 per replica, Mean) and print its GB/s; for profiling single kernels")
     ap.add_argument("--case-ranks", type=int, default=8, choices=range(2, 17), metavar="P",
                     help="P (2..16) for --case ar/rs/ag/bc/sgd/accfirst/acc/acclast")
     ap.add_argument("--case-dtype", choices=["f32", "bf16"], default="f32",
@@ -184,6 +191,15 @@ def vit_layout():
 
 def vit_bytes(n: int, P: int = P_VIT) -> int:
     return 2 * P * n * 2 + 16 * n
+
+
+def vit_config(world: int) -> dict:
+    """The ``config`` of the ViT step's line (both arms print the same)."""
+    import workloads
+    return {"workload": WORKLOAD, "P": P_VIT, "params": sum(workloads.vit_b16_numels()),
+            "buckets": 8, "bucket_cap_mib": 25, "grad_dtype": "bf16", "accumulate": "fp32",
+            "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (4.155 GB moved per step, no flush)"}
 
 
 class VitStep:
@@ -441,14 +457,17 @@ class E2EStep:
         red.finalize(stream)
 
     def finish(self, stream):
-        """Order ``stream`` after every copy-out issued so far."""
-        stream.wait_stream(self.out_stream)
-        stream.wait_stream(self.event_stream)
+        """Order ``stream`` after every copy issued so far (the drain of a
+        region)."""
+        for cs in self.copy_streams + [self.out_stream, self.event_stream]:
+            stream.wait_stream(cs)
 
     def copies_only(self, stream):
         """The step's host transfers alone, on the same streams and in the
         same pieces: every bucket's replicas in, its weights out, no kernel.
-        Their time is the host link's bound on the end-to-end step."""
+        Their time is the host link's bound on the end-to-end step.  As in
+        ``step``, a bucket's copy-in waits for nothing but its own stream
+        and a region ends with ``finish``."""
         import torch
         vs = self.vs
         k = 0
@@ -460,14 +479,15 @@ class E2EStep:
                     vs.grads[r][lo:hi].copy_(self.host_g[r][lo:hi], non_blocking=True)
             with torch.cuda.stream(self.out_stream):
                 self.host_w[lo:hi].copy_(vs.w[lo:hi], non_blocking=True)
-        for cs in self.copy_streams + [self.out_stream]:
-            stream.wait_stream(cs)
 
 
 def time_e2e(args, device, stream):
-    """The ViT step end to end from pinned host buffers (E2EStep): after 3
-    warm-up steps, three regions of K steps, each under one event pair; the
-    median region gives the value."""
+    """The ViT step end to end from pinned host buffers (E2EStep), and the
+    same transfers without the kernels (the host link's bound), measured
+    alike: after 3 warm-up steps, three regions of K steps each, every region
+    under one event pair with the same fill (``start``) and drain
+    (``finish``), interleaved so that both meet the same traffic on the
+    shared host; each figure is the median region."""
     import torch
     import gradient_all_reduce_gb300 as gar
     comm = gar.ar_init(P_VIT, device.index, gar.AR_MEAN)
@@ -476,53 +496,43 @@ def time_e2e(args, device, stream):
         vs = VitStep(comm, device)
         e2e = E2EStep(vs, device)
         steps = max(3, min(args.steps, 50))
-        # Three regions of `steps` steps each; the value is the median region.
-        # The host and its link are shared with other jobs, and one region
-        # that meets their traffic runs up to 15 % slower.
-        regions = []
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+
+        def region(fn):
+            t0.record(stream)
+            e2e.start(stream)
+            for _ in range(steps):
+                fn(stream)
+            e2e.finish(stream)
+            t1.record(stream)
+            torch.cuda.synchronize(device)
+            return t0.elapsed_time(t1) / 1e3 / steps
+
+        full, link = [], []
         with torch.cuda.stream(stream):
             for _ in range(3):
                 e2e.step(stream)
-            torch.cuda.synchronize(device)
-            t0 = torch.cuda.Event(enable_timing=True)
-            t1 = torch.cuda.Event(enable_timing=True)
-            for _ in range(3):
-                t0.record(stream)
-                e2e.start(stream)
-                for _ in range(steps):
-                    e2e.step(stream)
-                e2e.finish(stream)
-                t1.record(stream)
-                torch.cuda.synchronize(device)
-                regions.append(t0.elapsed_time(t1) / 1e3)
-        el = statistics.median(regions)
-        # The host link alone, moving the same bytes the same way: the
-        # ceiling of this measurement on this machine.  The host and its
-        # link are shared, so the region runs three times and the fastest
-        # counts (one run on a busy host measured twice the usual time).
-        link_steps = max(3, steps // 5)
-        link_runs = []
-        with torch.cuda.stream(stream):
-            e2e.copies_only(stream)
+                e2e.copies_only(stream)
+            e2e.finish(stream)
             torch.cuda.synchronize(device)
             for _ in range(3):
-                t0.record(stream)
-                e2e.start(stream)
-                for _ in range(link_steps):
-                    e2e.copies_only(stream)
-                t1.record(stream)
-                torch.cuda.synchronize(device)
-                link_runs.append(t0.elapsed_time(t1) / 1e3 / link_steps)
-        link = min(link_runs)
-        value = vs.step_bytes * steps / el / 1e9
+                full.append(region(e2e.step))
+                link.append(region(e2e.copies_only))
+        el, ln = statistics.median(full), statistics.median(link)
+        value = vs.step_bytes / el / 1e9
+        bound = vs.step_bytes / ln / 1e9
         return {"value": value, "unit": "GB/s",
                 "h2d_bytes_per_step": 2 * vs.n * P_VIT, "d2h_bytes_per_step": 4 * vs.n,
-                "steps": steps, "ms_per_step": el / steps * 1e3,
-                "ms_per_step_regions": [round(x / steps * 1e3, 3) for x in regions],
-                "link_only_ms_per_step": link * 1e3,
-                "link_only_ms_per_step_runs": [round(x * 1e3, 3) for x in link_runs],
-                "link_bound_GBps": vs.step_bytes / link / 1e9,
-                "frac_of_link_bound": value / (vs.step_bytes / link / 1e9),
+                "steps": steps, "ms_per_step": el * 1e3,
+                "ms_per_step_regions": [round(x * 1e3, 3) for x in full],
+                "link_only_ms_per_step": ln * 1e3,
+                "link_only_ms_per_step_regions": [round(x * 1e3, 3) for x in link],
+                "link_bound_GBps": bound,
+                "frac_of_link_bound": value / bound,
+                "statistic": ("median of three regions of `steps` steps for both the step and "
+                              "the link-only transfers, each region with the same fill and drain, "
+                              "the two kinds interleaved"),
                 "path": ("ar_reducer_* with per-bucket H2D on 4 copy streams and per-bucket D2H "
                          "of the updated weights after ar_reducer_wait_bucket; consecutive steps "
                          "ordered per bucket, not per step")}
@@ -720,64 +730,145 @@ def time_sweep(device, stream):
 
 
 # -------------------------------------------------------------- CPU oracle
+# The oracle is plain, single-threaded code.  Its Mean + SGD step is
+# elementwise, so the unchanged oracle function called from several host
+# threads on disjoint contiguous element ranges computes exactly the bits
+# of one call over all elements (ctypes releases the interpreter lock for
+# the duration of each call).  Nothing here imports the CUDA library.
 
-def oracle_sample(elems: int, offset: int = 0):
-    """Host inputs of a contiguous sample of the ViT step: ``elems`` gradient
-    elements of every replica starting at ``offset``, with their master
-    weights and zero momentum."""
+def host_cores() -> int:
+    """Host CPUs this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def vit_numel() -> int:
     import workloads
-    grads = [workloads.replica_values("normal", "bf16", workloads.VIT_GRAD_SEED + r, elems,
-                                      std=workloads.VIT_GRAD_STD, start=offset)
-             for r in range(P_VIT)]
-    w = workloads.normal_f32(workloads.VIT_MASTER_SEED, elems, std=workloads.VIT_MASTER_STD,
-                             start=offset)
-    return grads, w, np.zeros(elems, np.float32)
+    return sum(workloads.vit_b16_numels())
 
 
-def cpu_oracle_rate(elems: int, min_seconds: float):
-    """Run the oracle's bucketed Mean + SGD on the sample until at least
-    min_seconds have passed; returns (GB/s, repetitions, seconds)."""
+def oracle_inputs(elems: int, offset: int = 0, threads: int = 1):
+    """Host inputs of ``elems`` contiguous gradient elements of the ViT step
+    starting at ``offset``: every replica's bf16 gradients, the fp32 master
+    weights and zero momentum.  Drawn chunk by chunk over ``threads``."""
+    from concurrent.futures import ThreadPoolExecutor
+    import workloads
+    grads = [np.empty(elems, np.uint16) for _ in range(P_VIT)]
+    w = np.empty(elems, np.float32)
+    v = np.zeros(elems, np.float32)
+    chunk = 1 << 22
+
+    def fill(lo):
+        hi = min(elems, lo + chunk)
+        for r in range(P_VIT):
+            grads[r][lo:hi] = workloads.replica_values(
+                "normal", "bf16", workloads.VIT_GRAD_SEED + r, hi - lo,
+                std=workloads.VIT_GRAD_STD, start=offset + lo)
+        w[lo:hi] = workloads.normal_f32(workloads.VIT_MASTER_SEED, hi - lo,
+                                        std=workloads.VIT_MASTER_STD, start=offset + lo)
+
+    with ThreadPoolExecutor(max(1, threads)) as ex:
+        list(ex.map(fill, range(0, elems, chunk)))
+    return grads, w, v
+
+
+def oracle_step(inputs, threads: int = 1, pool=None) -> None:
+    """One Mean + SGD step (momentum 0.9, lr 0.1, write-back) of the oracle
+    over all of ``inputs``, in place: the oracle's bucket all-reduce called
+    once per thread on ``threads`` disjoint contiguous element ranges."""
     import oracle
-    grads, w, v = oracle_sample(elems)
-    reps, spent = 0, 0.0
-    while spent < min_seconds or reps == 0:
-        t0 = time.perf_counter()
+    grads, w, v = inputs
+    n = w.size
+    if threads <= 1 or pool is None:
         oracle.bucket_all_reduce([grads], op=oracle.MEAN, sgd=(0.1, 0.9, [w], [v], 1))
-        spent += time.perf_counter() - t0
-        reps += 1
-    return vit_bytes(elems) * reps / spent / 1e9, reps, spent
+        return
+    cuts = [n * k // threads for k in range(threads + 1)]
+
+    def run(k):
+        lo, hi = cuts[k], cuts[k + 1]
+        if hi > lo:
+            oracle.bucket_all_reduce([[g[lo:hi] for g in grads]], op=oracle.MEAN,
+                                     sgd=(0.1, 0.9, [w[lo:hi]], [v[lo:hi]], 1))
+
+    list(pool.map(run, range(threads)))
+
+
+def oracle_rate(inputs, threads: int, min_seconds: float, min_reps: int = 1):
+    """Repeat oracle_step until min_seconds (and min_reps) have passed;
+    returns (GB/s of algorithmic bytes, repetitions, seconds)."""
+    from concurrent.futures import ThreadPoolExecutor
+    import oracle
+    oracle.lib()
+    n = inputs[1].size
+    with ThreadPoolExecutor(threads) as pool:
+        oracle_step(inputs, threads, pool)            # first touch of every page
+        reps, spent = 0, 0.0
+        while spent < min_seconds or reps < min_reps:
+            t0 = time.perf_counter()
+            oracle_step(inputs, threads, pool)
+            spent += time.perf_counter() - t0
+            reps += 1
+    return vit_bytes(n) * reps / spent / 1e9, reps, spent
+
+
+def cpu_baseline_full(min_seconds: float = 3.0):
+    """The oracle on the whole ViT step (every one of the 86,567,656
+    gradient elements of all 8 replicas), on all host cores and on one."""
+    import oracle
+    oracle.build()
+    cores = host_cores()
+    n = vit_numel()
+    inputs = oracle_inputs(n, threads=cores)
+    rate_all, reps_all, spent_all = oracle_rate(inputs, cores, min_seconds, min_reps=3)
+    rate_one, reps_one, spent_one = oracle_rate(inputs, 1, min_seconds, min_reps=1)
+    what = (f"the oracle's Mean + SGD step (write-back) over all {n:,} gradient elements of "
+            f"all {P_VIT} replicas")
+    return {"value": rate_all, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": (f"{reps_all} runs of {what}, the unchanged oracle function called from "
+                       f"{cores} host threads on disjoint contiguous element ranges, "
+                       f"{spent_all:.1f} s"),
+            "single_thread": {"value": rate_one, "unit": "GB/s", "cores": 1,
+                              "sample": f"{reps_one} runs of {what} in one call, {spent_one:.1f} s"}}
 
 
 def run_reference(args):
-    """The CPU oracle timed on the host cores, on bounded samples of the ViT
-    step; rank 0 only."""
+    """The CPU oracle, timed on all host cores: each step is the oracle's
+    Mean + SGD over the whole ViT step when K + W such steps fit a bounded
+    budget, else over one contiguous slice of it; rank 0 only."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
     import oracle
     oracle.build()
-    n_total = sum(vit_layout()[0])
-    probe_elems = 1 << 20
-    rate, _, _ = cpu_oracle_rate(probe_elems, 0.5)
-    budget = 60.0                                   # seconds of oracle work in the timed steps
-    per_step_s = budget / max(1, args.steps + args.warmup)
-    elems = int(max(4096, min(n_total, rate * 1e9 * per_step_s / vit_bytes(1))))
-    grads, w, v = oracle_sample(elems)
-    for _ in range(args.warmup):
-        oracle.bucket_all_reduce([grads], op=oracle.MEAN, sgd=(0.1, 0.9, [w], [v], 1))
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle.bucket_all_reduce([grads], op=oracle.MEAN, sgd=(0.1, 0.9, [w], [v], 1))
-    el = time.perf_counter() - t0
+    cores = host_cores()
+    n_total = vit_numel()
+    probe = oracle_inputs(1 << 22, threads=cores)
+    rate, _, _ = oracle_rate(probe, cores, 0.5)
+    del probe
+    per_step_s = args.ref_budget / max(1, args.steps + args.warmup)
+    elems = int(max(1 << 16, min(n_total, rate * 1e9 * per_step_s / vit_bytes(1))))
+    inputs = oracle_inputs(elems, threads=cores)
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(cores) as pool:
+        for _ in range(args.warmup):
+            oracle_step(inputs, cores, pool)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            oracle_step(inputs, cores, pool)
+        el = time.perf_counter() - t0
     value = vit_bytes(elems) * args.steps / el / 1e9
-    sample = (f"each step: the oracle's Mean + SGD on {elems:,} of the {n_total:,} gradient "
-              f"elements of all {P_VIT} replicas (one contiguous slice), single thread")
+    part = ("all" if elems == n_total else f"the first {elems:,} of the")
+    sample = (f"each step: the oracle's Mean + SGD step (write-back) on {part} {n_total:,} "
+              f"gradient elements of all {P_VIT} replicas, the unchanged oracle function called "
+              f"from {cores} host threads on disjoint contiguous element ranges")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "sample_elements": elems},
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "config": vit_config(args.gpus),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -1151,6 +1242,9 @@ def run_case(args):
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
     stream = torch.cuda.current_stream()
+    if args.case == "tiny":   # the tiny all-reduce: P = 4, 2**20 fp32 per replica, Mean, in place
+        args.case, args.case_ranks, args.case_mib = "ar", 4, 4
+        args.case_dtype, args.case_op = "f32", "mean"
     flat = args.case in ("ar", "rs", "ag", "bc")
     P = args.case_ranks if flat or args.case.startswith("acc") or args.case == "sgd" else 8
     comm = gar.ar_init(P, 0, gar.AR_MEAN)
@@ -1167,13 +1261,14 @@ def run_case(args):
             sh = n // P
             rs = [torch.empty(sh, dtype=tdt, device=device) for _ in range(P)]
             ins = [x[r * sh:(r + 1) * sh] for r, x in enumerate(xs)]
-            fn, nbytes = {
-                "ar": (lambda: gar.ar_all_reduce(comm, xs, xs, n, dt, op, stream), 2 * P * n * es),
-                "rs": (lambda: gar.ar_reduce_scatter(comm, xs, rs, n, dt, op, stream),
+            prep, nbytes = {
+                "ar": (gar.PreparedCall("ar_all_reduce", comm, xs, xs, n, dt, op), 2 * P * n * es),
+                "rs": (gar.PreparedCall("ar_reduce_scatter", comm, xs, rs, n, dt, op),
                        (P + 1) * n * es),
-                "ag": (lambda: gar.ar_all_gather(comm, ins, xs, n, dt, stream), P * n * es),
-                "bc": (lambda: gar.ar_broadcast(comm, xs, n, dt, 0, stream), P * n * es),
+                "ag": (gar.PreparedCall("ar_all_gather", comm, ins, xs, n, dt), P * n * es),
+                "bc": (gar.PreparedCall("ar_broadcast", comm, xs, n, dt, 0), P * n * es),
             }[args.case]
+            fn = lambda: prep(stream)
             what = f"P={P} {args.case_dtype} {args.case_mib} MiB per replica"
             if args.case in ("ar", "rs"):
                 what += f", {op_name}"
@@ -1256,6 +1351,31 @@ def run_case(args):
         line = {"case": args.case, "workload": what, "us": t * 1e6, "GBps": nbytes / t / 1e9,
                 "frac": nbytes / t / 1e9 / peak, "us_cold": cold * 1e6,
                 "GBps_cold": nbytes / cold / 1e9, "frac_cold": nbytes / cold / 1e9 / peak}
+        if flat:
+            # The same calls replayed from one CUDA graph of K calls: no host
+            # time between launches, consecutive kernels chained by
+            # programmatic dependent launch (below ~40 MB per call the
+            # operands stay in L2 from one call to the next).
+            side = torch.cuda.Stream(device)
+            side.wait_stream(stream)
+            prep(side)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                cur = torch.cuda.current_stream()
+                for _ in range(args.steps):
+                    prep(cur)
+            graph.replay()
+            torch.cuda.synchronize()
+            e0.record(stream)
+            with torch.cuda.stream(stream):
+                graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            tg = e0.elapsed_time(e1) / 1e3 / args.steps
+            line.update({"us_graph": tg * 1e6, "GBps_graph": nbytes / tg / 1e9,
+                         "frac_graph": nbytes / tg / 1e9 / peak})
+            del graph
         if not args.no_cpu:
             line["cpu_baseline"] = case_cpu_baseline(
                 args.case, P, args.case_dtype if flat else "bf16",
@@ -1307,10 +1427,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "P": P_VIT, "params": res["n"], "buckets": 8,
-                   "bucket_cap_mib": 25, "grad_dtype": "bf16", "accumulate": "fp32",
-                   "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (4.155 GB moved per step, no flush)"},
+        "config": vit_config(world),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "kernel": ("k_reduce<BF16, P=8, SGD, CapLarge>: one launch over the 8 "
@@ -1343,15 +1460,7 @@ def main():
     if rank == 0 and not args.no_sweep:
         line["sweep"] = time_sweep(device, stream)
     if rank == 0 and not args.no_cpu:
-        import oracle
-        oracle.build()
-        elems = 8 << 20
-        rate, reps, spent = cpu_oracle_rate(elems, 10.0)
-        line["cpu_baseline"] = {
-            "value": rate, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": (f"{reps} runs of the oracle's Mean + SGD on the first {elems:,} of the "
-                       f"{res['n']:,} gradient elements of all {P_VIT} replicas, single "
-                       f"thread, {spent:.1f} s")}
+        line["cpu_baseline"] = cpu_baseline_full()
     barrier(world)
     if rank == 0:
         print(json.dumps(line), flush=True)
