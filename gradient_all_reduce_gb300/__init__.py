@@ -10,6 +10,9 @@ torch stream (the legacy default stream when torch is not imported).
 The library must be built first (``gradient_all_reduce_gb300.build.build()``
 or ``__graft_entry__.build()``).  It is loaded on first use; without it
 every call raises ImportError -- there is no fallback implementation.
+``GAR_LIBRARY=debug`` in the environment loads the debug build instead
+(``build(debug=True)``: the same library with the kernels' device-side
+index checks compiled in); any other value is taken as the library's path.
 """
 from __future__ import annotations
 
@@ -20,7 +23,18 @@ from typing import Sequence
 
 _LIB_PATH = Path(__file__).resolve().parent / "libgar.so"
 
-AR_OK, AR_ERR_INVALID_ARG, AR_ERR_UNSUPPORTED, AR_ERR_CUDA, AR_ERR_TIMEOUT, AR_ERR_STATE = range(6)
+
+def _lib_path() -> Path:
+    import os
+    choice = os.environ.get("GAR_LIBRARY", "")
+    if choice == "":
+        return _LIB_PATH
+    if choice == "debug":
+        return _LIB_PATH.with_name("libgar_debug.so")
+    return Path(choice)
+
+AR_OK, AR_ERR_INVALID_ARG, AR_ERR_UNSUPPORTED, AR_ERR_CUDA, AR_ERR_TIMEOUT, AR_ERR_STATE, \
+    AR_ERR_DEVICE_CHECK = range(7)
 AR_OP_DEFAULT, AR_SUM, AR_MEAN = -1, 0, 1
 AR_F32, AR_BF16 = 0, 1
 AR_MAX_RANKS = 16
@@ -53,10 +67,11 @@ class ar_sgd_t(ctypes.Structure):
 
 
 def _load() -> ctypes.CDLL:
-    if not _LIB_PATH.exists():
-        raise ImportError(f"{_LIB_PATH} is missing: build it with "
+    path = _lib_path()
+    if not path.exists():
+        raise ImportError(f"{path} is missing: build it with "
                           "gradient_all_reduce_gb300.build.build()")
-    lib = ctypes.CDLL(str(_LIB_PATH))
+    lib = ctypes.CDLL(str(path))
     P = ctypes.c_void_p
     PP = ctypes.POINTER(ctypes.c_void_p)
     sigs = {

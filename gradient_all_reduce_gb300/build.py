@@ -20,11 +20,15 @@ ROOT = PKG.parent
 CSRC = PKG / "csrc"
 INCLUDE = ROOT / "include"
 LIB = PKG / "libgar.so"
+LIB_DEBUG = PKG / "libgar_debug.so"
 
-UNITS = ["gar_api.cu", "gar_reducer.cu", "gar_reduce_f32.cu", "gar_reduce_bf16.cu", "gar_copy.cu"]
+UNITS = ["gar_api.cu", "gar_reducer.cu", "gar_copy.cu", "gar_reduce_f32.cu", "gar_reduce_bf16.cu",
+         "gar_sgd_f32.cu", "gar_sgd_bf16.cu", "gar_acc_f32.cu", "gar_acc_bf16.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+# The kernel images are stored compressed (many specialisations, each
+# loaded on first use).
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
-                     "-Xcompiler", "-O2", f"-I{INCLUDE}", f"-I{CSRC}"]
+                     "-Xcompiler", "-O2", "-Xfatbin", "-compress-all", f"-I{INCLUDE}", f"-I{CSRC}"]
 
 
 def nvcc() -> str:
@@ -44,13 +48,19 @@ def _stamp(extra: list[str]) -> str:
     return h.hexdigest()[:16]
 
 
-def build(verbose: bool = False, extra_flags: list[str] | None = None, force: bool = False) -> Path:
-    """Compile every translation unit and link ``libgar.so``; returns its path."""
+def build(verbose: bool = False, extra_flags: list[str] | None = None, force: bool = False,
+          debug: bool = False) -> Path:
+    """Compile every translation unit and link ``libgar.so``; returns its path.
+    ``debug``: build ``libgar_debug.so`` instead, with the kernels' device-side
+    index checks compiled in (GAR_DEBUG=1)."""
     extra = list(extra_flags or [])
-    stamp_file = LIB.with_suffix(".stamp")
+    lib = LIB_DEBUG if debug else LIB
+    if debug:
+        extra.append("-DGAR_DEBUG=1")
+    stamp_file = lib.with_suffix(".stamp")
     want = _stamp(extra)
-    if not force and LIB.exists() and stamp_file.exists() and stamp_file.read_text() == want:
-        return LIB
+    if not force and lib.exists() and stamp_file.exists() and stamp_file.read_text() == want:
+        return lib
     cc = nvcc()
     with tempfile.TemporaryDirectory(prefix="gar_build_") as tmp:
         objs = [Path(tmp) / (Path(u).stem + ".o") for u in UNITS]
@@ -74,10 +84,10 @@ def build(verbose: bool = False, extra_flags: list[str] | None = None, force: bo
         if res.returncode != 0:
             sys.stderr.write(res.stdout + res.stderr)
             raise RuntimeError("link failed: " + " ".join(cmd))
-        shutil.copyfile(tmp_lib, str(LIB) + ".tmp")
-        os.replace(str(LIB) + ".tmp", LIB)
+        shutil.copyfile(tmp_lib, str(lib) + ".tmp")
+        os.replace(str(lib) + ".tmp", lib)
     stamp_file.write_text(want)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

@@ -93,9 +93,14 @@ const char* ar_status_string(ar_status_t s) {
     case AR_ERR_CUDA: return "AR_ERR_CUDA: CUDA call or kernel launch failed";
     case AR_ERR_TIMEOUT: return "AR_ERR_TIMEOUT: a device-side bounded wait gave up";
     case AR_ERR_STATE: return "AR_ERR_STATE: comm is not live";
+    case AR_ERR_DEVICE_CHECK:
+      return "AR_ERR_DEVICE_CHECK: a device-side index check of a debug build failed";
   }
   return "unknown ar_status_t";
 }
+
+// Bytes per replica below which a flat all-reduce takes one vector per thread.
+constexpr uint64_t kSmallAllReduceBytes = 16ull << 20;
 
 ar_status_t ar_init(ar_comm_t* comm, int nranks, int cuda_device, ar_op_t default_op) {
   if (comm == nullptr) return AR_ERR_INVALID_ARG;
@@ -136,6 +141,12 @@ ar_status_t ar_init(ar_comm_t* comm, int nranks, int cuda_device, ar_op_t defaul
   // replica: 1.01-1.08 of the copy peak against 0.85-1.02).
   env = std::getenv("GAR_COPY");
   c->copy_tma = env != nullptr && std::strcmp(env, "tma") == 0;
+  // A flat all-reduce of fewer bytes per replica than this runs one vector
+  // per thread (four times the CTAs of the default unroll at P <= 4), so
+  // that a message of a few MB still spreads over every SM.
+  c->small_bytes = kSmallAllReduceBytes;
+  env = std::getenv("GAR_SMALL_ALL_REDUCE_BYTES");
+  if (env != nullptr) c->small_bytes = std::strtoull(env, nullptr, 10);
   if (cudaMalloc(&c->d_status, sizeof(uint32_t)) != cudaSuccess) {
     delete c;
     return AR_ERR_CUDA;
@@ -174,6 +185,7 @@ ar_status_t ar_get_async_error(ar_comm_t comm) {
   uint32_t s = 0;
   if (cudaMemcpy(&s, comm->d_status, sizeof s, cudaMemcpyDeviceToHost) != cudaSuccess)
     return AR_ERR_CUDA;
+  if (s & gar::kStatusBounds) return AR_ERR_DEVICE_CHECK;
   if (s != 0) return AR_ERR_TIMEOUT;
   return cudaPeekAtLastError() == cudaSuccess ? AR_OK : AR_ERR_CUDA;
 }
@@ -219,12 +231,14 @@ ar_status_t ar_all_reduce(ar_comm_t comm, const void* const* send, void* const* 
   init_table(t, P, P, 2 * P, P, rop == AR_MEAN);
   const bool tma = choose_tma(comm, P, false, es);
   if (tma) set_tma(t, comm, false, es);
+  if (!tma && bytes < comm->small_bytes) t.unroll = 1;
   void* ptrs[2 * AR_MAX_RANKS];
   for (int r = 0; r < P; ++r) {
     ptrs[r] = const_cast<void*>(send[r]);
     ptrs[P + r] = recv[r];
   }
-  if (!add_segment(t, ptrs, count, gar::reduce_tile(P, int(es), tma), vec_flag(ptrs, 2 * P)))
+  if (!add_segment(t, ptrs, count, gar::reduce_tile(P, int(es), tma, false, t.unroll),
+                   vec_flag(ptrs, 2 * P)))
     return AR_ERR_INVALID_ARG;
   return run_reduce(comm, dtype, false, t, static_cast<cudaStream_t>(stream));
 }
@@ -466,6 +480,7 @@ ar_status_t ar_bucket_accumulate(ar_comm_t comm, const ar_bucket_t* grads, const
   // One segment per (tensor, rank): ptr = {gradient, accumulator}.
   auto run = [&](auto& tab, int k0, int k1) -> ar_status_t {
     init_table(tab, 1, 1, 2, 1, false);
+    tab.status = comm->d_status;
     tab.scale = acc->scale;
     tab.first = acc->first ? 1 : 0;
     for (int k = k0; k < k1; ++k) {
@@ -515,6 +530,7 @@ ar_status_t ar_bucket_all_reduce_accumulated(ar_comm_t comm, const ar_bucket_t* 
   // One segment per tensor: ptr = {P gradient replicas, P accumulators}.
   auto run = [&](auto& tab, int t0, int t1) -> ar_status_t {
     init_table(tab, P, P, 2 * P, 0, rop == AR_MEAN);
+    tab.status = comm->d_status;
     tab.scale = acc->scale;
     tab.first = acc->first ? 1 : 0;
     if (sgd != nullptr) {
@@ -669,6 +685,7 @@ ar_status_t ar_syncbn_stats(ar_comm_t comm, const float* const* sum, const float
   a.eps = double(eps);
   a.channels = channels;
   a.np = P;
+  a.status = comm->d_status;
   const gar::LaunchCtx ctx{comm->device, comm->num_sms, static_cast<cudaStream_t>(stream), false,
                            comm->pdl};
   return from_cuda(gar::launch_syncbn_stats(ctx, a));
@@ -709,9 +726,13 @@ ar_status_t ar_bucket_plan(int ntensors, const size_t* nbytes, size_t cap_bytes,
 // the file-scope array below instead of in memory from cudaMalloc.
 // Scratch of ar_all_reduce_noalloc: 256 bytes on every GPU that loads the
 // library, held until the process exits.  Word 0 is the status word of the
-// pipeline's bounded waits (0 = no wait gave up, 1 = one did); a call needs
-// that one word.
+// pipeline's bounded waits (0 = no wait gave up, 1 = one did).  A call needs
+// that one word whatever its arguments, so no call can need more than the
+// array holds; the static_assert keeps it that way.
 constexpr size_t kNoAllocScratchBytes = 256;
+constexpr size_t kNoAllocCallScratchBytes = sizeof(uint32_t);
+static_assert(kNoAllocCallScratchBytes <= kNoAllocScratchBytes,
+              "ar_all_reduce_noalloc needs more scratch than its static array holds");
 static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocScratchBytes / sizeof(uint32_t)];
 
 namespace {
@@ -721,35 +742,38 @@ constexpr int kNoAllocMaxDevices = 64;
 struct NoAllocDevice {
   bool ready = false;
   int num_sms = 0;
-  uint32_t* scratch = nullptr;  // device address of g_noalloc_scratch on this device
 };
 
 std::mutex g_noalloc_mu;
 NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
 
-// Set-up, once per device, with that device current: check the device and
+// Set-up with the device current: check the device (once per device), and
 // look up the device address of the scratch array (the host-side name of
-// the array is only a stand-in, not an address a kernel can use).
-ar_status_t noalloc_setup(int dev, NoAllocDevice* out) {
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  NoAllocDevice& d = g_noalloc_dev[dev];
-  if (!d.ready) {
-    int major = 0, minor = 0, sms = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return AR_ERR_CUDA;
-    if (major != 10 || minor != 3) return AR_ERR_UNSUPPORTED;
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
-      cudaGetLastError();
-      return AR_ERR_CUDA;
+// the array is only a stand-in, not an address a kernel can use).  The
+// address is looked up on every call, which allocates nothing, so a
+// context created anew (after cudaDeviceReset) is served its own address.
+ar_status_t noalloc_setup(int dev, int* num_sms, uint32_t** scratch) {
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    NoAllocDevice& d = g_noalloc_dev[dev];
+    if (!d.ready) {
+      int major = 0, minor = 0, sms = 0;
+      if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return AR_ERR_CUDA;
+      if (major != 10 || minor != 3) return AR_ERR_UNSUPPORTED;
+      d.num_sms = sms;
+      d.ready = true;
     }
-    d.scratch = static_cast<uint32_t*>(p);
-    d.num_sms = sms;
-    d.ready = true;
+    *num_sms = d.num_sms;
   }
-  *out = d;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+    cudaGetLastError();
+    return AR_ERR_CUDA;
+  }
+  *scratch = static_cast<uint32_t*>(p);
   return AR_OK;
 }
 
@@ -766,23 +790,22 @@ extern "C" ar_status_t ar_all_reduce_noalloc(int nranks, const void* const* send
   size_t bytes;
   if (!mul_ok(count, es, &bytes)) return AR_ERR_INVALID_ARG;
   if (count == 0) return AR_OK;
-  // The call's scratch: one status word for its one launch.
-  if (sizeof(uint32_t) > kNoAllocScratchBytes) return AR_ERR_INVALID_ARG;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
     return AR_ERR_CUDA;
   }
   if (dev < 0 || dev >= kNoAllocMaxDevices) return AR_ERR_UNSUPPORTED;
-  NoAllocDevice d;
-  ar_status_t st = noalloc_setup(dev, &d);
+  int num_sms = 0;
+  uint32_t* scratch = nullptr;
+  ar_status_t st = noalloc_setup(dev, &num_sms, &scratch);
   if (st != AR_OK) return st;
 
   // The same argument checks as ar_all_reduce, against the current device.
   ar_comm_s view{};
   view.nranks = P;
   view.device = dev;
-  view.num_sms = d.num_sms;
+  view.num_sms = num_sms;
   const char* env = std::getenv("GAR_POINTER_CHECKS");
   view.check_pointers = !(env != nullptr && std::strcmp(env, "0") == 0);
   for (int r = 0; r < P; ++r) {
@@ -803,7 +826,7 @@ extern "C" ar_status_t ar_all_reduce_noalloc(int nranks, const void* const* send
   init_table(t, P, P, 2 * P, P, op == AR_MEAN);
   t.stages = gar::tma_stages(P, false, int(es));
   t.stage_bytes = gar::tma_stage_bytes(P, false, 16 / int(es));
-  t.status = d.scratch;
+  t.status = scratch;
   if (t.stages < 2) return AR_ERR_UNSUPPORTED;
   void* ptrs[2 * AR_MAX_RANKS];
   for (int r = 0; r < P; ++r) {
@@ -814,8 +837,8 @@ extern "C" ar_status_t ar_all_reduce_noalloc(int nranks, const void* const* send
     return AR_ERR_INVALID_ARG;
   const cudaStream_t strm = static_cast<cudaStream_t>(stream);
   // The status word keeps the previous call's value: clear it first.
-  if (cudaMemsetAsync(d.scratch, 0, sizeof(uint32_t), strm) != cudaSuccess) return AR_ERR_CUDA;
-  const gar::LaunchCtx ctx{dev, d.num_sms, strm, true, true};
+  if (cudaMemsetAsync(scratch, 0, kNoAllocCallScratchBytes, strm) != cudaSuccess) return AR_ERR_CUDA;
+  const gar::LaunchCtx ctx{dev, num_sms, strm, true, true};
   return from_cuda(dtype == AR_F32 ? gar::launch_reduce_f32<CapSmall>(ctx, false, t)
                                    : gar::launch_reduce_bf16<CapSmall>(ctx, false, t));
 }

@@ -11,6 +11,33 @@ namespace gar {
 constexpr int kMaxRanks = 16;
 constexpr int kThreads = 256;  // threads per CTA of every kernel
 
+// Bits of a comm's device status word.
+constexpr uint32_t kStatusTimeout = 1u;  // a bounded wait gave up
+constexpr uint32_t kStatusBounds = 2u;   // a debug-build index check failed
+
+// Device-side index checks of a debug build (compiled with GAR_DEBUG=1): a
+// kernel checks, before an access, that the index it is about to use lies
+// inside the segment, channel range or table that the launch describes.  A
+// failed check sets kStatusBounds in the status word and the thread leaves
+// the kernel without the access -- it never traps, so the context stays
+// usable and the host reads the failure with ar_get_async_error.  Only the
+// kernels without block-wide barriers carry checks (a thread that leaves
+// early would strand a barrier).  A release build compiles every check
+// away.
+#ifndef GAR_DEBUG
+#define GAR_DEBUG 0
+#endif
+#if GAR_DEBUG
+__device__ __forceinline__ bool dcheck(bool ok, uint32_t* status) {
+  if (!ok && status != nullptr) atomicOr(status, kStatusBounds);
+  return ok;
+}
+#define GAR_CHECK(cond, status) \
+  if (!::gar::dcheck((cond), (status))) return
+#else
+#define GAR_CHECK(cond, status) ((void)0)
+#endif
+
 // ------------------------------------------------------------ memory ops
 // Every replica value is read exactly once and written at most once per
 // call, so loads bypass L1 (no reuse) and stores are streaming.  In place,
@@ -29,9 +56,19 @@ constexpr int kThreads = 256;  // threads per CTA of every kernel
 #define GAR_ST_STREAMING 1
 #endif
 
+// GAR_LD_COHERENT 1 loads the replicas through the coherent path
+// (ld.global.L1::no_allocate) instead of the non-coherent one.
+#ifndef GAR_LD_COHERENT
+#define GAR_LD_COHERENT 0
+#endif
+
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
   uint4 r;
-#if GAR_LD_PREFETCH
+#if GAR_LD_COHERENT
+  asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+#elif GAR_LD_PREFETCH
   asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p));
@@ -222,10 +259,11 @@ __device__ __forceinline__ float div_small_bf16(float x, float d, float r) {
 // Mean: one correctly rounded fp32 division by P.  For P a power of two
 // the product with the exact reciprocal is the same correctly rounded
 // quotient, so powers of two multiply instead (decided at compile time for
-// a fixed P, per call for a runtime P).  Other runtime P divide by
-// Markstein's correction when FAST (the bf16 kernels: 8 divisions per
-// vector, and the same CTAs per SM), by the IEEE division otherwise (in the
-// fp32 kernels the correction's registers would cost one CTA per SM).
+// a fixed P, per call for a runtime P).  Other P divide by Markstein's
+// correction: always for a compile-time P (divisor and reciprocal are
+// constants), and for a runtime P when FAST (the bf16 kernels: 8 divisions
+// per vector); the fp32 kernels for a runtime P take the IEEE division (in
+// the bounded kernels the correction's registers cost one CTA per SM).
 // BF16_OUT: the mean is only stored as bf16, so a quotient with the same
 // bf16 rounding serves (div_small_bf16).
 template <int PT, bool FAST = false, bool BF16_OUT = false>
@@ -233,7 +271,12 @@ __device__ __forceinline__ float mean_of(float sum, int np) {
   if constexpr (PT > 0 && (PT & (PT - 1)) == 0) {
     return __fmul_rn(sum, 1.0f / float(PT));
   } else if constexpr (PT > 0) {
-    return __fdiv_rn(sum, float(PT));
+    constexpr float d = float(PT), r = 1.0f / float(PT);  // r = RN(1/d), folded at compile time
+    if constexpr (BF16_OUT) {
+      return div_small_bf16(sum, d, r);
+    } else {
+      return div_small(sum, d, r);
+    }
   } else {
     const float d = float(np), r = __frcp_rn(d);
     if constexpr (FAST && BF16_OUT) {

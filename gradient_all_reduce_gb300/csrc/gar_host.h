@@ -26,6 +26,7 @@ struct ar_comm_s {
   int kernel_mode;      // 0 = default (k_reduce), 1 = k_reduce, 2 = bulk-copy k_reduce_tma
   bool pdl;             // programmatic dependent launch between consecutive kernels
   bool copy_tma;        // all-gather / broadcast on the bulk-store k_copy_tma (GAR_COPY=tma)
+  uint64_t small_bytes; // a flat all-reduce below this many bytes per replica: one vector per thread
 };
 
 namespace gar_host {
@@ -189,6 +190,7 @@ inline bool choose_tma(const ar_comm_s* c, int P, bool sgd, size_t es) {
 
 template <class Cap>
 void init_table(SegTable<Cap>& t, int np, int ndst, int stride, int dst_off, bool mean) {
+  t.unroll = 0;
   t.stages = 0;
   t.stage_bytes = 0;
   t.status = nullptr;
@@ -250,20 +252,40 @@ inline uint32_t vec_flag(void* const* ptrs, int n, float* const* extra = nullptr
 
 inline ar_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? AR_OK : AR_ERR_CUDA; }
 
+// A debug build (GAR_DEBUG=1) hands every kernel the comm's status word,
+// where its index checks report; a release build passes the table as is.
+template <class Cap, class F>
+inline cudaError_t with_status(const ar_comm_s* c, const SegTable<Cap>& t, F&& launch) {
+#if GAR_DEBUG
+  if (t.status == nullptr) {
+    SegTable<Cap> d = t;
+    d.status = c->d_status;
+    return launch(d);
+  }
+#else
+  (void)c;
+#endif
+  return launch(t);
+}
+
 template <class Cap>
 inline ar_status_t run_reduce(const ar_comm_s* c, ar_dtype_t dt, bool sgd, const SegTable<Cap>& t,
                               cudaStream_t st) {
   if (t.ntiles == 0) return AR_OK;
   const gar::LaunchCtx ctx{c->device, c->num_sms, st, t.stages > 0, c->pdl};
-  return from_cuda(dt == AR_F32 ? gar::launch_reduce_f32<Cap>(ctx, sgd, t)
-                                : gar::launch_reduce_bf16<Cap>(ctx, sgd, t));
+  return from_cuda(with_status(c, t, [&](const SegTable<Cap>& x) {
+    return dt == AR_F32 ? gar::launch_reduce_f32<Cap>(ctx, sgd, x)
+                        : gar::launch_reduce_bf16<Cap>(ctx, sgd, x);
+  }));
 }
 
 template <class Cap>
 inline ar_status_t run_copy(const ar_comm_s* c, const SegTable<Cap>& t, cudaStream_t st) {
   if (t.ntiles == 0) return AR_OK;
   const gar::LaunchCtx ctx{c->device, c->num_sms, st, c->copy_tma, c->pdl};
-  return from_cuda(gar::launch_copy<Cap>(ctx, t));
+  return from_cuda(with_status(c, t, [&](const SegTable<Cap>& x) {
+    return gar::launch_copy<Cap>(ctx, x);
+  }));
 }
 
 // Common checks of a collective call: live comm, dtype, pointer arrays.

@@ -23,28 +23,29 @@
 
 namespace gar {
 
-// The kernel specialisation that serves P ranks: P itself for 2, 4 and 8;
-// otherwise a bounded kernel sized for at most 4, 8, 12 or 16 ranks
-// (PT = -4, -8, -12, 0) with P read at run time.  Host (tile sizes) and
-// launch agree on it.
+// The kernel specialisation that serves P ranks: P itself for 1 .. 8 (a
+// compile-time rank count: registers for exactly P ranks, and a Mean over a
+// P that is not a power of two divides by a compile-time constant);
+// otherwise a bounded kernel sized for at most 12 or 16 ranks (PT = -12, 0)
+// with P read at run time.  Host (tile sizes) and launch agree on it.
+//
+// Up to 8 ranks used to share three compile-time kernels (2, 4, 8) and two
+// bounded ones (at most 4 and 8 ranks), whose registers were sized for
+// their largest P: the last no_sync micro-batch at P = 5 took 149 registers
+// in the 8-rank kernel, 17 % of the SM's warps active and 79 % of DRAM
+// throughput on GB300.
 __host__ __device__ constexpr int rank_class(int P) {
-  return (P == 2 || P == 4 || P == 8) ? P
-                                      : (P <= 4 ? -4 : (P <= 8 ? -8 : (P <= 12 ? -12 : 0)));
+  return P <= 8 ? P : (P <= 12 ? -12 : 0);
 }
 
 // Vectors per thread per tile: enough 16-byte loads in flight per thread
-// (P * U * 16 bytes) to cover HBM latency, bounded by registers.  The
-// bounded kernels (a runtime P) take half the unroll of their maximum: they
-// hold registers for ranks they may not use, and a Mean over P that is not
-// a power of two divides, so more CTAs per SM hide more of that arithmetic.
-// Measured on GB300 at 128 MiB per replica, back to back, of the copy
-// peak: the 4-rank kernel at P = 3 with U = 4 / 3 / 2 (126 / 80 / 64
-// registers for bf16): bf16 Mean 0.91 / 0.99 / 1.01, fp32 1.00 / 1.01 /
-// 1.01; the 8-rank kernel at P = 5, 6, 7 with U = 2 / 1: bf16 Mean 0.94 /
-// 0.96, 0.99 / 1.00, 1.01 / 1.02 (fp32 up by 0.00-0.01).
+// (P * U * 16 bytes) to cover HBM latency, bounded by registers: 4 for up
+// to 4 ranks, 2 for up to 8, 1 for the bounded kernels, which hold
+// registers for ranks they may not use (at 12 ranks, U = 1 took 80
+// registers and 3 CTAs per SM against 101 and 2 with U = 2: 0.91 -> 1.03
+// of the copy peak on GB300 at 128 MiB per replica).
 __host__ __device__ constexpr int unroll_for(int PT) {
-  return PT == -4 ? 2 : PT == -8 ? 1 : PT < 0 ? unroll_for(-PT)
-         : (PT == 0 ? 1 : (PT <= 4 ? 4 : (PT <= 8 ? 2 : 1)));
+  return PT <= 0 ? 1 : (PT <= 4 ? 4 : 2);
 }
 // With the fused SGD step each vector also carries its fp32 master weights
 // and momentum (2 x E floats), all loaded up front: 2 vectors per thread for
@@ -52,7 +53,7 @@ __host__ __device__ constexpr int unroll_for(int PT) {
 // of the copy peak back to back against 0.978 with 1), 1 beyond, where 2
 // would take one CTA per SM (168 registers at 12 ranks).
 __host__ __device__ constexpr int unroll_for_sgd(int PT) {
-  return (PT == 0 || PT < -8) ? 1 : 2;  // 2 for up to 8 ranks, exact or bounded
+  return PT <= 0 ? 1 : 2;  // 2 for up to 8 ranks, 1 for the bounded kernels
 }
 // Copy vectors per thread: 2 measured best on GB300 (broadcast, P = 8, 64 MiB
 // to 1 GiB per replica: 0.978-0.995 of the copy peak against 0.964-0.991 with
@@ -83,6 +84,7 @@ struct SegTable {
   float lr, mu;               // SGD hyper-parameters
   float scale;                // accumulation: factor on each micro-batch gradient
   int first;                  // accumulation: 1 = overwrite the accumulators
+  int unroll;                 // k_reduce: 0 = the kernel's own unroll, 1 = one vector per thread
   int stages;                 // bulk-copy kernel: shared-memory stages
   uint32_t stage_bytes;       // bulk-copy kernel: bytes per stage
   uint32_t* status;           // the comm's device status word (bounded waits)
@@ -109,6 +111,28 @@ __device__ __forceinline__ uint32_t seg_of(const SegTable<Cap>& a, uint32_t tile
   return lo;
 }
 
+// Debug-build checks of a tile's segment (see GAR_CHECK): s is a segment of
+// the launch whose tile range holds `tile`, its pointers lie inside the
+// table, and its tile count is exactly what its element count needs at
+// `per_tile` elements (or bytes) per tile -- the host and the kernel agree
+// on the tile size.
+template <class Cap>
+__device__ __forceinline__ void check_segment(const SegTable<Cap>& a, uint32_t s, uint32_t tile,
+                                              uint64_t per_tile) {
+#if GAR_DEBUG
+  const bool ok = s < a.nseg && s < uint32_t(Cap::kSeg) && a.tile0[s] <= tile &&
+                  tile < a.tile0[s + 1] && (uint64_t(s) + 1) * a.stride <= uint64_t(Cap::kPtr) &&
+                  a.tile0[s + 1] - a.tile0[s] == (a.numel[s] + per_tile - 1) / per_tile;
+  if (!ok && a.status != nullptr) atomicOr(a.status, kStatusBounds);
+  if (!ok) asm volatile("exit;");
+#else
+  (void)a;
+  (void)s;
+  (void)tile;
+  (void)per_tile;
+#endif
+}
+
 // --------------------------------------------------------------- reduce
 
 // SGD on one vector's E elements, w and v already loaded (E / 4 float4
@@ -128,10 +152,12 @@ __device__ __forceinline__ void sgd_vec(const float (&g)[D::kElems], float4 (&w4
   }
 }
 
-template <class D, int PT, bool SGD, class Cap>
+// UO > 0 overrides the unroll (the host's tile size follows the table's
+// `unroll`, which selects the kernel).
+template <class D, int PT, bool SGD, class Cap, int UO = 0>
 __global__ void __launch_bounds__(kThreads)
     k_reduce(const __grid_constant__ SegTable<Cap> a) {
-  constexpr int U = SGD ? unroll_for_sgd(PT) : unroll_for(PT);
+  constexpr int U = UO > 0 ? UO : (SGD ? unroll_for_sgd(PT) : unroll_for(PT));
   constexpr int E = D::kElems;
   constexpr int MAXP = Ranks<PT>::kMax;
   constexpr int WV = SGD ? E / 4 : 1;  // float4 groups of w (and of v) per vector
@@ -143,6 +169,8 @@ __global__ void __launch_bounds__(kThreads)
   uint32_t s = 0;
   for (uint32_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
     s = seg_of(a, tile, s);
+    check_segment(a, s, tile, kTileVec * E);
+    GAR_CHECK(np <= a.stride && a.dst_off + a.ndst <= a.stride, a.status);
     const uint64_t n = a.numel[s];
     void* const* seg = a.ptr + uint64_t(s) * a.stride;
     void* const* dst = seg + a.dst_off;
@@ -150,6 +178,7 @@ __global__ void __launch_bounds__(kThreads)
     const bool do_store = !SGD || a.write_back;
     float* w = SGD ? a.master[s] : nullptr;
     float* v = SGD ? a.mom[s] : nullptr;
+    GAR_CHECK(!SGD || (w != nullptr && v != nullptr), a.status);
 
     if (a.flags[s] & kSegVec) {
       const uint64_t nvec = n / E;
@@ -162,6 +191,7 @@ __global__ void __launch_bounds__(kThreads)
       for (int u = 0; u < U; ++u) {
         const uint64_t vi = v0 + uint64_t(u) * kThreads;
         if (vi < nvec) {
+          GAR_CHECK((vi + 1) * E <= n, a.status);
 #pragma unroll
           for (int r = 0; r < MAXP; ++r)
             if (Ranks<PT>::has(r, np))
@@ -218,6 +248,7 @@ __global__ void __launch_bounds__(kThreads)
       if (lt + 1 == a.tile0[s + 1] - a.tile0[s]) {
         const uint64_t i = nvec * E + threadIdx.x;
         if (i < n) {
+          GAR_CHECK(i - nvec * E < uint64_t(E), a.status);
           float g = reduce_scalar<D, PT>(seg, i, np, mean);
           if constexpr (SGD) {
             sgd_step(g, a.lr, a.mu, w[i], v[i]);
@@ -233,6 +264,7 @@ __global__ void __launch_bounds__(kThreads)
       for (uint64_t k = threadIdx.x; k < kTileVec * E; k += kThreads) {
         const uint64_t i = e0 + k;
         if (i >= n) break;
+        GAR_CHECK(i < n, a.status);
         float g = reduce_scalar<D, PT>(seg, i, np, mean);
         if constexpr (SGD) {
           sgd_step(g, a.lr, a.mu, w[i], v[i]);
@@ -293,12 +325,14 @@ __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTa
   if (a.ndst == 0) {  // small copies: one tile to every destination per CTA
     for (uint32_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
       const uint32_t s = seg_of(a, tile, 0);
+      check_segment(a, s, tile, kTileVec * 16);
       const uint64_t nbytes = a.numel[s];
       void* const* seg = a.ptr + uint64_t(s) * a.stride;
       const void* src = seg[0];
       void* const* dst = seg + a.dst_off;
       const uint64_t lt = tile - a.tile0[s];
       const int nd = int(a.flags[s] >> 8);
+      GAR_CHECK(a.dst_off + nd <= a.stride && nbytes % 2 == 0, a.status);
       if (a.flags[s] & kSegVec) {
         const uint64_t nvec = nbytes / 16;
         const uint64_t v0 = lt * kTileVec + threadIdx.x;
@@ -306,6 +340,7 @@ __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTa
 #pragma unroll
         for (int u = 0; u < kCopyUnroll; ++u) {
           const uint64_t vi = v0 + uint64_t(u) * kThreads;
+          GAR_CHECK(vi >= nvec || (vi + 1) * 16 <= nbytes, a.status);
           if (vi < nvec) x[u] = ld_stream(static_cast<const uint4*>(src) + vi);
         }
 #pragma unroll
@@ -317,6 +352,7 @@ __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTa
         if (lt + 1 == a.tile0[s + 1] - a.tile0[s]) {
           const uint64_t h = (nvec * 16) / 2 + threadIdx.x;  // 2-byte units of the tail
           if (h < nbytes / 2) {
+            GAR_CHECK(2 * h + 2 <= nbytes, a.status);
             const uint16_t x1 = static_cast<const uint16_t*>(src)[h];
             for (int d = 0; d < nd; ++d) static_cast<uint16_t*>(dst[d])[h] = x1;
           }
@@ -326,6 +362,7 @@ __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTa
         for (uint64_t k = threadIdx.x; k < kTileVec * 8; k += kThreads) {
           const uint64_t h = h0 + k;
           if (h >= nbytes / 2) break;
+          GAR_CHECK(2 * h + 2 <= nbytes, a.status);
           const uint16_t x1 = static_cast<const uint16_t*>(src)[h];
           for (int d = 0; d < nd; ++d) static_cast<uint16_t*>(dst[d])[h] = x1;
         }
@@ -345,8 +382,10 @@ __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTa
     const uint64_t tile = uint64_t(win) * kCopyWindow + b % kCopyWindow;
     if (tile >= a.ntiles) continue;
     const uint32_t s = seg_of(a, uint32_t(tile), 0);
+    check_segment(a, s, uint32_t(tile), kTileVec * 16);
     const uint32_t nd = a.flags[s] >> 8;
     if (d >= nd) continue;
+    GAR_CHECK(a.dst_off + int(d) < a.stride, a.status);
     const uint64_t nbytes = a.numel[s];
     void* const* seg = a.ptr + uint64_t(s) * a.stride;
     const void* src = seg[0];
@@ -359,6 +398,7 @@ __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTa
 #pragma unroll
       for (int u = 0; u < kCopyUnroll; ++u) {
         const uint64_t vi = v0 + uint64_t(u) * kThreads;
+        GAR_CHECK(vi >= nvec || (vi + 1) * 16 <= nbytes, a.status);
         if (vi < nvec) x[u] = ld_keep(static_cast<const uint4*>(src) + vi, keep);
       }
 #pragma unroll
@@ -380,6 +420,7 @@ __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTa
       }
       if (lt + 1 == a.tile0[s + 1] - a.tile0[s]) {
         const uint64_t h = (nvec * 16) / 2 + threadIdx.x;  // 2-byte units of the tail
+        GAR_CHECK(h >= nbytes / 2 || 2 * h + 2 <= nbytes, a.status);
         if (h < nbytes / 2) static_cast<uint16_t*>(out)[h] = static_cast<const uint16_t*>(src)[h];
       }
     } else {
@@ -387,6 +428,7 @@ __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTa
       for (uint64_t k = threadIdx.x; k < kTileVec * 8; k += kThreads) {
         const uint64_t h = h0 + k;
         if (h >= nbytes / 2) break;
+        GAR_CHECK(2 * h + 2 <= nbytes, a.status);
         static_cast<uint16_t*>(out)[h] = static_cast<const uint16_t*>(src)[h];
       }
     }
@@ -425,6 +467,8 @@ __global__ void __launch_bounds__(kThreads) k_accumulate(const __grid_constant__
   uint32_t s = 0;
   for (uint32_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
     s = seg_of(a, tile, s);
+    check_segment(a, s, tile, kTileQuads * 4);
+    GAR_CHECK(a.stride >= 2, a.status);
     const uint64_t n = a.numel[s];
     const void* g = a.ptr[uint64_t(s) * a.stride];
     float* acc = static_cast<float*>(a.ptr[uint64_t(s) * a.stride + 1]);
@@ -438,6 +482,7 @@ __global__ void __launch_bounds__(kThreads) k_accumulate(const __grid_constant__
       for (int j = 0; j < J; ++j) {
         const uint64_t qi = q0 + uint64_t(j) * kThreads;
         if (qi < nq) {
+          GAR_CHECK(4 * qi + 4 <= n, a.status);
           x[j] = D::ld_quad(g, qi);
           a4[j] = FIRST ? make_float4(0.f, 0.f, 0.f, 0.f) : ld_f4(acc + 4 * qi);
         }
@@ -467,6 +512,7 @@ __global__ void __launch_bounds__(kThreads) k_accumulate(const __grid_constant__
       if (lt + 1 == a.tile0[s + 1] - a.tile0[s]) {
         const uint64_t i = nq * 4 + threadIdx.x;
         if (i < n) {
+          GAR_CHECK(i - nq * 4 < 4, a.status);
           const float sv = __fmul_rn(a.scale, D::load1(g, i));
           acc[i] = FIRST ? sv : __fadd_rn(acc[i], sv);
         }
@@ -476,6 +522,7 @@ __global__ void __launch_bounds__(kThreads) k_accumulate(const __grid_constant__
       for (uint64_t k = threadIdx.x; k < kTileQuads * 4; k += kThreads) {
         const uint64_t i = e0 + k;
         if (i >= n) break;
+        GAR_CHECK(i < n, a.status);
         const float sv = __fmul_rn(a.scale, D::load1(g, i));
         acc[i] = FIRST ? sv : __fadd_rn(acc[i], sv);
       }
@@ -597,17 +644,21 @@ __global__ void __launch_bounds__(kThreads)
   uint32_t s = 0;
   for (uint32_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
     s = seg_of(a, tile, s);
+    check_segment(a, s, tile, uint64_t(kThreads) * E);
+    GAR_CHECK(2 * np <= a.stride, a.status);
     const uint64_t n = a.numel[s];
     void* const* seg = a.ptr + uint64_t(s) * a.stride;
     const uint64_t lt = tile - a.tile0[s];
     const bool do_store = !SGD || a.write_back;
     float* w = SGD ? a.master[s] : nullptr;
     float* v = SGD ? a.mom[s] : nullptr;
+    GAR_CHECK(!SGD || (w != nullptr && v != nullptr), a.status);
     if (a.flags[s] & kSegVec) {
       const uint64_t nvec = n / E;
 #pragma unroll
       for (int turn = 0; turn < kThreads / T; ++turn) {
         const uint64_t vi = lt * kThreads + uint64_t(turn) * T + threadIdx.x;
+        GAR_CHECK(vi >= nvec || (vi + 1) * E <= n, a.status);
         if (vi < nvec)
           reduce_accumulated_vec<D, PT, SGD>(seg, np, vi, w, v, a.scale, a.lr, a.mu, mean, first,
                                              do_store);
@@ -615,6 +666,7 @@ __global__ void __launch_bounds__(kThreads)
       if (lt + 1 == a.tile0[s + 1] - a.tile0[s]) {
         const uint64_t i = nvec * E + threadIdx.x;
         if (i < n) {
+          GAR_CHECK(i - nvec * E < uint64_t(E), a.status);
           float g = 0.f;
           for (int r = 0; r < MAXP; ++r)
             if (Ranks<PT>::has(r, np)) {
@@ -634,6 +686,7 @@ __global__ void __launch_bounds__(kThreads)
       for (uint64_t k = threadIdx.x; k < uint64_t(kThreads) * E; k += T) {
         const uint64_t i = e0 + k;
         if (i >= n) break;
+        GAR_CHECK(i < n, a.status);
         float g = 0.f;
         for (int r = 0; r < MAXP; ++r)
           if (Ranks<PT>::has(r, np)) {

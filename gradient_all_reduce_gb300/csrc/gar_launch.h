@@ -2,6 +2,8 @@
 // kernel translation units (gar_reduce_*.cu, gar_copy.cu).
 #pragma once
 
+#include <type_traits>
+
 #include <cuda_runtime.h>
 
 #include "gar_tma.cuh"
@@ -45,12 +47,34 @@ inline int tma_stages(int P, bool sgd, int elem_bytes) {
   return s > uint32_t(kTmaMaxStages) ? kTmaMaxStages : int(s);
 }
 
-// Launch k_reduce on the table for fp32 or bf16 replicas, choosing the
-// specialisation for P (2, 4, 8, else the generic runtime-P kernel).
+// Launch k_reduce on the table for fp32 or bf16 replicas, without or with
+// the fused SGD step, choosing the specialisation for P (rank_class).  A
+// flat all-reduce's one-segment table (CapTiny) never carries the SGD step.
 template <class Cap>
-cudaError_t launch_reduce_f32(const LaunchCtx& ctx, bool sgd, const SegTable<Cap>& tab);
+cudaError_t launch_reduce_plain_f32(const LaunchCtx& ctx, const SegTable<Cap>& tab);
 template <class Cap>
-cudaError_t launch_reduce_bf16(const LaunchCtx& ctx, bool sgd, const SegTable<Cap>& tab);
+cudaError_t launch_reduce_plain_bf16(const LaunchCtx& ctx, const SegTable<Cap>& tab);
+template <class Cap>
+cudaError_t launch_reduce_sgd_f32(const LaunchCtx& ctx, const SegTable<Cap>& tab);
+template <class Cap>
+cudaError_t launch_reduce_sgd_bf16(const LaunchCtx& ctx, const SegTable<Cap>& tab);
+
+template <class Cap>
+inline cudaError_t launch_reduce_f32(const LaunchCtx& ctx, bool sgd, const SegTable<Cap>& tab) {
+  if constexpr (std::is_same<Cap, CapTiny>::value) {
+    return sgd ? cudaErrorNotSupported : launch_reduce_plain_f32(ctx, tab);
+  } else {
+    return sgd ? launch_reduce_sgd_f32(ctx, tab) : launch_reduce_plain_f32(ctx, tab);
+  }
+}
+template <class Cap>
+inline cudaError_t launch_reduce_bf16(const LaunchCtx& ctx, bool sgd, const SegTable<Cap>& tab) {
+  if constexpr (std::is_same<Cap, CapTiny>::value) {
+    return sgd ? cudaErrorNotSupported : launch_reduce_plain_bf16(ctx, tab);
+  } else {
+    return sgd ? launch_reduce_sgd_bf16(ctx, tab) : launch_reduce_plain_bf16(ctx, tab);
+  }
+}
 
 // The accumulation kernels (DDP's no_sync) for fp32 or bf16 gradients.
 template <class Cap>
@@ -75,6 +99,8 @@ struct SyncBnArgs {
   double eps;
   uint64_t channels;
   int np;
+  uint32_t lanes;                 // channels per warp (set by the launch)
+  uint32_t* status;               // the comm's status word (debug-build checks)
 };
 cudaError_t launch_syncbn_stats(const LaunchCtx& ctx, const SyncBnArgs& args);
 
@@ -82,11 +108,13 @@ cudaError_t launch_syncbn_stats(const LaunchCtx& ctx, const SyncBnArgs& args);
 cudaError_t launch_wait_selftest(cudaStream_t stream, uint32_t* status, uint64_t limit_ns);
 
 // Tile size in elements of k_reduce (or k_reduce_tma when tma is set) for
-// P ranks, the given element size, and with or without the SGD step.
-inline uint64_t reduce_tile(int P, int elem_bytes, bool tma = false, bool sgd = false) {
+// P ranks, the given element size, with or without the SGD step, and the
+// table's unroll (0 = the kernel's own).
+inline uint64_t reduce_tile(int P, int elem_bytes, bool tma = false, bool sgd = false,
+                            int unroll = 0) {
   if (tma) return tma_tile_elems(16 / elem_bytes);
   const int PT = rank_class(P);
-  const int U = sgd ? unroll_for_sgd(PT) : unroll_for(PT);
+  const int U = unroll > 0 ? unroll : (sgd ? unroll_for_sgd(PT) : unroll_for(PT));
   return uint64_t(U) * kThreads * (16 / elem_bytes);
 }
 
@@ -110,8 +138,10 @@ inline unsigned grid_for(uint32_t ntiles, int max_ctas) {
   return (ntiles + per_cta - 1) / per_cta;
 }
 
-// Resident CTAs per SM for a kernel (cached per function); smem is the
-// dynamic shared memory per CTA, which is also raised to that size once.
-int resident_ctas(const void* func, int threads = kThreads, size_t smem = 0);
+// Resident CTAs per SM of a kernel on the current device (cached per device,
+// function, block size and shared memory) into *per_sm; smem is the dynamic
+// shared memory per CTA, which the function's attribute is raised to on
+// every call.  Returns the CUDA error of either step.
+cudaError_t resident_ctas(const void* func, int threads, size_t smem, int* per_sm);
 
 }  // namespace gar

@@ -1,6 +1,5 @@
-// k_reduce instantiations for bf16 replicas.
-#define launch_reduce_dtype launch_reduce_bf16
-#define launch_reduce_acc_dtype launch_reduce_acc_bf16
-#define launch_accumulate_dtype launch_accumulate_bf16
+// k_reduce instantiations (no SGD step) for bf16 replicas.
+#define GAR_LAUNCH launch_reduce_plain_bf16
 #define GAR_DTYPE BF16
+#define GAR_PART 0
 #include "gar_reduce.inc"

@@ -1,6 +1,5 @@
-// k_reduce instantiations for fp32 replicas.
-#define launch_reduce_dtype launch_reduce_f32
-#define launch_reduce_acc_dtype launch_reduce_acc_f32
-#define launch_accumulate_dtype launch_accumulate_f32
+// k_reduce instantiations (no SGD step) for fp32 replicas.
+#define GAR_LAUNCH launch_reduce_plain_f32
 #define GAR_DTYPE F32
+#define GAR_PART 0
 #include "gar_reduce.inc"

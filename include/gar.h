@@ -64,7 +64,8 @@ typedef enum {
     AR_ERR_UNSUPPORTED = 2, /* no sm_103a device, or a feature not built */
     AR_ERR_CUDA = 3,        /* a CUDA runtime call or a kernel launch failed */
     AR_ERR_TIMEOUT = 4,     /* a device-side bounded wait gave up */
-    AR_ERR_STATE = 5        /* a comm used after ar_destroy, or not from ar_init */
+    AR_ERR_STATE = 5,       /* a comm used after ar_destroy, or not from ar_init */
+    AR_ERR_DEVICE_CHECK = 6 /* a debug build's device-side index check failed */
 } ar_status_t;
 
 /* ReduceOperation.  AR_OP_DEFAULT selects the comm's default_op. */
@@ -361,9 +362,12 @@ ar_status_t ar_reducer_launches(ar_reducer_t reducer, uint64_t *launches);
 ar_status_t ar_reducer_destroy(ar_reducer_t reducer);
 
 /*
- * Sticky device-side status of a comm: AR_ERR_TIMEOUT once a kernel's
- * bounded wait has given up, AR_ERR_CUDA for a sticky CUDA error on the
- * device, else AR_OK.  Synchronises the device (it reads the status word).
+ * Sticky device-side status of a comm: AR_ERR_DEVICE_CHECK once a kernel of
+ * a debug build (compiled with GAR_DEBUG=1) found an index outside the
+ * buffers its launch describes (the access is skipped, nothing traps);
+ * AR_ERR_TIMEOUT once a kernel's bounded wait has given up; AR_ERR_CUDA for
+ * a sticky CUDA error on the device; else AR_OK.  Synchronises the device
+ * (it reads the status word).
  */
 ar_status_t ar_get_async_error(ar_comm_t comm);
 
@@ -395,15 +399,16 @@ ar_status_t ar_selftest_wait_timeout(ar_comm_t comm, unsigned timeout_ms, ar_str
  * It always runs the bulk-copy pipelined kernel.  The caller passes inputs
  * and outputs; the kernel's scratch -- one 4-byte status word set when a
  * bounded wait gives up -- lives in a static 256-byte device array that
- * every GPU loading the library holds until the process exits.  A call
- * needing more scratch than that is refused with AR_ERR_INVALID_ARG.  The
- * call allocates no memory: no cudaMalloc, cudaFree or allocating library
- * routine.
+ * every GPU loading the library holds until the process exits.  Every call
+ * needs that one word whatever its arguments (a compile-time check keeps
+ * it inside the array), so no call can ask for more scratch than the
+ * array holds.  The call allocates no memory: no cudaMalloc, cudaFree or
+ * allocating library routine.
  *
- * The first call on a device sets that device up (checks it is sm_103 and
- * looks up the array's device address); make that first call before any
- * stream capture.  Every call clears the status word on `stream` before its
- * launch.  All calls on a device share the one array, so calls whose work
+ * The first call on a device sets that device up (checks it is sm_103);
+ * make that first call before any stream capture.  Every call looks up the
+ * array's device address in the current context (a lookup, no
+ * allocation) and clears the status word on `stream` before its launch.  All calls on a device share the one array, so calls whose work
  * overlaps on the GPU (different streams, no ordering between them) race on
  * it; calls on one stream are ordered and do not.  The status word has no
  * comm to be read through: a wait that gave up (after 2 s) leaves the
