@@ -484,10 +484,11 @@ class E2EStep:
 def time_e2e(args, device, stream):
     """The ViT step end to end from pinned host buffers (E2EStep), and the
     same transfers without the kernels (the host link's bound), measured
-    alike: after 3 warm-up steps, three regions of K steps each, every region
+    alike: after 3 warm-up steps, seven regions of K steps each, every region
     under one event pair with the same fill (``start``) and drain
     (``finish``), interleaved so that both meet the same traffic on the
-    shared host; each figure is the median region."""
+    shared host; each figure is the median region (one region in three met
+    another job's traffic on the host link in some runs)."""
     import torch
     import gradient_all_reduce_gb300 as gar
     comm = gar.ar_init(P_VIT, device.index, gar.AR_MEAN)
@@ -516,12 +517,15 @@ def time_e2e(args, device, stream):
                 e2e.copies_only(stream)
             e2e.finish(stream)
             torch.cuda.synchronize(device)
-            for _ in range(3):
+            for _ in range(7):
                 full.append(region(e2e.step))
                 link.append(region(e2e.copies_only))
         el, ln = statistics.median(full), statistics.median(link)
         value = vs.step_bytes / el / 1e9
         bound = vs.step_bytes / ln / 1e9
+        # Other jobs' traffic on the shared host link only ever slows a
+        # region down: the fastest region of each kind is the least disturbed.
+        best, best_link = min(full), min(link)
         return {"value": value, "unit": "GB/s",
                 "h2d_bytes_per_step": 2 * vs.n * P_VIT, "d2h_bytes_per_step": 4 * vs.n,
                 "steps": steps, "ms_per_step": el * 1e3,
@@ -530,9 +534,11 @@ def time_e2e(args, device, stream):
                 "link_only_ms_per_step_regions": [round(x * 1e3, 3) for x in link],
                 "link_bound_GBps": bound,
                 "frac_of_link_bound": value / bound,
-                "statistic": ("median of three regions of `steps` steps for both the step and "
+                "best_ms_per_step": best * 1e3, "best_link_only_ms_per_step": best_link * 1e3,
+                "frac_of_link_bound_best": best_link / best,
+                "statistic": ("median of seven regions of `steps` steps for both the step and "
                               "the link-only transfers, each region with the same fill and drain, "
-                              "the two kinds interleaved"),
+                              "the two kinds interleaved; *_best: the fastest region of each kind"),
                 "path": ("ar_reducer_* with per-bucket H2D on 4 copy streams and per-bucket D2H "
                          "of the updated weights after ar_reducer_wait_bucket; consecutive steps "
                          "ordered per bucket, not per step")}

@@ -147,6 +147,11 @@ ar_status_t ar_init(ar_comm_t* comm, int nranks, int cuda_device, ar_op_t defaul
   c->small_bytes = kSmallAllReduceBytes;
   env = std::getenv("GAR_SMALL_ALL_REDUCE_BYTES");
   if (env != nullptr) c->small_bytes = std::strtoull(env, nullptr, 10);
+  // Destinations per windowed copy item (all-gather, broadcast): by default
+  // ceil(D / 4) for D destinations (copy_group).
+  c->copy_group = -1;
+  env = std::getenv("GAR_COPY_GROUP");
+  if (env != nullptr) c->copy_group = std::max(0, std::min(AR_MAX_RANKS, std::atoi(env)));
   if (cudaMalloc(&c->d_status, sizeof(uint32_t)) != cudaSuccess) {
     delete c;
     return AR_ERR_CUDA;
@@ -322,6 +327,9 @@ ar_status_t ar_all_gather(ar_comm_t comm, const void* const* send, void* const* 
   SegTable<CapSmall> t;
   init_table(t, 1, 0, P + 1, 1, false);
   t.status = comm->d_status;
+  t.unroll = copy_unroll(comm, bytes);
+  const uint64_t tile = copy_tile(comm, bytes);
+  int max_nd = 0;
   for (int q = 0; q < P; ++q) {
     void* ptrs[AR_MAX_RANKS + 1];
     int nd = 0;
@@ -332,8 +340,10 @@ ar_status_t ar_all_gather(ar_comm_t comm, const void* const* send, void* const* 
     }
     for (int k = 1 + nd; k < P + 1; ++k) ptrs[k] = ptrs[0];
     const uint32_t flags = vec_flag(ptrs, 1 + nd) | (uint32_t(nd) << 8);
-    if (!add_segment(t, ptrs, sbytes, copy_tile(comm), flags)) return AR_ERR_INVALID_ARG;
+    if (!add_segment(t, ptrs, sbytes, tile, flags)) return AR_ERR_INVALID_ARG;
+    max_nd = std::max(max_nd, nd);
   }
+  t.dgroup = copy_group(comm, max_nd);
   return run_copy(comm, t, static_cast<cudaStream_t>(stream));
 }
 
@@ -362,13 +372,15 @@ ar_status_t ar_broadcast(ar_comm_t comm, void* const* buf, size_t count, ar_dtyp
   SegTable<CapSmall> t;
   init_table(t, 1, 0, P, 1, false);
   t.status = comm->d_status;
+  t.dgroup = copy_group(comm, P - 1);
+  t.unroll = copy_unroll(comm, bytes);
   void* ptrs[AR_MAX_RANKS];
   int nd = 0;
   ptrs[0] = buf[root];
   for (int r = 0; r < P; ++r)
     if (r != root) ptrs[1 + nd++] = buf[r];
   const uint32_t flags = vec_flag(ptrs, P) | (uint32_t(nd) << 8);
-  if (!add_segment(t, ptrs, bytes, copy_tile(comm), flags)) return AR_ERR_INVALID_ARG;
+  if (!add_segment(t, ptrs, bytes, copy_tile(comm, bytes), flags)) return AR_ERR_INVALID_ARG;
   return run_copy(comm, t, static_cast<cudaStream_t>(stream));
 }
 

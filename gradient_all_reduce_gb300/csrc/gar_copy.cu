@@ -76,20 +76,33 @@ cudaError_t launch_copy(const LaunchCtx& ctx, const SegTable<Cap>& tab) {
     if (grid == 0) return cudaSuccess;
     return launch_ex(ctx, k, grid, 32, smem, tab);
   }
-  // A large copy from one source (a broadcast) runs destination by
-  // destination in windows: the destination count travels in ndst (the
-  // bulk-store kernel reads each segment's own count instead).  Everything
-  // else keeps ndst = 0: one CTA per tile, every destination.
+  // A copy of at least kCopyWindowBytes runs by destination groups in
+  // windows (a.dgroup destinations per item, see k_copy): the most
+  // destinations of any segment travels in ndst (the bulk-store kernel
+  // reads each segment's own count instead).  a.dgroup = 0 keeps ndst = 0:
+  // one CTA per tile, every destination.
+  // tab.unroll = 1 or 2: a copy below kCopyWindowBytes, cut into tiles of
+  // that many vectors per thread (copy_unroll_for) and always in the classic
+  // order.
+  if (tab.unroll == 1 || tab.unroll == 2) {
+    SegTable<Cap> t = tab;
+    t.ndst = 0;
+    const unsigned grid = grid_per_tile(t.ntiles);
+    if (grid == 0) return cudaSuccess;
+    return tab.unroll == 1 ? launch_ex(ctx, &k_copy<Cap, 1>, grid, kThreads, 0, t)
+                           : launch_ex(ctx, &k_copy<Cap, 2>, grid, kThreads, 0, t);
+  }
   SegTable<Cap> t = tab;
   t.ndst = 0;
   uint64_t items = t.ntiles;
-  if (t.nseg == 1 && t.ntiles >= kCopyWindowMin) {
+  if (t.dgroup > 0) {
     for (uint32_t s = 0; s < t.nseg; ++s) t.ndst = std::max(t.ndst, int(t.flags[s] >> 8));
-    items = (uint64_t(t.ntiles) + kCopyWindow - 1) / kCopyWindow * kCopyWindow * uint64_t(t.ndst);
+    const uint64_t groups = (uint64_t(t.ndst) + t.dgroup - 1) / uint64_t(t.dgroup);
+    items = (uint64_t(t.ntiles) + kCopyWindow - 1) / kCopyWindow * kCopyWindow * groups;
   }
   const unsigned grid = items < 0x7FFFFFFFull ? unsigned(items) : 0x7FFFFFFFu;
   if (grid == 0) return cudaSuccess;
-  return launch_ex(ctx, &k_copy<Cap>, grid, kThreads, 0, t);
+  return launch_ex(ctx, &k_copy<Cap, kCopyUnroll>, grid, kThreads, 0, t);
 }
 
 __global__ void k_wait_selftest(uint32_t* status, uint64_t limit_ns) {
@@ -110,53 +123,62 @@ cudaError_t launch_wait_selftest(cudaStream_t stream, uint32_t* status, uint64_t
   return cudaGetLastError();
 }
 
-// Synchronized batch-norm statistics: one thread per channel pools the
-// ranks' per-channel sums in fp64 (rank order), forms mean, biased
-// variance and invstd with IEEE-rounded fp64 operations, and writes both,
-// rounded to fp32, for every rank.
+// Synchronized batch-norm statistics: for each channel, the ranks' fp32
+// sums and sums of squares pooled in fp64 in rank order, then mean, biased
+// variance and invstd = 1 / sqrt(var + eps) with IEEE-rounded fp64
+// operations, written rounded to fp32 to every rank.
 //
 // The call is latency-bound: a few KB of inputs, and per channel a chain of
-// about 70 fp64 instructions (conversions, adds, three divisions, a square
-// root) on GB300's narrow fp64 pipe.  So the kernel is specialised on the
-// rank count NP: a thread issues the loads of all 2 NP inputs before the
-// first add, and executes exactly NP - 1 adds per sum (a loop to the
-// largest rank count under a guard issued the guarded-off fp64
-// instructions too).  The channels are spread over every SM sub-partition:
-// each warp takes `lanes` channels (lane < lanes), so that up to
-// 4 x SMs warps share the fp64 work, four to a CTA.
+// fp64 conversions, adds, three divisions and a square root on GB300's
+// narrow fp64 pipe, with one warp per scheduler and nothing to hide it.  A
+// warp's time is its instruction count times the chain's latency, so the
+// work of one channel is spread over a group of L lanes (L = P rounded up to
+// a power of two): lane k of the group loads, and at the end stores, rank
+// k's values, and every lane of the group receives all ranks' values by
+// shuffles and runs the same rank-ordered adds and the same division chain
+// (identical bits in every lane).  With one thread per channel doing all
+// of it, a warp at P = 8 executed 484 instructions at 14 cycles each.
+// The kernel is specialised on the rank count NP: exactly NP - 1 adds per
+// sum.  Warps take 32 / L channels each, four warps to a CTA.
 constexpr int kSyncBnThreads = 128;
+
+__host__ __device__ constexpr int syncbn_group(int np) {
+  return np <= 1 ? 1 : np <= 2 ? 2 : np <= 4 ? 4 : np <= 8 ? 8 : 16;
+}
 
 template <int NP>
 __global__ void __launch_bounds__(kSyncBnThreads) k_syncbn_stats(const __grid_constant__ SyncBnArgs a) {
+  constexpr int L = syncbn_group(NP);    // lanes per channel
+  constexpr int CPW = 32 / L;            // channels per warp
   griddep_launch_dependents();
   griddep_wait();
-  const uint32_t lane = threadIdx.x & 31u;
-  if (lane >= a.lanes) return;
+  GAR_CHECK(a.np == NP, a.status);
+  const int lane = int(threadIdx.x & 31u);
+  const int k = lane % L;                // the rank this lane loads and stores
+  const int g0 = lane - k;               // first lane of the group
   const uint64_t warp = (uint64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const uint64_t stride = (uint64_t(gridDim.x) * blockDim.x >> 5) * a.lanes;
-  GAR_CHECK(a.np == NP && a.lanes >= 1 && a.lanes <= 32, a.status);
-  for (uint64_t c = warp * a.lanes + lane; c < a.channels; c += stride) {
-    GAR_CHECK(c < a.channels, a.status);
-    float x1[NP], x2[NP];
-#pragma unroll
-    for (int r = 0; r < NP; ++r) {
-      x1[r] = __ldg(a.sum[r] + c);
-      x2[r] = __ldg(a.sqsum[r] + c);
+  const uint64_t nwarps = uint64_t(gridDim.x) * blockDim.x >> 5;
+  for (uint64_t base = warp * CPW; base < a.channels; base += nwarps * CPW) {
+    const uint64_t c = base + uint64_t(lane / L);
+    const bool mine = k < NP && c < a.channels;
+    GAR_CHECK(!mine || c < a.channels, a.status);
+    double x1 = 0.0, x2 = 0.0;
+    if (mine) {
+      x1 = double(__ldg(a.sum[k] + c));
+      x2 = double(__ldg(a.sqsum[k] + c));
     }
-    double s1 = double(x1[0]), s2 = double(x2[0]);
+    double s1 = __shfl_sync(0xFFFFFFFFu, x1, g0), s2 = __shfl_sync(0xFFFFFFFFu, x2, g0);
 #pragma unroll
     for (int r = 1; r < NP; ++r) {
-      s1 = __dadd_rn(s1, double(x1[r]));
-      s2 = __dadd_rn(s2, double(x2[r]));
+      s1 = __dadd_rn(s1, __shfl_sync(0xFFFFFFFFu, x1, g0 + r));
+      s2 = __dadd_rn(s2, __shfl_sync(0xFFFFFFFFu, x2, g0 + r));
     }
     const double m = __ddiv_rn(s1, a.n);
     const double var = __dsub_rn(__ddiv_rn(s2, a.n), __dmul_rn(m, m));
     const double is = __ddiv_rn(1.0, __dsqrt_rn(__dadd_rn(var, a.eps)));
-    const float mf = __double2float_rn(m), isf = __double2float_rn(is);
-#pragma unroll
-    for (int r = 0; r < NP; ++r) {
-      a.mean[r][c] = mf;
-      a.invstd[r][c] = isf;
+    if (mine) {
+      a.mean[k][c] = __double2float_rn(m);
+      a.invstd[k][c] = __double2float_rn(is);
     }
   }
 }
@@ -164,16 +186,13 @@ __global__ void __launch_bounds__(kSyncBnThreads) k_syncbn_stats(const __grid_co
 template <int NP>
 static cudaError_t launch_syncbn_np(const LaunchCtx& ctx, const SyncBnArgs& args) {
   if (args.np != NP) return launch_syncbn_np<NP - 1>(ctx, args);
-  SyncBnArgs a = args;
-  // Channels per warp: as few as spread the channels over 4 warps per SM.
-  const uint64_t warps_max = uint64_t(ctx.num_sms) * (kSyncBnThreads / 32);
-  const uint64_t lanes = (a.channels + warps_max - 1) / warps_max;
-  a.lanes = uint32_t(lanes < 1 ? 1 : (lanes > 32 ? 32 : lanes));
-  const uint64_t warps = (a.channels + a.lanes - 1) / a.lanes;
+  constexpr uint64_t kCpw = 32 / syncbn_group(NP);
+  const uint64_t warps = (args.channels + kCpw - 1) / kCpw;
   const uint64_t blocks = (warps + kSyncBnThreads / 32 - 1) / (kSyncBnThreads / 32);
-  const unsigned grid = unsigned(blocks < warps_max ? blocks : warps_max);
+  const uint64_t cap = uint64_t(ctx.num_sms) * 8;
+  const unsigned grid = unsigned(blocks < cap ? blocks : cap);
   if (grid == 0) return cudaSuccess;
-  return launch_ex(ctx, &k_syncbn_stats<NP>, grid, kSyncBnThreads, 0, a);
+  return launch_ex(ctx, &k_syncbn_stats<NP>, grid, kSyncBnThreads, 0, args);
 }
 template <>
 cudaError_t launch_syncbn_np<0>(const LaunchCtx&, const SyncBnArgs&) {

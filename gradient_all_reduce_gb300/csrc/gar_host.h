@@ -27,6 +27,7 @@ struct ar_comm_s {
   bool pdl;             // programmatic dependent launch between consecutive kernels
   bool copy_tma;        // all-gather / broadcast on the bulk-store k_copy_tma (GAR_COPY=tma)
   uint64_t small_bytes; // a flat all-reduce below this many bytes per replica: one vector per thread
+  int copy_group;       // destinations per windowed copy item (-1 = ceil(D / 4), 0 = classic order)
 };
 
 namespace gar_host {
@@ -191,6 +192,7 @@ inline bool choose_tma(const ar_comm_s* c, int P, bool sgd, size_t es) {
 template <class Cap>
 void init_table(SegTable<Cap>& t, int np, int ndst, int stride, int dst_off, bool mean) {
   t.unroll = 0;
+  t.dgroup = 0;
   t.stages = 0;
   t.stage_bytes = 0;
   t.status = nullptr;
@@ -237,9 +239,26 @@ void set_tma(SegTable<Cap>& t, const ar_comm_s* c, bool sgd, size_t es) {
   t.status = c->d_status;
 }
 
-// Tile (bytes) of the copy kernel a comm uses.
-inline uint64_t copy_tile(const ar_comm_s* c) {
-  return c->copy_tma ? uint64_t(gar::kCopyTmaTile) : gar::copy_tile_bytes();
+// Destinations per windowed item of a copy with at most D destinations per
+// segment: ceil(D / 4), about four groups per window (see k_copy), unless
+// the comm fixes it (GAR_COPY_GROUP; 0 selects the classic order).
+inline int copy_group(const ar_comm_s* c, int D) {
+  if (c->copy_group >= 0) return c->copy_group;
+  return D < 1 ? 1 : (D + 3) / 4;
+}
+
+// Tile (bytes) of the copy kernel a comm uses for a copy of `src_bytes` of
+// source, and the table's unroll that selects the register-staged kernel's
+// form: 1 or 2 vectors per thread below kCopyWindowBytes, 0 above (four
+// vectors, the windowed order).
+inline uint64_t copy_tile(const ar_comm_s* c, uint64_t src_bytes) {
+  if (c->copy_tma) return uint64_t(gar::kCopyTmaTile);
+  return gar::copy_tile_bytes(src_bytes);
+}
+inline int copy_unroll(const ar_comm_s* c, uint64_t src_bytes) {
+  if (c->copy_tma) return 0;
+  const int u = gar::copy_unroll_for(src_bytes);
+  return u == gar::kCopyUnroll ? 0 : u;
 }
 
 inline uint32_t vec_flag(void* const* ptrs, int n, float* const* extra = nullptr, int nextra = 0) {

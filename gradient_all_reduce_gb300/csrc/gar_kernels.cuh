@@ -55,10 +55,14 @@ __host__ __device__ constexpr int unroll_for(int PT) {
 __host__ __device__ constexpr int unroll_for_sgd(int PT) {
   return PT <= 0 ? 1 : 2;  // 2 for up to 8 ranks, 1 for the bounded kernels
 }
-// Copy vectors per thread: 2 measured best on GB300 (broadcast, P = 8, 64 MiB
-// to 1 GiB per replica: 0.978-0.995 of the copy peak against 0.964-0.991 with
-// 4 and 0.934-0.987 with 8).
-constexpr int kCopyUnroll = 2;
+// Copy vectors per thread: 4 (16 KB tiles) for large copies.  The windowed
+// copies below are bound by the work each CTA does per item, which a
+// larger tile spreads over twice the bytes: on GB300 at 256 MiB per
+// replica, broadcast P = 8 1.09 of the copy peak against 0.97 with 2
+// vectors (same items, one destination each), all-gather P = 4 1.05
+// against 0.93.  Smaller copies take fewer vectors per thread, so that a
+// few MB still spread over every SM (copy_unroll_for).
+constexpr int kCopyUnroll = 4;
 
 // Segment table capacities: a flat all-reduce (one segment) uses a 400-byte
 // parameter block, small launches (<= 16 segments) about 5 KB, large ones
@@ -85,6 +89,7 @@ struct SegTable {
   float scale;                // accumulation: factor on each micro-batch gradient
   int first;                  // accumulation: 1 = overwrite the accumulators
   int unroll;                 // k_reduce: 0 = the kernel's own unroll, 1 = one vector per thread
+  int dgroup;                 // k_copy: destinations per windowed item (0 = the classic order)
   int stages;                 // bulk-copy kernel: shared-memory stages
   uint32_t stage_bytes;       // bulk-copy kernel: bytes per stage
   uint32_t* status;           // the comm's device status word (bounded waits)
@@ -282,31 +287,35 @@ __global__ void __launch_bounds__(kThreads)
 // has flags[s] >> 8 destinations (an in-place all-gather skips the shard
 // that is already in place).
 //
-// Windowed copies (a.ndst = D > 0; the host picks them for a broadcast of
-// at least kCopyWindowMin tiles): one CTA copies one tile of a segment to
-// one destination, and the work items run destination by destination within
-// windows of kCopyWindow tiles -- item b is tile (b / (W D)) W + b % W for
-// destination (b / W) % D.  The CTAs in flight then write one or two
-// destinations at a time, while the window's source tiles, read from HBM
-// for the first destination, are read again from L2: the source is loaded
+// Windowed copies (a.ndst = D > 0, the most destinations of any segment;
+// the host picks them for copies of at least kCopyWindowBytes): one
+// CTA copies one tile of a segment to a group of a.dgroup = G of its
+// destinations, and the work items run group by group within windows of
+// kCopyWindow tiles -- item b is tile (b / (W NG)) W + b % W for destination
+// group (b / W) % NG, NG = ceil(D / G).  The CTAs in flight then write a
+// few destinations at a time, while the window's source tiles, read from
+// HBM for the first group, are read again from L2: the source is loaded
 // with an L2 evict-last policy so that the L2's replacement keeps it
 // (without the hint the reuse depended on what had run before), and the CTA
-// of a tile's last destination returns the tile's lines to normal priority.
-// Measured on GB300, broadcast at P = 8, 64 MiB - 1 GiB per replica:
-// 1.04-1.08 of the copy peak against 0.96-0.99 when each CTA wrote its tile
-// to every destination (windows of 512-2048 tiles measured; 1024 best).
-// For an all-gather (one source segment per rank) the same order measured
-// 0.88-0.91 with the hint and 0.92-1.07 without it depending on what had
-// run before; with the priority reset too, 0.90 at P = 8 (256 MiB and
-// 1 GiB per replica) against 0.98-1.00 in the classic order, and no better
-// at P = 4.  So an all-gather keeps the order below.
+// of a tile's last group returns the tile's lines to normal priority.
+//
+// The host takes G = ceil(D / 4): about four groups per window.  Measured on
+// GB300 at 256 MiB per replica, of the copy peak, back to back (4 vectors per
+// thread): all-gather P = 8 (D = 7) G = 1 / 2 / 3 / 4: 1.07 / 1.09 / 1.07 /
+// 1.04, every destination from one CTA (the classic order below) 0.99;
+// all-gather P = 4 (D = 3) G = 1 / 2 / 3: 1.05 / 1.03 / 1.01, classic 1.01;
+// broadcast P = 8, G = 1: 1.09.  ncu on the classic order: 15 % issue
+// activity but 83 % DRAM throughput (seven write streams at once); on
+// windowed items of one destination and 8 KB, 70 % issue activity, the
+// per-item work (segment search, window arithmetic, priority reset) limiting
+// the rate, and the same DRAM bytes and L2 hits as the broadcast.
 //
 // Other copies (a.ndst = 0): each CTA copies one tile to every destination
-// of its segment (all-gather 0.96-0.99; small broadcasts, below
-// kCopyWindowMin tiles, 0.92 against 0.87 for single calls from a cold
-// L2 at 16 MiB per replica, as fewer CTAs carry the same bytes).
-constexpr uint64_t kCopyWindow = 1024;
-constexpr uint64_t kCopyWindowMin = 4 * kCopyWindow;
+// of its segment (small copies, below kCopyWindowBytes: 0.92 against
+// 0.87 for single broadcasts from a cold L2 at 16 MiB per replica in the
+// windowed order, as fewer CTAs carry the same bytes).
+constexpr uint64_t kCopyWindow = 1024;          // tiles per window: 16 MB of source
+constexpr uint64_t kCopyWindowBytes = 32u << 20;  // copies of at least this much source
 
 // 16-byte load that asks L2 to keep the line (policy from createpolicy).
 __device__ __forceinline__ uint4 ld_keep(const uint4* p, uint64_t policy) {
@@ -317,9 +326,9 @@ __device__ __forceinline__ uint4 ld_keep(const uint4* p, uint64_t policy) {
   return r;
 }
 
-template <class Cap>
+template <class Cap, int U>
 __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTable<Cap> a) {
-  constexpr uint64_t kTileVec = uint64_t(kCopyUnroll) * kThreads;
+  constexpr uint64_t kTileVec = uint64_t(U) * kThreads;
   griddep_launch_dependents();
   griddep_wait();
   if (a.ndst == 0) {  // small copies: one tile to every destination per CTA
@@ -336,15 +345,15 @@ __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTa
       if (a.flags[s] & kSegVec) {
         const uint64_t nvec = nbytes / 16;
         const uint64_t v0 = lt * kTileVec + threadIdx.x;
-        uint4 x[kCopyUnroll];
+        uint4 x[U];
 #pragma unroll
-        for (int u = 0; u < kCopyUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
           const uint64_t vi = v0 + uint64_t(u) * kThreads;
           GAR_CHECK(vi >= nvec || (vi + 1) * 16 <= nbytes, a.status);
-          if (vi < nvec) x[u] = ld_stream(static_cast<const uint4*>(src) + vi);
+          if (vi < nvec) x[u] = ld_stream_ro(static_cast<const uint4*>(src) + vi);
         }
 #pragma unroll
-        for (int u = 0; u < kCopyUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
           const uint64_t vi = v0 + uint64_t(u) * kThreads;
           if (vi < nvec)
             for (int d = 0; d < nd; ++d) st_stream(static_cast<uint4*>(dst[d]) + vi, x[u]);
@@ -373,40 +382,46 @@ __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTa
   uint64_t keep;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
   const uint32_t D = uint32_t(a.ndst);
-  const uint64_t items = (uint64_t(a.ntiles) + kCopyWindow - 1) / kCopyWindow * kCopyWindow * D;
+  const uint32_t G = a.dgroup > 0 ? uint32_t(a.dgroup) : 1u;  // destinations per item
+  const uint32_t NG = (D + G - 1) / G;                        // destination groups
+  const uint64_t items = (uint64_t(a.ntiles) + kCopyWindow - 1) / kCopyWindow * kCopyWindow * NG;
   for (uint64_t b = blockIdx.x; b < items; b += gridDim.x) {
-    // (window, destination) pair and tile: a shift and one 32-bit division
-    // (pairs number below 2^32: tiles / kCopyWindow * D).
+    // (window, destination group) pair and tile: a shift and one 32-bit
+    // division (pairs number below 2^32: tiles / kCopyWindow * NG).
     const uint32_t q = uint32_t(b / kCopyWindow);
-    const uint32_t win = q / D, d = q - win * D;
+    const uint32_t win = q / NG, g = q - win * NG;
     const uint64_t tile = uint64_t(win) * kCopyWindow + b % kCopyWindow;
     if (tile >= a.ntiles) continue;
     const uint32_t s = seg_of(a, uint32_t(tile), 0);
     check_segment(a, s, uint32_t(tile), kTileVec * 16);
     const uint32_t nd = a.flags[s] >> 8;
-    if (d >= nd) continue;
-    GAR_CHECK(a.dst_off + int(d) < a.stride, a.status);
+    const uint32_t d0 = g * G;
+    if (d0 >= nd) continue;
+    const uint32_t d1 = min(d0 + G, nd);
+    GAR_CHECK(a.dst_off + int(d1) <= a.stride, a.status);
     const uint64_t nbytes = a.numel[s];
     void* const* seg = a.ptr + uint64_t(s) * a.stride;
     const void* src = seg[0];
-    void* out = seg[a.dst_off + d];
+    void* const* outs = seg + a.dst_off;
     const uint64_t lt = tile - a.tile0[s];
     if (a.flags[s] & kSegVec) {
       const uint64_t nvec = nbytes / 16;
       const uint64_t v0 = lt * kTileVec + threadIdx.x;
-      uint4 x[kCopyUnroll];
+      uint4 x[U];
 #pragma unroll
-      for (int u = 0; u < kCopyUnroll; ++u) {
+      for (int u = 0; u < U; ++u) {
         const uint64_t vi = v0 + uint64_t(u) * kThreads;
         GAR_CHECK(vi >= nvec || (vi + 1) * 16 <= nbytes, a.status);
         if (vi < nvec) x[u] = ld_keep(static_cast<const uint4*>(src) + vi, keep);
       }
+      for (uint32_t d = d0; d < d1; ++d) {
 #pragma unroll
-      for (int u = 0; u < kCopyUnroll; ++u) {
-        const uint64_t vi = v0 + uint64_t(u) * kThreads;
-        if (vi < nvec) st_stream(static_cast<uint4*>(out) + vi, x[u]);
+        for (int u = 0; u < U; ++u) {
+          const uint64_t vi = v0 + uint64_t(u) * kThreads;
+          if (vi < nvec) st_stream(static_cast<uint4*>(outs[d]) + vi, x[u]);
+        }
       }
-      if (d + 1 == nd) {
+      if (d1 == nd) {
         // The tile's last destination: its source lines go back to normal
         // eviction priority.  Lines are 128 bytes: each address is the
         // 128-byte boundary at or below a byte of the tile (so inside the
@@ -421,7 +436,10 @@ __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTa
       if (lt + 1 == a.tile0[s + 1] - a.tile0[s]) {
         const uint64_t h = (nvec * 16) / 2 + threadIdx.x;  // 2-byte units of the tail
         GAR_CHECK(h >= nbytes / 2 || 2 * h + 2 <= nbytes, a.status);
-        if (h < nbytes / 2) static_cast<uint16_t*>(out)[h] = static_cast<const uint16_t*>(src)[h];
+        if (h < nbytes / 2) {
+          const uint16_t x1 = static_cast<const uint16_t*>(src)[h];
+          for (uint32_t d = d0; d < d1; ++d) static_cast<uint16_t*>(outs[d])[h] = x1;
+        }
       }
     } else {
       const uint64_t h0 = lt * kTileVec * 8;  // 2-byte units per tile
@@ -429,7 +447,8 @@ __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTa
         const uint64_t h = h0 + k;
         if (h >= nbytes / 2) break;
         GAR_CHECK(2 * h + 2 <= nbytes, a.status);
-        static_cast<uint16_t*>(out)[h] = static_cast<const uint16_t*>(src)[h];
+        const uint16_t x1 = static_cast<const uint16_t*>(src)[h];
+        for (uint32_t d = d0; d < d1; ++d) static_cast<uint16_t*>(outs[d])[h] = x1;
       }
     }
   }
@@ -712,9 +731,19 @@ __host__ __device__ constexpr uint64_t reduce_acc_tile_elems(int elems_per_vec) 
   return uint64_t(kThreads) * elems_per_vec;
 }
 
-// Tile of the copy kernel, in bytes.
-__host__ __device__ constexpr uint64_t copy_tile_bytes() {
-  return uint64_t(kCopyUnroll) * kThreads * 16;
+// Vectors per thread of a copy of `src_bytes` of source: 1 below 8 MiB, 2
+// below kCopyWindowBytes, kCopyUnroll (and the windowed order) above.
+// Measured on GB300 (broadcast and all-gather, P = 2, 4, 8, of the copy
+// peak, one vector / two): at 4 MiB per replica 0.69-0.86 / 0.52-0.63
+// replayed from a CUDA graph and the same cold; at 16 MiB 0.91-1.13 /
+// 0.93-1.17 graph-replayed, 0.48-0.88 / 0.51-0.95 cold.
+__host__ __device__ constexpr int copy_unroll_for(uint64_t src_bytes) {
+  return src_bytes < (8u << 20) ? 1 : (src_bytes < kCopyWindowBytes ? 2 : kCopyUnroll);
+}
+
+// Tile of the copy kernel, in bytes, for a copy of `src_bytes` of source.
+__host__ __device__ constexpr uint64_t copy_tile_bytes(uint64_t src_bytes) {
+  return uint64_t(copy_unroll_for(src_bytes)) * kThreads * 16;
 }
 
 }  // namespace gar

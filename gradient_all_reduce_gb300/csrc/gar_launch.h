@@ -99,7 +99,6 @@ struct SyncBnArgs {
   double eps;
   uint64_t channels;
   int np;
-  uint32_t lanes;                 // channels per warp (set by the launch)
   uint32_t* status;               // the comm's status word (debug-build checks)
 };
 cudaError_t launch_syncbn_stats(const LaunchCtx& ctx, const SyncBnArgs& args);

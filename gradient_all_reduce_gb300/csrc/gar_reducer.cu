@@ -161,6 +161,8 @@ void start_group(SegTable<CapLarge>& g, const SegTable<Cap>& src) {
   g.mu = src.mu;
   g.scale = src.scale;
   g.first = src.first;
+  g.unroll = src.unroll;
+  g.dgroup = src.dgroup;
   g.stages = src.stages;
   g.stage_bytes = src.stage_bytes;
   g.status = src.status;

@@ -373,3 +373,145 @@ def test_chained_collectives_without_syncs(comms, dt):
         assert_bits_equal(got, want, f"{dt} replica {r} after {seq}")
     assert_bits_equal(to_np(w), hw, "master")
     assert_bits_equal(to_np(v), hv, "momentum")
+
+
+def _copy_comm(P, group):
+    """A comm whose windowed copies take `group` destinations per item
+    (None: the library's default rule)."""
+    import os
+    old = os.environ.get("GAR_COPY_GROUP")
+    if group is not None:
+        os.environ["GAR_COPY_GROUP"] = str(group)
+    try:
+        return gar.ar_init(P, 0, gar.AR_MEAN)
+    finally:
+        if old is None:
+            os.environ.pop("GAR_COPY_GROUP", None)
+        else:
+            os.environ["GAR_COPY_GROUP"] = old
+
+
+# Sizes above the 32 MB of source at which copies take the windowed order:
+# a ragged tail (not a whole number of 16-byte vectors) and a partial last
+# window.
+WINDOWED_BYTES = (32 << 20) + (3 << 20) + 6
+
+
+@pytest.mark.parametrize("P", [2, 3, 5, 8])
+@pytest.mark.parametrize("group", [None, 1, 2, 3, 7])
+def test_windowed_all_gather(P, group):
+    """All-gather of shards large enough for the windowed order, with every
+    destination-group size: out of place, in place, in place for some ranks
+    only (segments with different destination counts), and shards one
+    element past a 16-byte boundary (the scalar path), against the oracle."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    dt = "bf16"
+    shard = WINDOWED_BYTES // 2 // P
+    n = shard * P
+    comm = _copy_comm(P, group)
+    try:
+        host = host_replicas(P, shard, dt, "uniform", 80 + P)
+        want = oracle.all_gather(host)
+        xs = replicas(P, shard, dt, "uniform", 80 + P)
+        ys = [empty(n, dt) for _ in range(P)]
+        gar.ar_all_gather(comm, xs, ys, n, DT[dt])
+        _sync_ok(comm)
+        for r in range(P):
+            assert_bits_equal(to_np(ys[r]), want[r], f"out of place {r}")
+        for in_place in ({*range(P)}, {r for r in range(P) if r % 2 == 0}):
+            ys = [empty(n, dt) for _ in range(P)]
+            send = []
+            for r in range(P):
+                if r in in_place:
+                    ys[r][r * shard:(r + 1) * shard].copy_(xs[r])
+                    send.append(ys[r][r * shard:(r + 1) * shard])
+                else:
+                    send.append(xs[r])
+            gar.ar_all_gather(comm, send, ys, n, DT[dt])
+            _sync_ok(comm)
+            for r in range(P):
+                assert_bits_equal(to_np(ys[r]), want[r], f"in place {sorted(in_place)} rank {r}")
+        xs1 = replicas(P, shard, dt, "uniform", 80 + P, offset=1)
+        ys1 = [empty(n, dt, offset=1) for _ in range(P)]
+        gar.ar_all_gather(comm, xs1, ys1, n, DT[dt])
+        _sync_ok(comm)
+        for r in range(P):
+            assert_bits_equal(to_np(ys1[r]), want[r], f"unaligned {r}")
+    finally:
+        gar.ar_destroy(comm)
+
+
+@pytest.mark.parametrize("P", [2, 4, 8, 16])
+@pytest.mark.parametrize("group", [None, 1, 3, 15])
+def test_windowed_broadcast(P, group):
+    """Broadcast of a buffer large enough for the windowed order, from the
+    first, a middle and the last root, aligned and unaligned, against the
+    oracle."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    dt = "f32"
+    n = WINDOWED_BYTES // 4 + 1
+    comm = _copy_comm(P, group)
+    try:
+        for root, offset in ((0, 0), (P // 2, 1), (P - 1, 0)):
+            xs = replicas(P, n, dt, "uniform", 90, offset=offset)
+            gar.ar_broadcast(comm, xs, n, DT[dt], root)
+            _sync_ok(comm)
+            want = host_replicas(1, n, dt, "uniform", 90 + root)[0]   # the root's draws
+            for r in range(P):
+                assert_bits_equal(to_np(xs[r]), want, f"root {root} rank {r}")
+    finally:
+        gar.ar_destroy(comm)
+
+
+# Between 8 MiB and 32 MB of source a copy takes two vectors per thread in the
+# classic order; below 8 MiB one.
+MID_BYTES = (12 << 20) + 6
+
+
+@pytest.mark.parametrize("P", [2, 3, 8])
+@pytest.mark.parametrize("nbytes", [MID_BYTES, (6 << 20) + 2])
+def test_mid_size_copies(P, nbytes):
+    """All-gather (out of place, in place, in place for some ranks,
+    unaligned) and broadcast (three roots, unaligned) at sizes of each
+    small-copy tile class, against the oracle."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    dt = "bf16"
+    comm = gar.ar_init(P, 0, gar.AR_MEAN)
+    try:
+        shard = nbytes // 2 // P
+        n = shard * P
+        host = host_replicas(P, shard, dt, "uniform", 110 + P)
+        want = oracle.all_gather(host)
+        xs = replicas(P, shard, dt, "uniform", 110 + P)
+        for in_place in (set(), {*range(P)}, {r for r in range(P) if r % 2 == 1}):
+            ys = [empty(n, dt) for _ in range(P)]
+            send = []
+            for r in range(P):
+                if r in in_place:
+                    ys[r][r * shard:(r + 1) * shard].copy_(xs[r])
+                    send.append(ys[r][r * shard:(r + 1) * shard])
+                else:
+                    send.append(xs[r])
+            gar.ar_all_gather(comm, send, ys, n, DT[dt])
+            _sync_ok(comm)
+            for r in range(P):
+                assert_bits_equal(to_np(ys[r]), want[r], f"in place {sorted(in_place)} rank {r}")
+        xs1 = replicas(P, shard, dt, "uniform", 110 + P, offset=1)
+        ys1 = [empty(n, dt, offset=1) for _ in range(P)]
+        gar.ar_all_gather(comm, xs1, ys1, n, DT[dt])
+        _sync_ok(comm)
+        for r in range(P):
+            assert_bits_equal(to_np(ys1[r]), want[r], f"unaligned {r}")
+        nb = nbytes // 2
+        for root, offset in ((0, 1), (P - 1, 0)):
+            bs = replicas(P, nb, dt, "uniform", 120, offset=offset)
+            gar.ar_broadcast(comm, bs, nb, DT[dt], root)
+            _sync_ok(comm)
+            src = host_replicas(1, nb, dt, "uniform", 120 + root)[0]
+            for r in range(P):
+                assert_bits_equal(to_np(bs[r]), src, f"broadcast root {root} rank {r}")
+    finally:
+        gar.ar_destroy(comm)
