@@ -23,29 +23,26 @@
 
 namespace gar {
 
-// The kernel specialisation that serves P ranks: P itself for 1 .. 8 (a
-// compile-time rank count: registers for exactly P ranks, and a Mean over a
-// P that is not a power of two divides by a compile-time constant);
-// otherwise a bounded kernel sized for at most 12 or 16 ranks (PT = -12, 0)
-// with P read at run time.  Host (tile sizes) and launch agree on it.
+// The kernel specialisation that serves P ranks: P itself, for every P from
+// 1 to kMaxRanks -- registers for exactly P ranks, loops of exactly P, and a
+// Mean over a P that is not a power of two divides by a compile-time
+// constant.  (The register-staged kernels no longer use the runtime-P form
+// Ranks<0>; the bulk-copy pipeline keeps it for P outside 2, 4, 8.)
 //
-// Up to 8 ranks used to share three compile-time kernels (2, 4, 8) and two
-// bounded ones (at most 4 and 8 ranks), whose registers were sized for
-// their largest P: the last no_sync micro-batch at P = 5 took 149 registers
-// in the 8-rank kernel, 17 % of the SM's warps active and 79 % of DRAM
-// throughput on GB300.
-__host__ __device__ constexpr int rank_class(int P) {
-  return P <= 8 ? P : (P <= 12 ? -12 : 0);
-}
+// Kernels sized for the largest P of a class of rank counts, with P read at
+// run time, paid for registers they did not use: the last no_sync
+// micro-batch at P = 5 took 149 registers in the 8-rank kernel, 17 % of the
+// SM's warps active and 79 % of DRAM throughput on GB300 (0.94 of the copy
+// peak; 1.03 with the kernel for exactly 5 ranks).
+__host__ __device__ constexpr int rank_class(int P) { return P; }
 
 // Vectors per thread per tile: enough 16-byte loads in flight per thread
 // (P * U * 16 bytes) to cover HBM latency, bounded by registers: 4 for up
-// to 4 ranks, 2 for up to 8, 1 for the bounded kernels, which hold
-// registers for ranks they may not use (at 12 ranks, U = 1 took 80
-// registers and 3 CTAs per SM against 101 and 2 with U = 2: 0.91 -> 1.03
-// of the copy peak on GB300 at 128 MiB per replica).
+// to 4 ranks, 2 for up to 8, 1 above (at 12 ranks, U = 1 took 80 registers
+// and 3 CTAs per SM against 101 and 2 with U = 2: 0.91 -> 1.03 of the copy
+// peak on GB300 at 128 MiB per replica).
 __host__ __device__ constexpr int unroll_for(int PT) {
-  return PT <= 0 ? 1 : (PT <= 4 ? 4 : 2);
+  return (PT <= 0 || PT > 8) ? 1 : (PT <= 4 ? 4 : 2);
 }
 // With the fused SGD step each vector also carries its fp32 master weights
 // and momentum (2 x E floats), all loaded up front: 2 vectors per thread for
@@ -53,7 +50,7 @@ __host__ __device__ constexpr int unroll_for(int PT) {
 // of the copy peak back to back against 0.978 with 1), 1 beyond, where 2
 // would take one CTA per SM (168 registers at 12 ranks).
 __host__ __device__ constexpr int unroll_for_sgd(int PT) {
-  return PT <= 0 ? 1 : 2;  // 2 for up to 8 ranks, 1 for the bounded kernels
+  return (PT <= 0 || PT > 8) ? 1 : 2;  // 2 for up to 8 ranks, 1 above
 }
 // Copy vectors per thread: 4 (16 KB tiles) for large copies.  The windowed
 // copies below are bound by the work each CTA does per item, which a
@@ -575,7 +572,9 @@ __global__ void __launch_bounds__(kThreads) k_accumulate(const __grid_constant__
 // tried here too: from a cold L2 it gained at P = 2 and 4 (1.01 -> 1.05,
 // 1.03 -> 1.05) but back to back nothing, and the runtime-P kernels lost
 // 0.02-0.04 to the 10-16 registers it added, so the vector layout stays.
-__host__ __device__ constexpr int acc_threads(int PT) { return PT <= 0 ? kThreads / 2 : kThreads; }
+__host__ __device__ constexpr int acc_threads(int PT) {
+  return (PT <= 0 || PT > 8) ? kThreads / 2 : kThreads;
+}
 
 template <int PT>
 __device__ __forceinline__ float total_of(float g, float acc, float scale, bool first) {
