@@ -175,7 +175,9 @@ __global__ void __launch_bounds__(kSyncBnThreads) k_syncbn_stats(const __grid_co
     }
     const double m = __ddiv_rn(s1, a.n);
     const double var = __dsub_rn(__ddiv_rn(s2, a.n), __dmul_rn(m, m));
-    const double is = __ddiv_rn(1.0, __dsqrt_rn(__dadd_rn(var, a.eps)));
+    // 1 / sqrt(var + eps): the correctly rounded reciprocal is the IEEE
+    // quotient 1 / x, by a shorter sequence than the general division.
+    const double is = __drcp_rn(__dsqrt_rn(__dadd_rn(var, a.eps)));
     if (mine) {
       a.mean[k][c] = __double2float_rn(m);
       a.invstd[k][c] = __double2float_rn(is);
