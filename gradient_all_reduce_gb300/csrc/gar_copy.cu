@@ -151,7 +151,6 @@ __global__ void __launch_bounds__(kSyncBnThreads) k_syncbn_stats(const __grid_co
   constexpr int L = syncbn_group(NP);    // lanes per channel
   constexpr int CPW = 32 / L;            // channels per warp
   griddep_launch_dependents();
-  griddep_wait();
   GAR_CHECK(a.np == NP, a.status);
   const int lane = int(threadIdx.x & 31u);
   const int k = lane % L;                // the rank this lane loads and stores
@@ -162,10 +161,13 @@ __global__ void __launch_bounds__(kSyncBnThreads) k_syncbn_stats(const __grid_co
     const uint64_t c = base + uint64_t(lane / L);
     const bool mine = k < NP && c < a.channels;
     GAR_CHECK(!mine || c < a.channels, a.status);
+    const float* p1 = a.sum[k < NP ? k : 0];
+    const float* p2 = a.sqsum[k < NP ? k : 0];
+    griddep_wait();  // the parameter reads above overlap the previous kernel's drain
     double x1 = 0.0, x2 = 0.0;
     if (mine) {
-      x1 = double(__ldg(a.sum[k] + c));
-      x2 = double(__ldg(a.sqsum[k] + c));
+      x1 = double(__ldg(p1 + c));
+      x2 = double(__ldg(p2 + c));
     }
     double s1 = __shfl_sync(0xFFFFFFFFu, x1, g0), s2 = __shfl_sync(0xFFFFFFFFu, x2, g0);
 #pragma unroll

@@ -144,7 +144,10 @@ __device__ __forceinline__ void reg_fence(float4& v) {
 
 // Programmatic dependent launch: let the next kernel of the stream start
 // its launch now, and wait until the previous kernel has finished and its
-// writes are visible (both are no-ops when the launch did not opt in).
+// writes are visible (both are no-ops when the launch did not opt in).  A
+// kernel calls the wait before its first global-memory access and after
+// its reads of its own parameter table, which need nothing from the
+// previous kernel; the wait returns at once when called again.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

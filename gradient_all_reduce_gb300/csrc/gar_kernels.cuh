@@ -167,7 +167,6 @@ __global__ void __launch_bounds__(kThreads)
   const int np = a.np;
   const bool mean = a.mean != 0;
   griddep_launch_dependents();
-  griddep_wait();
   uint32_t s = 0;
   for (uint32_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
     s = seg_of(a, tile, s);
@@ -181,8 +180,18 @@ __global__ void __launch_bounds__(kThreads)
     float* w = SGD ? a.master[s] : nullptr;
     float* v = SGD ? a.mom[s] : nullptr;
     GAR_CHECK(!SGD || (w != nullptr && v != nullptr), a.status);
+    const bool vec = (a.flags[s] & kSegVec) != 0;
+    const void* src[MAXP];
+#pragma unroll
+    for (int r = 0; r < MAXP; ++r)
+      if (Ranks<PT>::has(r, np)) src[r] = seg[r];
+    // Everything above reads the launch's own table (kernel parameters),
+    // nothing the previous kernel writes: under programmatic dependent
+    // launch it runs while that kernel drains.  Memory is touched only after
+    // the wait (which returns at once after its first call).
+    griddep_wait();
 
-    if (a.flags[s] & kSegVec) {
+    if (vec) {
       const uint64_t nvec = n / E;
       const uint64_t v0 = lt * kTileVec + threadIdx.x;
       // Every load of the tile (all replicas, and w, v with SGD) is issued
@@ -197,7 +206,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
           for (int r = 0; r < MAXP; ++r)
             if (Ranks<PT>::has(r, np))
-              in[u][r] = ld_stream(static_cast<const uint4*>(seg[r]) + vi);
+              in[u][r] = ld_stream(static_cast<const uint4*>(src[r]) + vi);
           if constexpr (SGD) {
 #pragma unroll
             for (int q = 0; q < WV; ++q) {
@@ -327,7 +336,6 @@ template <class Cap, int U>
 __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTable<Cap> a) {
   constexpr uint64_t kTileVec = uint64_t(U) * kThreads;
   griddep_launch_dependents();
-  griddep_wait();
   if (a.ndst == 0) {  // small copies: one tile to every destination per CTA
     for (uint32_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
       const uint32_t s = seg_of(a, tile, 0);
@@ -339,6 +347,7 @@ __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTa
       const uint64_t lt = tile - a.tile0[s];
       const int nd = int(a.flags[s] >> 8);
       GAR_CHECK(a.dst_off + nd <= a.stride && nbytes % 2 == 0, a.status);
+      griddep_wait();  // the table lookups above overlap the previous kernel's drain
       if (a.flags[s] & kSegVec) {
         const uint64_t nvec = nbytes / 16;
         const uint64_t v0 = lt * kTileVec + threadIdx.x;
@@ -401,6 +410,7 @@ __global__ void __launch_bounds__(kThreads) k_copy(const __grid_constant__ SegTa
     const void* src = seg[0];
     void* const* outs = seg + a.dst_off;
     const uint64_t lt = tile - a.tile0[s];
+    griddep_wait();  // the table lookups above overlap the previous kernel's drain
     if (a.flags[s] & kSegVec) {
       const uint64_t nvec = nbytes / 16;
       const uint64_t v0 = lt * kTileVec + threadIdx.x;
@@ -479,7 +489,6 @@ __global__ void __launch_bounds__(kThreads) k_accumulate(const __grid_constant__
   constexpr int J = kAccUnroll * D::kElems / 4;  // quads per thread per tile
   constexpr uint64_t kTileQuads = uint64_t(J) * kThreads;
   griddep_launch_dependents();
-  griddep_wait();
   uint32_t s = 0;
   for (uint32_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
     s = seg_of(a, tile, s);
@@ -489,6 +498,7 @@ __global__ void __launch_bounds__(kThreads) k_accumulate(const __grid_constant__
     const void* g = a.ptr[uint64_t(s) * a.stride];
     float* acc = static_cast<float*>(a.ptr[uint64_t(s) * a.stride + 1]);
     const uint64_t lt = tile - a.tile0[s];
+    griddep_wait();  // the table lookups above overlap the previous kernel's drain
     if (a.flags[s] & kSegVec) {
       const uint64_t nq = n / 4;
       const uint64_t q0 = lt * kTileQuads + threadIdx.x;
@@ -658,7 +668,6 @@ __global__ void __launch_bounds__(kThreads)
   const int np = a.np;
   const bool mean = a.mean != 0, first = a.first != 0;
   griddep_launch_dependents();
-  griddep_wait();
   uint32_t s = 0;
   for (uint32_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
     s = seg_of(a, tile, s);
@@ -671,6 +680,7 @@ __global__ void __launch_bounds__(kThreads)
     float* w = SGD ? a.master[s] : nullptr;
     float* v = SGD ? a.mom[s] : nullptr;
     GAR_CHECK(!SGD || (w != nullptr && v != nullptr), a.status);
+    griddep_wait();  // the table lookups above overlap the previous kernel's drain
     if (a.flags[s] & kSegVec) {
       const uint64_t nvec = n / E;
 #pragma unroll
