@@ -22,8 +22,8 @@ INCLUDE = ROOT / "include"
 LIB = PKG / "libgar.so"
 LIB_DEBUG = PKG / "libgar_debug.so"
 
-UNITS = ["gar_api.cu", "gar_reducer.cu", "gar_copy.cu", "gar_reduce_f32.cu", "gar_reduce_bf16.cu",
-         "gar_sgd_f32.cu", "gar_sgd_bf16.cu", "gar_acc_f32.cu", "gar_acc_bf16.cu"]
+UNITS = ["gar_api.cu", "gar_noalloc.cu", "gar_reducer.cu", "gar_copy.cu", "gar_reduce_f32.cu",
+         "gar_reduce_bf16.cu", "gar_sgd_f32.cu", "gar_sgd_bf16.cu", "gar_acc_f32.cu", "gar_acc_bf16.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # The kernel images are stored compressed (many specialisations, each
 # loaded on first use).

@@ -86,9 +86,9 @@ def test_bucket_plan_matches_oracle(gar):
 
 
 def test_no_alloc_entry_point_source_allocates_nothing():
-    """The allocation-free all-reduce's section of the C ABI source calls
-    no allocating CUDA routine."""
-    src = (ROOT / "gradient_all_reduce_gb300" / "csrc" / "gar_api.cu").read_text()
+    """The allocation-free all-reduce's source file (its static array, its
+    set-up and the entry point) calls no allocating CUDA routine."""
+    src = (ROOT / "gradient_all_reduce_gb300" / "csrc" / "gar_noalloc.cu").read_text()
     section = src[src.index("// All-reduce without any allocation."):]
     section = re.sub(r"//[^\n]*", "", section)   # the comments explain why; check the code
     for word in ("cudaMalloc", "cudaFree", "cudaHostAlloc", "cudaMallocAsync", "new ", "malloc("):
