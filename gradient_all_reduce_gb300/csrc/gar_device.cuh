@@ -233,9 +233,11 @@ struct BF16 {
 };
 
 // ---------------------------------------------------------- reduction
-// PT > 0: P is the compile-time constant PT.  PT < 0: P is the runtime
-// value np, at most -PT; PT == 0: at most kMaxRanks.  Bounded loops run to
-// the maximum under a guard so the operands stay in registers.
+// PT > 0: P is the compile-time constant PT (every register-staged kernel).
+// PT < 0: P is the runtime value np, at most -PT; PT == 0: at most
+// kMaxRanks (the bulk-copy pipeline's kernel for P outside 2, 4, 8).
+// Bounded loops run to the maximum under a guard so the operands stay in
+// registers.
 template <int PT>
 struct Ranks {
   static constexpr int kMax = PT > 0 ? PT : (PT < 0 ? -PT : kMaxRanks);
@@ -280,9 +282,8 @@ __device__ __forceinline__ float div_small_bf16(float x, float d, float r) {
 // quotient, so powers of two multiply instead (decided at compile time for
 // a fixed P, per call for a runtime P).  Other P divide by Markstein's
 // correction: always for a compile-time P (divisor and reciprocal are
-// constants), and for a runtime P when FAST (the bf16 kernels: 8 divisions
-// per vector); the fp32 kernels for a runtime P take the IEEE division (in
-// the bounded kernels the correction's registers cost one CTA per SM).
+// constants), and for a runtime P when FAST (the bulk-copy pipeline's bf16
+// kernel: 8 divisions per vector); its fp32 kernel takes the IEEE division.
 // BF16_OUT: the mean is only stored as bf16, so a quotient with the same
 // bf16 rounding serves (div_small_bf16).
 template <int PT, bool FAST = false, bool BF16_OUT = false>

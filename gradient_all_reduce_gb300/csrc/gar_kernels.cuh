@@ -566,22 +566,23 @@ __global__ void __launch_bounds__(kThreads) k_accumulate(const __grid_constant__
 // A thread takes one vector at a time and issues every load of it (the
 // gradients, the accumulators, and w and v with SGD) before any arithmetic.
 // Loading w and v only after the reduction cost a second round trip to HBM
-// per vector.  The kernels for a runtime P (the bounded rank classes) hold
-// registers for up to 4, 8, 12 or 16 ranks, which leaves room for two
-// 256-thread CTAs per SM at most; they run 128-thread CTAs that take the
-// tile's vectors in two turns, so that an SM holds more CTAs whose phases
+// per vector.  Above 8 ranks a kernel holds 162-252 registers, room for
+// one 256-thread CTA per SM; those kernels run 128-thread CTAs that take the
+// tile's vectors in two turns, so that an SM holds two CTAs whose phases
 // overlap.  Measured on GB300, one 25 MiB bf16 bucket per replica, Mean +
 // SGD, from a cold L2, as fractions of the copy peak:
 //   P                        2     3     4     5     6     8     11    16
 //   w, v after the reduction 0.62  0.62  0.69  -     0.77  1.01  0.86  0.94
 //   w, v up front            1.01  0.92  1.03  -     0.80  1.05  0.94  0.98
-//   + 128-thread CTAs        1.01  0.97  1.03  0.94  0.96  1.04  0.95  1.00
-// With 128-thread CTAs only from the 12-rank class up, P = 5 and 6 measured
-// 0.76 and 0.80; only from the 8-rank class up, P = 3 measured 0.92.  The
-// quad layout of k_accumulate (fp32 accesses contiguous across a warp) was
-// tried here too: from a cold L2 it gained at P = 2 and 4 (1.01 -> 1.05,
-// 1.03 -> 1.05) but back to back nothing, and the runtime-P kernels lost
-// 0.02-0.04 to the 10-16 registers it added, so the vector layout stays.
+//   kernels then sized for up to 4, 8, 12 or 16 ranks with P read at run
+//   time, 128-thread CTAs    1.01  0.97  1.03  0.94  0.96  1.04  0.95  1.00
+//   a kernel for every P     1.00  1.04  1.03  1.03  1.04  1.05  1.02  1.02
+// (The runtime-P kernels with 256-thread CTAs measured 0.76 and 0.80 at
+// P = 5 and 6.)  The quad layout of k_accumulate (fp32 accesses contiguous
+// across a warp) was tried here too: from a cold L2 it gained at P = 2 and 4
+// (1.01 -> 1.05, 1.03 -> 1.05) but back to back nothing, and the runtime-P
+// kernels lost 0.02-0.04 to the 10-16 registers it added, so the vector
+// layout stays.
 __host__ __device__ constexpr int acc_threads(int PT) {
   return (PT <= 0 || PT > 8) ? kThreads / 2 : kThreads;
 }
