@@ -6,7 +6,8 @@ statistics) checks each segment, tile and index against the launch's own
 table before it loads or stores, and a failed check sets a bit of the
 comm's status word and skips the access instead of trapping.  This test
 builds that library and runs the collective, bucket, accumulation, ZeRO-1,
-SyncBN, reducer and guard-band parity tests against it in a child process:
+SyncBN, reducer, guard-band and every-rank-count parity tests against it in
+a child process:
 they must pass against the oracle as before, with every comm's status
 still AR_OK when it is destroyed (tests/debug_status_plugin.py), and the
 child must have loaded the debug library and not the release one."""
@@ -22,7 +23,7 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 FILES = ["test_gpu_collectives.py", "test_gpu_buckets.py", "test_gpu_accumulate.py",
          "test_gpu_sharded.py", "test_gpu_syncbn.py", "test_gpu_reducer.py",
-         "test_gpu_guard_bands.py"]
+         "test_gpu_guard_bands.py", "test_gpu_every_rank_count.py"]
 
 
 def test_parity_cases_pass_under_the_debug_build():
