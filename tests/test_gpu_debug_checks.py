@@ -7,10 +7,9 @@ table before it loads or stores, and a failed check sets a bit of the
 comm's status word and skips the access instead of trapping.  This test
 builds that library and runs the collective, bucket, accumulation, ZeRO-1,
 SyncBN, reducer, guard-band and every-rank-count parity tests against it in
-a child process:
-they must pass against the oracle as before, with every comm's status
-still AR_OK when it is destroyed (tests/debug_status_plugin.py), and the
-child must have loaded the debug library and not the release one."""
+a child process: they must pass against the oracle as before, with every
+comm's status still AR_OK when it is destroyed (tests/debug_status_plugin.py),
+and the child must have loaded the debug library and not the release one."""
 import os
 import subprocess
 import sys
