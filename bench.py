@@ -484,7 +484,7 @@ class E2EStep:
 def time_e2e(args, device, stream):
     """The ViT step end to end from pinned host buffers (E2EStep), and the
     same transfers without the kernels (the host link's bound), measured
-    alike: after 3 warm-up steps, seven regions of K steps each, every region
+    alike: after 3 warm-up steps, eleven regions of K steps each, every region
     under one event pair with the same fill (``start``) and drain
     (``finish``), interleaved so that both meet the same traffic on the
     shared host; each figure is the median region (one region in three met
@@ -517,7 +517,7 @@ def time_e2e(args, device, stream):
                 e2e.copies_only(stream)
             e2e.finish(stream)
             torch.cuda.synchronize(device)
-            for _ in range(7):
+            for _ in range(11):
                 full.append(region(e2e.step))
                 link.append(region(e2e.copies_only))
         el, ln = statistics.median(full), statistics.median(link)
@@ -536,7 +536,7 @@ def time_e2e(args, device, stream):
                 "frac_of_link_bound": value / bound,
                 "best_ms_per_step": best * 1e3, "best_link_only_ms_per_step": best_link * 1e3,
                 "frac_of_link_bound_best": best_link / best,
-                "statistic": ("median of seven regions of `steps` steps for both the step and "
+                "statistic": ("median of eleven regions of `steps` steps for both the step and "
                               "the link-only transfers, each region with the same fill and drain, "
                               "the two kinds interleaved; *_best: the fastest region of each kind"),
                 "path": ("ar_reducer_* with per-bucket H2D on 4 copy streams and per-bucket D2H "
