@@ -562,7 +562,9 @@ def time_sweep(device, stream):
     """Flat all-reduce (Mean, in place) GB/s for P = 2, 4, 8 at 64 MiB,
     256 MiB and 1 GiB per replica, fp32 and bf16; reduce-scatter,
     all-gather and broadcast at 256 MiB per replica, P = 4 and 8; and the
-    latency of small all-reduces (4 KiB .. 1 MiB, P = 8, fp32).  L2 is
+    latency of small all-reduces (4 KiB .. 1 MiB, P = 8, fp32) and of
+    SyncBN statistics, each also as one of 20 dependent calls replayed from
+    one CUDA graph (chained_us).  L2 is
     flushed between repetitions (flush_l2: a 256 MiB write, then a 256 MiB
     read)."""
     import torch
@@ -586,6 +588,32 @@ def time_sweep(device, stream):
                     ts.append((e0, e1))
             torch.cuda.synchronize(device)
         return statistics.median(a.elapsed_time(b) / 1e3 for a, b in ts)
+
+    def chained(call, k=20):
+        """Per-call time of k calls captured in one CUDA graph, each kernel
+        chained to the one before by programmatic dependent launch: the
+        cost of one more dependent call in a sequence, launch overlapped
+        (the *_us rows beside it time a call alone, its launch included)."""
+        side = torch.cuda.Stream(device)
+        side.wait_stream(stream)
+        call(side)
+        torch.cuda.synchronize(device)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            cur = torch.cuda.current_stream()
+            for _ in range(k):
+                call(cur)
+        with torch.cuda.stream(stream):
+            graph.replay()
+            torch.cuda.synchronize(device)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+            for i in range(5):
+                ev[i].record(stream)
+                graph.replay()
+            ev[5].record(stream)
+            torch.cuda.synchronize(device)
+        del graph
+        return statistics.median(ev[i].elapsed_time(ev[i + 1]) for i in range(5)) / 1e3 / k
 
     for P in (2, 4, 8):
         comm = gar.ar_init(P, device.index, gar.AR_MEAN)
@@ -640,10 +668,13 @@ def time_sweep(device, stream):
                     with torch.cuda.graph(graph):
                         call(torch.cuda.current_stream())
                     t_graph = timed(graph.replay, 200, flush_between=False)
+                    del graph
+                    t_chain = chained(call)
                     out["small_all_reduce_us"].append({"P": P, "KiB_per_replica": kib,
                                                        "api_us": t_api * 1e6,
                                                        "prepared_us": t_prep * 1e6,
-                                                       "graph_us": t_graph * 1e6})
+                                                       "graph_us": t_graph * 1e6,
+                                                       "chained_us": t_chain * 1e6})
                     del xs
         finally:
             gar.ar_destroy(comm)
@@ -725,8 +756,11 @@ def time_sweep(device, stream):
             with torch.cuda.graph(graph):
                 call(torch.cuda.current_stream())
             t_graph = timed(graph.replay, 200, flush_between=False)
+            del graph
+            t_chain = chained(prep)
             res.append({"P": P, "channels": C, "api_us": t_api * 1e6,
-                        "prepared_us": t_prep * 1e6, "graph_us": t_graph * 1e6})
+                        "prepared_us": t_prep * 1e6, "graph_us": t_graph * 1e6,
+                        "chained_us": t_chain * 1e6})
         out["syncbn_stats_latency"] = res
     finally:
         gar.ar_destroy(comm)
@@ -1241,7 +1275,9 @@ def run_case(args):
     per replica for ar / rs / ag / bc (P and the element type from
     --case-ranks and --case-dtype; P = 8, fp32 by default); one 25 MiB bf16
     bucket for sgd, accfirst, acc and acclast (P from --case-ranks); the ViT-B/16 gradient
-    set (bf16, P = 8) for zero1."""
+    set (bf16, P = 8) for zero1.  Also the host's issue time per call in the
+    back-to-back loop (host_us) and the K calls replayed from one CUDA graph
+    (us_graph, GBps_graph, frac_graph)."""
     import torch
     import gradient_all_reduce_gb300 as gar
     from workloads import gpu as wgpu
@@ -1274,7 +1310,7 @@ def run_case(args):
                 "ag": (gar.PreparedCall("ar_all_gather", comm, ins, xs, n, dt), P * n * es),
                 "bc": (gar.PreparedCall("ar_broadcast", comm, xs, n, dt, 0), P * n * es),
             }[args.case]
-            fn = lambda: prep(stream)
+            call = prep
             what = f"P={P} {args.case_dtype} {args.case_mib} MiB per replica"
             if args.case in ("ar", "rs"):
                 what += f", {op_name}"
@@ -1286,8 +1322,8 @@ def run_case(args):
             params = [torch.empty(n, dtype=torch.bfloat16, device=device) for _ in range(P)]
             ws = [torch.zeros(n // P, device=device) for _ in range(P)]
             vs = [torch.zeros(n // P, device=device) for _ in range(P)]
-            fn = lambda: gar.ar_sharded_sgd_step(comm, g, params, ws, vs, n, gar.AR_BF16, 0.1, 0.9,
-                                                 gar.AR_MEAN, stream)
+            call = gar.PreparedCall("ar_sharded_sgd_step", comm, g, params, ws, vs, n, gar.AR_BF16,
+                                    gar.AR_MEAN, 0.1, 0.9)
             nbytes, what = 4 * P * n + 16 * n, "ViT-B/16 flat unit, P=8 bf16"
         elif args.case == "sgd":
             n = (25 << 20) // 2
@@ -1295,8 +1331,8 @@ def run_case(args):
             for r, x in enumerate(g):
                 wgpu.fill(x, "normal", 100 + r, std=1e-3)
             w, v = torch.zeros(n, device=device), torch.zeros(n, device=device)
-            fn = lambda: gar.ar_bucket_all_reduce(comm, [g], [n], gar.AR_BF16, gar.AR_MEAN,
-                                                  sgd=(0.1, 0.9, [w], [v], 1), stream=stream)
+            call = gar.PreparedBucket(comm, [g], [n], gar.AR_BF16, gar.AR_MEAN,
+                                      sgd=(0.1, 0.9, [w], [v], 1))
             nbytes = 4 * P * n + 16 * n
             what = f"one 25 MiB bf16 bucket, P={P}, Mean + SGD with write-back"
         elif args.case in ("accfirst", "acc"):
@@ -1306,8 +1342,8 @@ def run_case(args):
             for r, x in enumerate(g):
                 wgpu.fill(x, "normal", 100 + r, std=1e-3)
             acc = [[torch.zeros(n, device=device) for _ in range(P)]]
-            fn = lambda: gar.ar_bucket_accumulate(comm, [g], [n], gar.AR_BF16, acc, 0.25, first,
-                                                  stream)
+            call = lambda s: gar.ar_bucket_accumulate(comm, [g], [n], gar.AR_BF16, acc, 0.25,
+                                                      first, s)
             nbytes = (6 if first else 10) * P * n
             what = (f"one 25 MiB bf16 bucket, P={P}, "
                     + ("the first micro-batch" if first else "a micro-batch before the last"))
@@ -1318,9 +1354,9 @@ def run_case(args):
                 wgpu.fill(x, "normal", 100 + r, std=1e-3)
             acc = [[torch.zeros(n, device=device) for _ in range(P)]]
             w, v = torch.zeros(n, device=device), torch.zeros(n, device=device)
-            fn = lambda: gar.ar_bucket_all_reduce_accumulated(
+            call = lambda s: gar.ar_bucket_all_reduce_accumulated(
                 comm, [g], [n], gar.AR_BF16, acc, 0.25, False, gar.AR_MEAN,
-                sgd=(0.1, 0.9, [w], [v], 1), stream=stream)
+                sgd=(0.1, 0.9, [w], [v], 1), stream=s)
             nbytes = 8 * P * n + 16 * n
             what = f"one 25 MiB bf16 bucket, P={P}, the last micro-batch with Mean + SGD"
         else:
@@ -1329,15 +1365,18 @@ def run_case(args):
             sq = [torch.rand(C, device=device) + 1 for _ in range(P)]
             mo = [torch.empty(C, device=device) for _ in range(P)]
             io = [torch.empty(C, device=device) for _ in range(P)]
-            fn = lambda: gar.ar_syncbn_stats(comm, sums, sq, [1000] * P, mo, io, C, 1e-5, stream)
+            call = gar.PreparedCall("ar_syncbn_stats", comm, sums, sq, [1000] * P, mo, io, C, 1e-5)
             nbytes, what = 4 * P * C * 4, "P=8, 2048 channels"
+        fn = lambda: call(stream)
         for _ in range(max(1, args.warmup)):
             fn()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        h0 = time.perf_counter()
         for _ in range(args.steps):
             fn()
+        host = (time.perf_counter() - h0) / args.steps
         e1.record(stream)
         torch.cuda.synchronize()
         t = e0.elapsed_time(e1) / 1e3 / args.steps
@@ -1356,32 +1395,35 @@ def run_case(args):
         peak, _ = measured_peak()
         line = {"case": args.case, "workload": what, "us": t * 1e6, "GBps": nbytes / t / 1e9,
                 "frac": nbytes / t / 1e9 / peak, "us_cold": cold * 1e6,
-                "GBps_cold": nbytes / cold / 1e9, "frac_cold": nbytes / cold / 1e9 / peak}
-        if flat:
-            # The same calls replayed from one CUDA graph of K calls: no host
-            # time between launches, consecutive kernels chained by
-            # programmatic dependent launch (below ~40 MB per call the
-            # operands stay in L2 from one call to the next).
-            side = torch.cuda.Stream(device)
-            side.wait_stream(stream)
-            prep(side)
-            torch.cuda.synchronize()
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph):
-                cur = torch.cuda.current_stream()
-                for _ in range(args.steps):
-                    prep(cur)
+                "GBps_cold": nbytes / cold / 1e9, "frac_cold": nbytes / cold / 1e9 / peak,
+                "host_us": host * 1e6}
+        # The same calls replayed from one CUDA graph of K calls: no host
+        # time between launches, consecutive kernels chained by
+        # programmatic dependent launch (below ~40 MB per call the
+        # operands stay in L2 from one call to the next).  Back to back
+        # from the host, a call whose host issue time (host_us) is above
+        # its device time leaves the GPU idle between calls; the graph
+        # shows the device time alone.
+        side = torch.cuda.Stream(device)
+        side.wait_stream(stream)
+        call(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            cur = torch.cuda.current_stream()
+            for _ in range(args.steps):
+                call(cur)
+        graph.replay()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        with torch.cuda.stream(stream):
             graph.replay()
-            torch.cuda.synchronize()
-            e0.record(stream)
-            with torch.cuda.stream(stream):
-                graph.replay()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            tg = e0.elapsed_time(e1) / 1e3 / args.steps
-            line.update({"us_graph": tg * 1e6, "GBps_graph": nbytes / tg / 1e9,
-                         "frac_graph": nbytes / tg / 1e9 / peak})
-            del graph
+        e1.record(stream)
+        torch.cuda.synchronize()
+        tg = e0.elapsed_time(e1) / 1e3 / args.steps
+        line.update({"us_graph": tg * 1e6, "GBps_graph": nbytes / tg / 1e9,
+                     "frac_graph": nbytes / tg / 1e9 / peak})
+        del graph
         if not args.no_cpu:
             line["cpu_baseline"] = case_cpu_baseline(
                 args.case, P, args.case_dtype if flat else "bf16",
