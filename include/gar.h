@@ -406,11 +406,11 @@ ar_status_t ar_selftest_wait_timeout(ar_comm_t comm, unsigned timeout_ms, ar_str
  * allocating library routine.
  *
  * The first call on a device sets that device up (checks it is sm_103 and
- * looks up the array's device address in the device's context); make that
- * first call before any stream capture.  The address is kept for the rest
- * of the process: do not call this entry point on a device after
- * cudaDeviceReset has destroyed the context it was set up in.  Every call
- * clears the status word on `stream` before its launch.  All calls on a device share the one array, so calls whose work
+ * looks up the array's device address in the device's context).  The
+ * address is kept for the rest of the process: do not call this entry
+ * point on a device after cudaDeviceReset has destroyed the context it was
+ * set up in.  Every call clears the status word on `stream` before its
+ * launch.  All calls on a device share the one array, so calls whose work
  * overlaps on the GPU (different streams, no ordering between them) race on
  * it; calls on one stream are ordered and do not.  The status word has no
  * comm to be read through: a wait that gave up (after 2 s) leaves the
