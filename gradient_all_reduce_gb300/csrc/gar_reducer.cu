@@ -21,7 +21,13 @@
 // Buckets that one call completes together (mark_ready_many, finalize) go
 // out as one launch over their combined segment table when it fits one
 // parameter block: the same arithmetic per element, fewer launches and no
-// ramp-up and drain between them.
+// ramp-up and drain between them.  When one call completes every bucket of
+// the step and every tensor of the step was marked on one stream, nothing
+// is left to overlap with: the buckets launch on that stream itself, so
+// that consecutive steps' kernels follow each other on one stream, where
+// programmatic dependent launch lets each start while the one before
+// drains (a launch on a communication stream is joined by events on both
+// sides, which no kernel can start ahead of).
 #include <mutex>
 #include <new>
 #include <unordered_set>
@@ -40,6 +46,8 @@ struct ar_reducer_s {
     bool launched = false;
     cudaEvent_t done = nullptr;                // recorded after the bucket's kernel
     std::vector<cudaStream_t> mark_streams;    // distinct streams that marked its tensors
+    bool direct = false;                       // launched on its marking stream (below)
+    cudaStream_t direct_stream = nullptr;
   };
 
   ar_comm_s* comm = nullptr;
@@ -55,6 +63,8 @@ struct ar_reducer_s {
   bool used[2] = {false, false};
   int next = 0;
   cudaEvent_t join = nullptr;
+  bool direct = false;                         // this step's buckets went to direct_stream
+  cudaStream_t direct_stream = nullptr;
   SegTable<CapLarge> group;                    // combined table of buckets launched together
   uint64_t launches = 0;                       // kernel launches issued so far
 };
@@ -80,32 +90,101 @@ void release(ar_reducer_s* r) {
   delete r;
 }
 
-// Launch bucket b on the next communication stream, after the work of
-// every stream that marked one of its tensors.
-ar_status_t launch_bucket(ar_reducer_s* r, int b) {
-  ar_reducer_s::Bucket& bk = r->buckets[b];
-  const int k = r->next;
-  r->next ^= 1;
-  cudaStream_t s = r->streams[k];
-  for (cudaStream_t ms : bk.mark_streams) {
-    if (cudaEventRecord(r->join, ms) != cudaSuccess) return AR_ERR_CUDA;
-    if (cudaStreamWaitEvent(s, r->join, 0) != cudaSuccess) return AR_ERR_CUDA;
+// Where the buckets one call completes are launched: the communication
+// streams, or (direct) the one stream that marked every tensor of the step,
+// when the call completes every bucket of the step.
+struct Target {
+  bool direct = false;
+  cudaStream_t stream = nullptr;
+};
+
+Target pick_target(const ar_reducer_s* r, const std::vector<int>& ready) {
+  Target tg;
+  size_t nonempty = 0;
+  for (const auto& bk : r->buckets) {
+    if (bk.launched) return tg;
+    if (!bk.tensors.empty()) ++nonempty;
   }
+  if (ready.size() != nonempty || ready.empty()) return tg;
+  const cudaStream_t s = r->buckets[ready.front()].mark_streams.empty()
+                             ? nullptr
+                             : r->buckets[ready.front()].mark_streams.front();
+  for (int b : ready) {
+    const auto& ms = r->buckets[b].mark_streams;
+    if (ms.size() != 1 || ms.front() != s) return tg;
+  }
+  tg.direct = true;
+  tg.stream = s;
+  return tg;
+}
+
+// The stream of a launch: the next communication stream (index *k), after
+// the work of every stream that marked a tensor of buckets bs; or, direct,
+// the marking stream itself (*k = -1), which orders the launch already.
+ar_status_t launch_stream(ar_reducer_s* r, const Target& tg, const std::vector<int>& bs, int* k,
+                          cudaStream_t* s) {
+  if (tg.direct) {
+    *k = -1;
+    *s = tg.stream;
+    return AR_OK;
+  }
+  *k = r->next;
+  r->next ^= 1;
+  *s = r->streams[*k];
+  std::vector<cudaStream_t> waited;
+  for (int b : bs)
+    for (cudaStream_t ms : r->buckets[b].mark_streams) {
+      bool seen = false;
+      for (cudaStream_t x : waited) seen = seen || x == ms;
+      if (seen) continue;
+      waited.push_back(ms);
+      if (cudaEventRecord(r->join, ms) != cudaSuccess) return AR_ERR_CUDA;
+      if (cudaStreamWaitEvent(*s, r->join, 0) != cudaSuccess) return AR_ERR_CUDA;
+    }
+  return AR_OK;
+}
+
+// Buckets bs were launched on stream s (communication stream k, or direct
+// when k < 0).  On a communication stream their completion events are
+// recorded now; a direct launch records a bucket's event only when
+// ar_reducer_wait_bucket asks for it, so that nothing comes between
+// consecutive steps' kernels on the stream.
+ar_status_t note_launched(ar_reducer_s* r, const std::vector<int>& bs, int k, cudaStream_t s) {
+  if (k >= 0) {
+    if (cudaEventRecord(r->done[k], s) != cudaSuccess) return AR_ERR_CUDA;
+    r->used[k] = true;
+  } else {
+    r->direct = true;
+    r->direct_stream = s;
+  }
+  for (int b : bs) {
+    auto& bk = r->buckets[b];
+    if (k >= 0 && cudaEventRecord(bk.done, s) != cudaSuccess) return AR_ERR_CUDA;
+    bk.direct = k < 0;
+    bk.direct_stream = s;
+    bk.launched = true;
+  }
+  return AR_OK;
+}
+
+// Launch bucket b alone (each of its launch tables).
+ar_status_t launch_bucket(ar_reducer_s* r, int b, const Target& tg) {
+  ar_reducer_s::Bucket& bk = r->buckets[b];
+  int k = -1;
+  cudaStream_t s = nullptr;
+  ar_status_t st = launch_stream(r, tg, {b}, &k, &s);
+  if (st != AR_OK) return st;
   for (const auto& t : bk.small) {
-    ar_status_t st = run_reduce(r->comm, r->dtype, r->sgd, t, s);
+    st = run_reduce(r->comm, r->dtype, r->sgd, t, s);
     if (st != AR_OK) return st;
     if (t.ntiles > 0) ++r->launches;
   }
   for (const auto& t : bk.large) {
-    ar_status_t st = run_reduce(r->comm, r->dtype, r->sgd, t, s);
+    st = run_reduce(r->comm, r->dtype, r->sgd, t, s);
     if (st != AR_OK) return st;
     if (t.ntiles > 0) ++r->launches;
   }
-  if (cudaEventRecord(r->done[k], s) != cudaSuccess) return AR_ERR_CUDA;
-  if (cudaEventRecord(bk.done, s) != cudaSuccess) return AR_ERR_CUDA;
-  r->used[k] = true;
-  bk.launched = true;
-  return AR_OK;
+  return note_launched(r, {b}, k, s);
 }
 
 void note_stream(ar_reducer_s::Bucket& bk, cudaStream_t s) {
@@ -169,44 +248,29 @@ void start_group(SegTable<CapLarge>& g, const SegTable<Cap>& src) {
   g.tile0[0] = 0;
 }
 
-// One launch of the combined table of buckets bs, on the next stream,
-// after the work of every stream that marked one of their tensors.
-ar_status_t launch_group(ar_reducer_s* r, const std::vector<int>& bs) {
-  const int k = r->next;
-  r->next ^= 1;
-  cudaStream_t s = r->streams[k];
-  std::vector<cudaStream_t> waited;
-  for (int b : bs)
-    for (cudaStream_t ms : r->buckets[b].mark_streams) {
-      bool seen = false;
-      for (cudaStream_t x : waited) seen = seen || x == ms;
-      if (seen) continue;
-      waited.push_back(ms);
-      if (cudaEventRecord(r->join, ms) != cudaSuccess) return AR_ERR_CUDA;
-      if (cudaStreamWaitEvent(s, r->join, 0) != cudaSuccess) return AR_ERR_CUDA;
-    }
-  ar_status_t st = run_reduce(r->comm, r->dtype, r->sgd, r->group, s);
+// One launch of the combined table of buckets bs.
+ar_status_t launch_group(ar_reducer_s* r, const std::vector<int>& bs, const Target& tg) {
+  int k = -1;
+  cudaStream_t s = nullptr;
+  ar_status_t st = launch_stream(r, tg, bs, &k, &s);
+  if (st != AR_OK) return st;
+  st = run_reduce(r->comm, r->dtype, r->sgd, r->group, s);
   if (st != AR_OK) return st;
   if (r->group.ntiles > 0) ++r->launches;
-  if (cudaEventRecord(r->done[k], s) != cudaSuccess) return AR_ERR_CUDA;
-  for (int b : bs) {
-    if (cudaEventRecord(r->buckets[b].done, s) != cudaSuccess) return AR_ERR_CUDA;
-    r->buckets[b].launched = true;
-  }
-  r->used[k] = true;
-  return AR_OK;
+  return note_launched(r, bs, k, s);
 }
 
 // Launch the buckets that one call completed, in completion order:
 // consecutive buckets with a single launch table each share one launch of
 // their combined table while it fits; any other bucket launches alone.
 ar_status_t launch_ready(ar_reducer_s* r, const std::vector<int>& ready) {
-  if (ready.size() == 1) return launch_bucket(r, ready.front());
+  const Target tg = pick_target(r, ready);
+  if (ready.size() == 1) return launch_bucket(r, ready.front(), tg);
   std::vector<int> group;
   auto flush = [&]() -> ar_status_t {
     ar_status_t st = AR_OK;
-    if (group.size() == 1) st = launch_bucket(r, group.front());
-    else if (!group.empty()) st = launch_group(r, group);
+    if (group.size() == 1) st = launch_bucket(r, group.front(), tg);
+    else if (!group.empty()) st = launch_group(r, group, tg);
     group.clear();
     return st;
   };
@@ -215,7 +279,7 @@ ar_status_t launch_ready(ar_reducer_s* r, const std::vector<int>& ready) {
     const bool single = bk.small.size() + bk.large.size() == 1;
     if (!single) {
       ar_status_t st = flush();
-      if (st == AR_OK) st = launch_bucket(r, b);
+      if (st == AR_OK) st = launch_bucket(r, b, tg);
       if (st != AR_OK) return st;
       continue;
     }
@@ -353,7 +417,7 @@ ar_status_t ar_reducer_mark_ready(ar_reducer_t r, int tensor, ar_stream_t stream
   r->marked[tensor] = 1;
   ar_reducer_s::Bucket& bk = r->buckets[r->bucket_of[tensor]];
   note_stream(bk, static_cast<cudaStream_t>(stream));
-  if (--bk.pending == 0) return launch_bucket(r, r->bucket_of[tensor]);
+  if (--bk.pending == 0) return launch_ready(r, {r->bucket_of[tensor]});
   return AR_OK;
 }
 
@@ -400,26 +464,37 @@ ar_status_t ar_reducer_finalize(ar_reducer_t r, ar_stream_t stream) {
   ar_status_t st = rest.empty() ? AR_OK : launch_ready(r, rest);
   for (int k = 0; k < 2 && st == AR_OK; ++k)
     if (r->used[k] && cudaStreamWaitEvent(s, r->done[k], 0) != cudaSuccess) st = AR_ERR_CUDA;
+  if (st == AR_OK && r->direct && r->direct_stream != s &&
+      (cudaEventRecord(r->join, r->direct_stream) != cudaSuccess ||
+       cudaStreamWaitEvent(s, r->join, 0) != cudaSuccess))
+    st = AR_ERR_CUDA;
   for (auto& bk : r->buckets) {
     bk.pending = int(bk.tensors.size());
     bk.launched = false;
+    bk.direct = false;
     bk.mark_streams.clear();
   }
   std::fill(r->marked.begin(), r->marked.end(), 0);
   r->used[0] = r->used[1] = false;
+  r->direct = false;
   return st;
 }
 
 ar_status_t ar_reducer_wait_bucket(ar_reducer_t r, int bucket, ar_stream_t stream) {
   if (!reducer_live(r) || !is_live(r->comm)) return AR_ERR_STATE;
   if (bucket < 0 || bucket >= int(r->buckets.size())) return AR_ERR_INVALID_ARG;
-  if (!r->buckets[bucket].launched) return AR_ERR_STATE;
+  const ar_reducer_s::Bucket& bk = r->buckets[bucket];
+  if (!bk.launched) return AR_ERR_STATE;
   DeviceGuard guard(r->comm->device);
   if (!guard.ok()) return AR_ERR_CUDA;
-  return cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), r->buckets[bucket].done, 0) ==
-                 cudaSuccess
-             ? AR_OK
-             : AR_ERR_CUDA;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (bk.direct) {
+    // Launched on its marking stream: already ordered for that stream; any
+    // other stream waits for an event recorded there now.
+    if (bk.direct_stream == s) return AR_OK;
+    if (cudaEventRecord(bk.done, bk.direct_stream) != cudaSuccess) return AR_ERR_CUDA;
+  }
+  return cudaStreamWaitEvent(s, bk.done, 0) == cudaSuccess ? AR_OK : AR_ERR_CUDA;
 }
 
 ar_status_t ar_reducer_set_sgd(ar_reducer_t r, float lr, float momentum) {

@@ -311,6 +311,10 @@ ar_status_t ar_reducer_create(ar_reducer_t *reducer, ar_comm_t comm, const ar_bu
  * marked, that bucket's kernel is launched on a communication stream,
  * ordered after every stream that marked one of its tensors (consecutive
  * buckets alternate between the two streams and may overlap on the GPU).
+ * Exception: a call that completes every bucket of the step when every
+ * tensor of the step was marked on one stream launches on that stream
+ * itself (nothing of the step is left to overlap with; consecutive steps
+ * on one stream then chain without events between their kernels).
  * AR_ERR_INVALID_ARG for an index out of range; AR_ERR_STATE for a tensor
  * already marked in this step.
  */
@@ -324,15 +328,17 @@ ar_status_t ar_reducer_mark_ready(ar_reducer_t reducer, int tensor, ar_stream_t 
  * whose combined segment table fits one launch (<= 256 tensors, <= 2048
  * replica pointers) share a single kernel launch, with the same results
  * and every bucket's completion (ar_reducer_wait_bucket) recorded after
- * it. */
+ * it.  Launched on the communication streams, or on `stream` itself as
+ * for ar_reducer_mark_ready. */
 ar_status_t ar_reducer_mark_ready_many(ar_reducer_t reducer, const int *tensors, int n,
                                        ar_stream_t stream);
 
 /*
  * End of the step: launches every bucket not launched yet (its unmarked
- * tensors are taken as ready on `stream`; combined launches as in
- * ar_reducer_mark_ready_many), makes `stream` wait for all the step's
- * buckets (no host blocking), and clears the marks for the next step.
+ * tensors are taken as ready on `stream`; combined launches and the
+ * choice of stream as in ar_reducer_mark_ready_many), makes `stream` wait
+ * for all the step's buckets (no host blocking), and clears the marks for
+ * the next step.
  */
 ar_status_t ar_reducer_finalize(ar_reducer_t reducer, ar_stream_t stream);
 

@@ -417,3 +417,90 @@ def test_reducer_launch_count():
     for _ in range(3):
         host = oracle.all_reduce(host, op=oracle.SUM)
     assert_bits_equal(to_np(flat[2]), host[2], "three Sum steps")
+
+
+def test_reducer_step_marked_on_one_stream_launches_there():
+    """Every tensor marked in one call on a side stream (after a slow
+    producer on that stream): the buckets launch on that stream itself.  The
+    caller's stream at finalize, and a third stream through wait_bucket,
+    still see the results; the next step, marked tensor by tensor on the
+    communication-stream path, follows it correctly."""
+    P = 4
+    numels = [1 << 20, 3, 4097, 1 << 21, 768, 1 << 19]
+    offs = np.concatenate([[0], np.cumsum(numels)])
+    n = int(offs[-1])
+    src = [torch.empty(n, dtype=torch.float32, device=dev()) for _ in range(P)]
+    for r, x in enumerate(src):
+        wgpu.fill(x, "uniform", 80 + r)
+    flat = [torch.zeros(n, dtype=torch.float32, device=dev()) for _ in range(P)]
+    grads = [[g[offs[t]:offs[t + 1]] for g in flat] for t in range(len(numels))]
+    torch.cuda.synchronize()
+    comm = gar.ar_init(P, 0, gar.AR_SUM)
+    red = gar.Reducer(comm, grads, numels, gar.AR_F32, 8 << 20, gar.AR_SUM)
+    prod, other = torch.cuda.Stream(), torch.cuda.Stream()
+    main = torch.cuda.current_stream()
+    try:
+        bucket_of = red.bucket_of()
+        assert len(set(bucket_of)) >= 2
+        with torch.cuda.stream(prod):
+            torch.cuda._sleep(2_000_000)
+            for r in range(P):
+                flat[r].copy_(src[r])
+        red.mark_ready_many(list(range(len(numels) - 1, -1, -1)), prod)
+        assert red.launches() == 1
+        b0 = bucket_of[0]
+        red.wait_bucket(b0, other)
+        with torch.cuda.stream(other):
+            got = flat[1][offs[0]:offs[1]].clone()
+        red.finalize(main)
+        out = [x.clone() for x in flat]              # on the main stream, after finalize
+        for t in range(len(numels) - 1, -1, -1):     # second step: one bucket per launch
+            red.mark_ready(t, main)
+        red.finalize(main)
+        out2 = [x.clone() for x in flat]
+        torch.cuda.synchronize()
+        assert red.launches() == 1 + len(set(bucket_of))
+        assert gar.ar_get_async_error(comm) == gar.AR_OK
+    finally:
+        red.destroy()
+        gar.ar_destroy(comm)
+    want = oracle.all_reduce(host_replicas(P, n, "f32", "uniform", 80), op=oracle.SUM)
+    assert_bits_equal(to_np(got), want[1][offs[0]:offs[1]], "copied after wait_bucket")
+    for r in range(P):
+        assert_bits_equal(to_np(out[r]), want[r], f"step 1 rank {r}")
+    want2 = oracle.all_reduce([w.copy() for w in want], op=oracle.SUM)
+    for r in range(P):
+        assert_bits_equal(to_np(out2[r]), want2[r], f"step 2 rank {r}")
+
+
+def test_reducer_steps_on_one_stream_chain_with_sgd():
+    """Four Mean + SGD steps each marked in one call and finalized on the
+    same stream, no synchronisation between them (consecutive steps' kernels
+    follow each other on that stream): the oracle's bits after four steps."""
+    P = 8
+    numels, offs = _vit_prefix(3_000_000)
+    n = int(offs[-1])
+    flat, w, v, grads, ws, vs = _setup(P, numels, offs, seed=150)
+    comm = gar.ar_init(P, 0, gar.AR_MEAN)
+    red = gar.Reducer(comm, grads, numels, gar.AR_BF16, 1 << 20, gar.AR_MEAN,
+                      sgd=(0.1, 0.9, ws, vs, 1))
+    order = list(range(len(numels) - 1, -1, -1))
+    s = torch.cuda.Stream()
+    try:
+        for _ in range(4):
+            red.mark_ready_many(order, s)
+            red.finalize(s)
+        torch.cuda.synchronize()
+        assert gar.ar_get_async_error(comm) == gar.AR_OK
+    finally:
+        red.destroy()
+        gar.ar_destroy(comm)
+    host = host_replicas(P, n, "bf16", "normal", 150, std=1e-3)
+    hw = [workloads.normal_f32(200, n, std=0.02)]
+    hv = [np.zeros(n, np.float32)]
+    for _ in range(4):
+        oracle.bucket_all_reduce([host], op=oracle.MEAN, sgd=(0.1, 0.9, hw, hv, 1))
+    assert_bits_equal(to_np(w), hw[0], "master")
+    assert_bits_equal(to_np(v), hv[0], "momentum")
+    for r in (0, 3, P - 1):
+        assert_bits_equal(to_np(flat[r]), host[r], f"grad {r}")
