@@ -693,7 +693,8 @@ ar_status_t ar_syncbn_stats(ar_comm_t comm, const float* const* sum, const float
     a.mean[r] = mean[r];
     a.invstd[r] = invstd[r];
   }
-  a.n = double(n);
+  a.n = double(n);  // exact: n <= 2^53
+  a.rn = 1.0 / a.n;  // the IEEE quotient, rounded to nearest
   a.eps = double(eps);
   a.channels = channels;
   a.np = P;

@@ -129,60 +129,51 @@ cudaError_t launch_wait_selftest(cudaStream_t stream, uint32_t* status, uint64_t
 // operations, written rounded to fp32 to every rank.
 //
 // The call is latency-bound: a few KB of inputs, and per channel a chain of
-// fp64 conversions, adds, three divisions and a square root on GB300's
-// narrow fp64 pipe, with one warp per scheduler and nothing to hide it.  A
-// warp's time is its instruction count times the chain's latency, so the
-// work of one channel is spread over a group of L lanes (L = P rounded up to
-// a power of two): lane k of the group loads, and at the end stores, rank
-// k's values, and every lane of the group receives all ranks' values by
-// shuffles and runs the same rank-ordered adds and the same division chain
-// (identical bits in every lane).  With one thread per channel doing all
-// of it, a warp at P = 8 executed 484 instructions at 14 cycles each.
-// The kernel is specialised on the rank count NP: exactly NP - 1 adds per
-// sum.  Warps take 32 / L channels each, four warps to a CTA.
-constexpr int kSyncBnThreads = 128;
-
-__host__ __device__ constexpr int syncbn_group(int np) {
-  return np <= 1 ? 1 : np <= 2 ? 2 : np <= 4 ? 4 : np <= 8 ? 8 : 16;
-}
+// dependent fp64 operations.  On GB300 every fp64 warp instruction takes
+// about 64 cycles whatever the number of active lanes, and an SM issues one
+// every 19 cycles for all its warps, so the kernel keeps the fp64 work per
+// channel short and spreads the channels thin:
+// - one lane per channel, so a warp instruction serves 32 channels, and
+//   one-warp CTAs, so the warps spread over the SMs (with a group of lanes
+//   per channel running the same chain, the SMs' fp64 units were the
+//   bottleneck);
+// - the two divisions by the pooled count by Markstein's correction with
+//   the host's RN(1/n) (div_count: five dependent fp64 operations against
+//   the IEEE division's ~560 cycles).
+// The rank-ordered adds, the square root and the reciprocal are the IEEE
+// operations.  The kernel is specialised on the rank count NP.
+constexpr int kSyncBnThreads = 32;
 
 template <int NP>
 __global__ void __launch_bounds__(kSyncBnThreads) k_syncbn_stats(const __grid_constant__ SyncBnArgs a) {
-  constexpr int L = syncbn_group(NP);    // lanes per channel
-  constexpr int CPW = 32 / L;            // channels per warp
   griddep_launch_dependents();
   GAR_CHECK(a.np == NP, a.status);
-  const int lane = int(threadIdx.x & 31u);
-  const int k = lane % L;                // the rank this lane loads and stores
-  const int g0 = lane - k;               // first lane of the group
-  const uint64_t warp = (uint64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const uint64_t nwarps = uint64_t(gridDim.x) * blockDim.x >> 5;
-  for (uint64_t base = warp * CPW; base < a.channels; base += nwarps * CPW) {
-    const uint64_t c = base + uint64_t(lane / L);
-    const bool mine = k < NP && c < a.channels;
-    GAR_CHECK(!mine || c < a.channels, a.status);
-    const float* p1 = a.sum[k < NP ? k : 0];
-    const float* p2 = a.sqsum[k < NP ? k : 0];
-    griddep_wait();  // the parameter reads above overlap the previous kernel's drain
-    double x1 = 0.0, x2 = 0.0;
-    if (mine) {
-      x1 = double(__ldg(p1 + c));
-      x2 = double(__ldg(p2 + c));
+  const uint64_t stride = uint64_t(gridDim.x) * blockDim.x;
+  uint64_t c = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  griddep_wait();
+  for (; c < a.channels; c += stride) {
+    float x1[NP], x2[NP];
+#pragma unroll
+    for (int r = 0; r < NP; ++r) {
+      x1[r] = __ldg(a.sum[r] + c);
+      x2[r] = __ldg(a.sqsum[r] + c);
     }
-    double s1 = __shfl_sync(0xFFFFFFFFu, x1, g0), s2 = __shfl_sync(0xFFFFFFFFu, x2, g0);
+    double s1 = double(x1[0]), s2 = double(x2[0]);
 #pragma unroll
     for (int r = 1; r < NP; ++r) {
-      s1 = __dadd_rn(s1, __shfl_sync(0xFFFFFFFFu, x1, g0 + r));
-      s2 = __dadd_rn(s2, __shfl_sync(0xFFFFFFFFu, x2, g0 + r));
+      s1 = __dadd_rn(s1, double(x1[r]));
+      s2 = __dadd_rn(s2, double(x2[r]));
     }
-    const double m = __ddiv_rn(s1, a.n);
-    const double var = __dsub_rn(__ddiv_rn(s2, a.n), __dmul_rn(m, m));
+    const double m = div_count(s1, a.n, a.rn);
+    const double var = __dsub_rn(div_count(s2, a.n, a.rn), __dmul_rn(m, m));
     // 1 / sqrt(var + eps): the correctly rounded reciprocal is the IEEE
     // quotient 1 / x, by a shorter sequence than the general division.
     const double is = __drcp_rn(__dsqrt_rn(__dadd_rn(var, a.eps)));
-    if (mine) {
-      a.mean[k][c] = __double2float_rn(m);
-      a.invstd[k][c] = __double2float_rn(is);
+    const float mf = __double2float_rn(m), isf = __double2float_rn(is);
+#pragma unroll
+    for (int r = 0; r < NP; ++r) {
+      a.mean[r][c] = mf;
+      a.invstd[r][c] = isf;
     }
   }
 }
@@ -190,10 +181,8 @@ __global__ void __launch_bounds__(kSyncBnThreads) k_syncbn_stats(const __grid_co
 template <int NP>
 static cudaError_t launch_syncbn_np(const LaunchCtx& ctx, const SyncBnArgs& args) {
   if (args.np != NP) return launch_syncbn_np<NP - 1>(ctx, args);
-  constexpr uint64_t kCpw = 32 / syncbn_group(NP);
-  const uint64_t warps = (args.channels + kCpw - 1) / kCpw;
-  const uint64_t blocks = (warps + kSyncBnThreads / 32 - 1) / (kSyncBnThreads / 32);
-  const uint64_t cap = uint64_t(ctx.num_sms) * 8;
+  const uint64_t blocks = (args.channels + kSyncBnThreads - 1) / kSyncBnThreads;
+  const uint64_t cap = uint64_t(ctx.num_sms) * 16;
   const unsigned grid = unsigned(blocks < cap ? blocks : cap);
   if (grid == 0) return cudaSuccess;
   return launch_ex(ctx, &k_syncbn_stats<NP>, grid, kSyncBnThreads, 0, args);

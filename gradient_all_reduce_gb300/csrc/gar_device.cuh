@@ -350,4 +350,28 @@ __device__ __forceinline__ void sgd_step(float g, float lr, float mu, float& w, 
   w = __fsub_rn(w, __fmul_rn(lr, v));
 }
 
+// ---------------------------------------------------------------------------
+// The SyncBN statistics' division by the pooled count.  On GB300 a dependent
+// fp64 warp instruction takes about 64 cycles and the IEEE division about
+// 560.
+
+// s / n rounded to nearest even, for n an integer count (1 <= n <= 2^53)
+// and y = RN(1/n), by Markstein's correction applied twice (P. W.
+// Markstein, IBM J. Res. Develop. 34(1), 1990).  q0 = RN(s y) lies within
+// two ulps of s/n; one correction, q1 = RN(q0 + y RN(s - q0 n)), lands
+// within half an ulp plus 2^-51 ulp, so q1 is one of the two fp64 numbers
+// around s/n.  For such a q1 the residual s - q1 n is exact (one FMA), and
+// with y within half an ulp of 1/n, RN(q1 + y (s - q1 n)) is RN(s/n).  No
+// step underflows or overflows for the sums this serves (|s| >= 2^-149
+// unless zero, |s| < 2^133).  Zero (whose sign the correction would lose),
+// infinity and NaN take the IEEE division.
+__device__ __forceinline__ double div_count(double s, double n, double y) {
+  if (s == 0.0 || !(fabs(s) < __longlong_as_double(0x7FF0000000000000ll))) return __ddiv_rn(s, n);
+  double q = __dmul_rn(s, y);
+  double r = __fma_rn(-q, n, s);
+  q = __fma_rn(r, y, q);
+  r = __fma_rn(-q, n, s);
+  return __fma_rn(r, y, q);
+}
+
 }  // namespace gar

@@ -96,6 +96,7 @@ struct SyncBnArgs {
   float* mean[kMaxRanks];         // outputs, every rank
   float* invstd[kMaxRanks];
   double n;                       // total values per channel over all ranks
+  double rn;                      // RN(1 / n)
   double eps;
   uint64_t channels;
   int np;

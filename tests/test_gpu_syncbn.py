@@ -97,3 +97,52 @@ def test_prepared_syncbn_equals_direct_call():
     for k in range(2):
         for r in range(P):
             assert_bits_equal(to_np(prepared[k][r]), to_np(direct[k][r]), f"output {k} rank {r}")
+
+
+@pytest.mark.parametrize("P", [2, 3, 8, 16])
+def test_syncbn_stats_hard_inputs_equal_oracle(P):
+    """Channels chosen to stress the kernel's sums and divisions: ranks'
+    sums whose exponents lie close together or far apart, zeros of both
+    signs, ranks that cancel exactly, subnormal sums, infinities and NaNs
+    (which take the IEEE division), and a pooled count with many significant
+    bits; every output against the oracle."""
+    C = 4099
+    rng = np.random.default_rng(900 + P)
+    counts = [int(c) for c in rng.integers(1, 1 << 40, size=P)]
+    spread = rng.integers(0, 80, size=C)
+    sums, sq = [], []
+    for r in range(P):
+        mant = rng.uniform(1, 2, size=C) * rng.choice([-1.0, 1.0], size=C)
+        expo = rng.integers(-20, 20, size=C) + (rng.integers(0, 1 << 30, size=C) % (spread + 1))
+        sums.append(np.float32(np.ldexp(mant, expo)))
+        sq.append(np.float32(np.ldexp(rng.uniform(1, 2, size=C), expo + 2)))
+    sums, sq = np.stack(sums), np.stack(sq)
+    sums[:, 0:40] = 0.0
+    sums[:, 0:20] = -0.0
+    sums[0, 20:30] = -0.0
+    for r in range(1, P, 2):                    # rank r cancels rank r - 1
+        sums[r, 40:80] = -sums[r - 1, 40:80]
+    sums[:, 80:100] = np.float32(1e-45) * rng.integers(-3, 4, size=(P, 20))
+    sums[P - 1, 100] = np.inf
+    sums[0, 101] = -np.inf
+    sums[P - 1, 102] = np.nan
+    sq[0, 103] = np.inf
+    sq[P - 1, 104] = np.nan
+    sums[0, 105], sums[P - 1, 105] = np.inf, -np.inf
+    sums, sq = [np.ascontiguousarray(x) for x in sums], [np.ascontiguousarray(x) for x in sq]
+    d_s = [torch.from_numpy(x).to(dev()) for x in sums]
+    d_q = [torch.from_numpy(x).to(dev()) for x in sq]
+    d_m = [torch.empty(C, device=dev()) for _ in range(P)]
+    d_i = [torch.empty(C, device=dev()) for _ in range(P)]
+    comm = gar.ar_init(P, 0, gar.AR_SUM)
+    try:
+        gar.ar_syncbn_stats(comm, d_s, d_q, counts, d_m, d_i, C, 1e-5)
+        torch.cuda.synchronize()
+    finally:
+        gar.ar_destroy(comm)
+    want_m, want_i = oracle.syncbn_stats(sums, sq, counts, eps=1e-5)
+    for r in range(P):
+        for got, want, what in ((to_np(d_m[r]), want_m[r], "mean"), (to_np(d_i[r]), want_i[r], "invstd")):
+            nan = np.isnan(want)
+            assert np.array_equal(nan, np.isnan(got)), f"{what} {r}: NaN positions"
+            assert_bits_equal(got[~nan], want[~nan], f"{what} {r}")
