@@ -246,7 +246,7 @@ class VitStep:
             self.numels, gar.AR_BF16, CAP, gar.AR_MEAN,
             sgd=(0.1, 0.9, [self.w[o[t]:o[t + 1]] for t in range(len(self.numels))],
                  [self.v[o[t]:o[t + 1]] for t in range(len(self.numels))], 1))
-        self.reverse = list(range(len(self.numels) - 1, -1, -1))
+        self.reverse = self.reducer.marks(range(len(self.numels) - 1, -1, -1))
 
     def step(self, stream):
         """One step through the reducer: every gradient marked ready in
@@ -332,15 +332,17 @@ def time_vit(args, device, stream, world):
     try:
         vs = VitStep(comm, device)
         K = args.steps
-        with torch.cuda.stream(stream):
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # The clock sampler starts first (it takes a moment to produce
+        # samples), so that the warm-up steps, not an idle GPU, come right
+        # before the timed region.
+        with ClockSampler(device.index) as clocks, torch.cuda.stream(stream):
             for _ in range(args.warmup):
                 vs.step(stream)
-        torch.cuda.synchronize(device)
-        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier(world)
-        torch.cuda.synchronize(device)
-        launches0 = vs.reducer.launches()
-        with ClockSampler(device.index) as clocks, torch.cuda.stream(stream):
+            torch.cuda.synchronize(device)
+            barrier(world)
+            torch.cuda.synchronize(device)
+            launches0 = vs.reducer.launches()
             start.record(stream)
             for _ in range(K):
                 vs.step(stream)

@@ -362,17 +362,25 @@ class Reducer:
                                 ctypes.byref(s) if s is not None else None), "ar_reducer_create")
         self.handle = int(h.value)
         self._mark = L.ar_reducer_mark_ready
+        self._mark_many = L.ar_reducer_mark_ready_many
+        self._finalize = L.ar_reducer_finalize
 
     def mark_ready(self, tensor: int, stream=None) -> None:
         _ok(self._mark(self.handle, int(tensor), _stream(stream)), "ar_reducer_mark_ready")
 
-    def mark_ready_many(self, tensors: Sequence[int], stream=None) -> None:
-        arr = (ctypes.c_int * max(len(tensors), 1))(*[int(t) for t in tensors])
-        _ok(load().ar_reducer_mark_ready_many(self.handle, arr, len(tensors), _stream(stream)),
+    def marks(self, tensors: Sequence[int]) -> ctypes.Array:
+        """A list of tensor indices marshalled once, for a mark_ready_many
+        call repeated every step (the library still checks every index)."""
+        return (ctypes.c_int * len(tensors))(*[int(t) for t in tensors])
+
+    def mark_ready_many(self, tensors, stream=None) -> None:
+        """``tensors``: indices, or the array ``marks`` made of them."""
+        arr = tensors if isinstance(tensors, ctypes.Array) else self.marks(tensors)
+        _ok(self._mark_many(self.handle, arr, len(arr), _stream(stream)),
             "ar_reducer_mark_ready_many")
 
     def finalize(self, stream=None) -> None:
-        _ok(load().ar_reducer_finalize(self.handle, _stream(stream)), "ar_reducer_finalize")
+        _ok(self._finalize(self.handle, _stream(stream)), "ar_reducer_finalize")
 
     def wait_bucket(self, bucket: int, stream=None) -> None:
         _ok(load().ar_reducer_wait_bucket(self.handle, int(bucket), _stream(stream)),
