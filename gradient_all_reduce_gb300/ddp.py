@@ -70,6 +70,7 @@ class ReplicaDDP:
         for t in range(len(self.params) - 1, -1, -1):      # the order gradients become final
             self._bucket_tensors[self._bucket_of[t]].append(t)
         self._pending = [len(ts) for ts in self._bucket_tensors]
+        self._bucket_marks = [self.reducer.marks(ts) for ts in self._bucket_tensors]
         self.hooks_enabled = True
         self._stream = None          # handle of the stream the current backward runs on
         self._handles = []
@@ -85,7 +86,7 @@ class ReplicaDDP:
                     self._stream = torch.cuda.current_stream().cuda_stream
                 self._pending[b] -= 1
                 if self._pending[b] == 0:
-                    self.reducer.mark_ready_many(self._bucket_tensors[b], self._stream)
+                    self.reducer.mark_ready_many(self._bucket_marks[b], self._stream)
         return hook
 
     def replica_grad(self, rank: int, t: int) -> torch.Tensor:
