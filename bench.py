@@ -421,7 +421,7 @@ class E2EStep:
         # copy-out.
         self.event_stream = torch.cuda.Stream(device)
         o = vs.offs
-        self.spans = [(int(o[min(b)]), int(o[max(b) + 1]), b) for b in vs.buckets]
+        self.spans = [(int(o[min(b)]), int(o[max(b) + 1]), vs.reducer.marks(b)) for b in vs.buckets]
         self.kernel_done = [torch.cuda.Event() for _ in self.spans]
         self.out_done = [torch.cuda.Event() for _ in self.spans]
 
