@@ -317,11 +317,16 @@ def time_vit(args, device, stream, world):
     vs = None
 
     def region(fn):
+        """K calls of fn back to back under one event pair.  One untimed call
+        is queued first, so the timed calls find the GPU busy: the host's
+        time to issue the first call, with the GPU idle, is not counted as
+        kernel time."""
         with torch.cuda.stream(stream):
             for _ in range(args.warmup):
                 fn(stream)
             torch.cuda.synchronize(device)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            fn(stream)
             e0.record(stream)
             for _ in range(K):
                 fn(stream)
@@ -1490,8 +1495,9 @@ def main():
                                 "buckets' 152 tensors (4.155 GB)"),
                      "note": ("the kernel the reducer launches in the headline region, issued "
                               "K times back to back on the timing stream under one CUDA-event "
-                              "pair (second timed region): region time / K = average launch "
-                              "duration"),
+                              "pair (second timed region), behind one untimed launch so that "
+                              "the host's first issue is not counted: region time / K = "
+                              "average launch duration"),
                      "achieved_per_bucket_launch": per_bucket,
                      "frac_per_bucket_launch": per_bucket / peak,
                      "per_bucket_note": ("the 8 bucket calls one after another on one stream "
