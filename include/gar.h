@@ -345,9 +345,11 @@ ar_status_t ar_reducer_finalize(ar_reducer_t reducer, ar_stream_t stream);
 /*
  * Makes `stream` wait (no host blocking) for bucket `bucket` of the current
  * step -- e.g. to copy that bucket's results out while later buckets are
- * still being produced (DDP's per-bucket completion).  AR_ERR_STATE if the
- * bucket has not been launched in this step; AR_ERR_INVALID_ARG for an
- * index outside 0 .. nbuckets-1 (see ar_reducer_info).
+ * still being produced (DDP's per-bucket completion).  For a bucket
+ * launched on its marking stream (see ar_reducer_mark_ready) the wait
+ * covers that stream's work up to this call.  AR_ERR_STATE if the bucket
+ * has not been launched in this step; AR_ERR_INVALID_ARG for an index
+ * outside 0 .. nbuckets-1 (see ar_reducer_info).
  */
 ar_status_t ar_reducer_wait_bucket(ar_reducer_t reducer, int bucket, ar_stream_t stream);
 
