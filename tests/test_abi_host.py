@@ -93,3 +93,25 @@ def test_no_alloc_entry_point_source_allocates_nothing():
     section = re.sub(r"//[^\n]*", "", section)   # the comments explain why; check the code
     for word in ("cudaMalloc", "cudaFree", "cudaHostAlloc", "cudaMallocAsync", "new ", "malloc("):
         assert word not in section, word
+
+
+def test_reducer_marks_pass_the_indices_and_their_count(gar):
+    """Reducer.mark_ready_many passes the indices and their number, whether
+    it gets a list or the array Reducer.marks made once (checked against a
+    stand-in for the library call, no GPU)."""
+    r = object.__new__(gar.Reducer)
+    r.handle = 1234
+    seen = []
+
+    def call(handle, arr, n, stream):
+        seen.append((handle, [arr[i] for i in range(n)], n, stream))
+        return gar.AR_OK
+
+    r._mark_many = call
+    prepared = r.marks(range(5, 2, -1))
+    r.mark_ready_many(prepared, 7)
+    r.mark_ready_many(prepared, 7)
+    r.mark_ready_many([2, 0], 7)
+    r.mark_ready_many([], 7)
+    assert seen == [(1234, [5, 4, 3], 3, 7), (1234, [5, 4, 3], 3, 7), (1234, [2, 0], 2, 7),
+                    (1234, [], 0, 7)]
